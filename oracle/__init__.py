@@ -1,0 +1,258 @@
+"""CPU oracle for the forward 2D convolution and its two re-layouts.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  The GPU library
+never imports, links or runs anything here, and nothing here imports the GPU
+library: the two sides share only the seeded input generators of
+``workloads.py``, which hold none of the method's arithmetic.
+
+Functions and the passages they follow
+--------------------------------------
+``output_size``
+    Output extent along one axis, floor((L + 2p - d(K-1) - 1)/s) + 1.
+    "Unifying Convolutions and GEMM", section 5 prints (H + 2p - K)//s + 1;
+    the dilated form reduces to it at d = 1.
+``conv2d_direct`` / ``conv2d_points``
+    The naive 7-loop convolution ("Unifying Convolutions and GEMM",
+    section 1) with zero padding and bias (section 5) and dilation ("The
+    Indirect Convolution Algorithm", Abstract), in fp64 C (conv_oracle.c).
+``conv2d_im2col_gemm``
+    The second route the tutorial gives: im2col (section 2) then the GEMM
+    Y_col = X_col W_row^T (section 3), then bias and reshape (section 5).
+    fp64 numpy; used to pin the direct oracle on small inputs.
+``im2win``
+    Window-order re-layout ("Im2win: An Efficient Convolution Paradigm on
+    GPU", Abstract).  The abstract gives no layout; the reading used is
+    Win[n][ho][wc][kh][ci] = X[n][ho*s + kh*d - p][wc - p][ci] (zero outside),
+    wc in [0, W_used), W_used = (W_out - 1)s + (KW - 1)d + 1, so the window
+    of every output pixel of row ho is one contiguous run of Win.
+``indirection_buffer``
+    The indirection buffer ("The Indirect Convolution Algorithm", Abstract:
+    a buffer of pointers to the start of each row of image pixels).  Reading:
+    one entry per (output pixel, tap), holding the element offset
+    ((h*W) + w)*C_in of that input pixel's C_in-vector within one image, or
+    -1 where the tap falls in the zero padding; batch-independent, laid out
+    [H_out*W_out][KH*KW].
+``im2col_elements`` / ``im2win_elements``
+    Footprints the workspace claim is judged against (section 2: X_col has
+    (N*H_out*W_out) x (C_in*KH*KW) entries).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against things
+other than itself: torch's CPU conv2d in fp64, closed forms, invariants the
+pages state (1x1 stride-1 convolution is a GEMM; a kernel covering the whole
+image is a dense layer) and brute force on tiny inputs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "conv_oracle.c")
+_LIB = os.path.join(_HERE, "_liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile conv_oracle.c into oracle/_liboracle.so with gcc (OpenMP if available)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".tmp%d" % os.getpid()
+    base = ["gcc", "-O2", "-shared", "-fPIC", "-std=c99", _SRC, "-o", tmp]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        L, P = ctypes.c_long, ctypes.c_void_p
+        lib.oracle_output_size.argtypes = [L] * 5
+        lib.oracle_output_size.restype = L
+        lib.oracle_conv2d_direct.argtypes = [P, P, P] + [L] * 10 + [P, P]
+        lib.oracle_conv2d_direct.restype = ctypes.c_int
+        lib.oracle_conv2d_points.argtypes = [P, P, P] + [L] * 10 + [P, L, P, P]
+        lib.oracle_conv2d_points.restype = ctypes.c_int
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """Host threads the C oracle's parallel loops use."""
+    return int(_load().oracle_num_threads())
+
+
+def output_size(L: int, K: int, s: int, p: int, d: int = 1) -> int:
+    """floor((L + 2p - d(K-1) - 1)/s) + 1, or 0 when the window does not fit."""
+    return int(_load().oracle_output_size(L, K, s, p, d))
+
+
+def _bits(a, name):
+    """Raw bf16 bit patterns as a C-contiguous uint16 array (torch or numpy input)."""
+    if a is None:
+        return None
+    if hasattr(a, "view") and hasattr(a, "dtype") and "bfloat16" in str(a.dtype):
+        import torch  # only reached when a torch bf16 tensor is passed
+        a = a.detach().contiguous().view(torch.int16).numpy().view(np.uint16)
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("%s must hold bf16 bit patterns (uint16), got %s" % (name, a.dtype))
+    return a
+
+
+def conv2d_direct(x, w, bias, stride: int, pad: int, dilation: int = 1):
+    """Direct convolution in fp64.
+
+    x: bf16 bits [N][H][W][C_in]; w: bf16 bits [C_out][KH][KW][C_in];
+    bias: bf16 bits [C_out] or None.  Returns (y, bound), both float64
+    [N][H_out][W_out][C_out]; bound = |bias| + sum |x*w| per output.
+    """
+    x, w, b = _bits(x, "x"), _bits(w, "w"), _bits(bias, "bias")
+    N, H, W, C_in = x.shape
+    C_out, KH, KW, C_in2 = w.shape
+    if C_in2 != C_in:
+        raise ValueError("channel mismatch")
+    H_out = output_size(H, KH, stride, pad, dilation)
+    W_out = output_size(W, KW, stride, pad, dilation)
+    if H_out < 1 or W_out < 1:
+        raise ValueError("empty output")
+    y = np.empty((N, H_out, W_out, C_out), np.float64)
+    mag = np.empty_like(y)
+    rc = _load().oracle_conv2d_direct(
+        x.ctypes.data, w.ctypes.data, None if b is None else b.ctypes.data,
+        N, C_in, H, W, C_out, KH, KW, stride, pad, dilation,
+        y.ctypes.data, mag.ctypes.data)
+    if rc:
+        raise ValueError("oracle rejected geometry (rc=%d)" % rc)
+    return y, mag
+
+
+def conv2d_points(x, w, bias, stride: int, pad: int, dilation: int, points):
+    """Selected outputs of the direct convolution in fp64.
+
+    points: int array [P, 4] of (n, co, ho, wo).  Returns (values, bounds), float64 [P].
+    """
+    x, w, b = _bits(x, "x"), _bits(w, "w"), _bits(bias, "bias")
+    N, H, W, C_in = x.shape
+    C_out, KH, KW, _ = w.shape
+    pts = np.ascontiguousarray(points, dtype=np.int64).reshape(-1, 4)
+    out = np.empty(len(pts), np.float64)
+    mag = np.empty_like(out)
+    rc = _load().oracle_conv2d_points(
+        x.ctypes.data, w.ctypes.data, None if b is None else b.ctypes.data,
+        N, C_in, H, W, C_out, KH, KW, stride, pad, dilation,
+        pts.ctypes.data, len(pts), out.ctypes.data, mag.ctypes.data)
+    if rc:
+        raise ValueError("oracle rejected points (rc=%d)" % rc)
+    return out, mag
+
+
+def bf16_bits_to_f64(a) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float64."""
+    a = _bits(a, "array")
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def im2col(x_f64: np.ndarray, KH: int, KW: int, stride: int, pad: int, dilation: int = 1):
+    """X_col of the tutorial's section 2, in NHWC-order rows.
+
+    x_f64: float64 [N][H][W][C_in].  Returns [N*H_out*W_out, KH*KW*C_in]: row
+    (n, ho, wo) holds that output pixel's receptive patch, column
+    (kh*KW + kw)*C_in + ci, zero where the patch leaves the image.
+    """
+    N, H, W, C = x_f64.shape
+    H_out = output_size(H, KH, stride, pad, dilation)
+    W_out = output_size(W, KW, stride, pad, dilation)
+    xp = np.zeros((N, H + 2 * pad, W + 2 * pad, C), np.float64)
+    xp[:, pad:pad + H, pad:pad + W, :] = x_f64
+    cols = np.empty((N, H_out, W_out, KH, KW, C), np.float64)
+    for kh in range(KH):
+        for kw in range(KW):
+            h0, w0 = kh * dilation, kw * dilation
+            cols[:, :, :, kh, kw, :] = xp[:, h0:h0 + stride * (H_out - 1) + 1:stride,
+                                          w0:w0 + stride * (W_out - 1) + 1:stride, :]
+    return cols.reshape(N * H_out * W_out, KH * KW * C)
+
+
+def conv2d_im2col_gemm(x, w, bias, stride: int, pad: int, dilation: int = 1):
+    """Y = X_col W_row^T + bias, reshaped to [N][H_out][W_out][C_out] (fp64)."""
+    xf = bf16_bits_to_f64(x)
+    wf = bf16_bits_to_f64(w)
+    N, H, W, _ = xf.shape
+    C_out, KH, KW, _ = wf.shape
+    H_out = output_size(H, KH, stride, pad, dilation)
+    W_out = output_size(W, KW, stride, pad, dilation)
+    X_col = im2col(xf, KH, KW, stride, pad, dilation)
+    W_row = wf.reshape(C_out, -1)
+    Y_col = X_col @ W_row.T
+    if bias is not None:
+        Y_col = Y_col + bf16_bits_to_f64(bias)[None, :]
+    return Y_col.reshape(N, H_out, W_out, C_out)
+
+
+def im2win(x, KH: int, KW: int, stride: int, pad: int, dilation: int = 1) -> np.ndarray:
+    """Window-order buffer Win[n][ho][wc][kh][ci] (bf16 bits, uint16), see module doc."""
+    x = _bits(x, "x")
+    N, H, W, C = x.shape
+    H_out = output_size(H, KH, stride, pad, dilation)
+    W_out = output_size(W, KW, stride, pad, dilation)
+    W_used = (W_out - 1) * stride + (KW - 1) * dilation + 1
+    win = np.zeros((N, H_out, W_used, KH, C), np.uint16)
+    for ho in range(H_out):
+        for kh in range(KH):
+            h = ho * stride + kh * dilation - pad
+            if h < 0 or h >= H:
+                continue
+            for wc in range(W_used):
+                w = wc - pad
+                if 0 <= w < W:
+                    win[:, ho, wc, kh, :] = x[:, h, w, :]
+    return win
+
+
+def indirection_buffer(H: int, W: int, C_in: int, KH: int, KW: int, stride: int,
+                       pad: int, dilation: int = 1) -> np.ndarray:
+    """int32 [H_out*W_out][KH*KW]: offset ((h*W)+w)*C_in of each tap's pixel, or -1."""
+    H_out = output_size(H, KH, stride, pad, dilation)
+    W_out = output_size(W, KW, stride, pad, dilation)
+    buf = np.full((H_out, W_out, KH, KW), -1, np.int64)
+    for ho in range(H_out):
+        for wo in range(W_out):
+            for kh in range(KH):
+                for kw in range(KW):
+                    h = ho * stride + kh * dilation - pad
+                    w = wo * stride + kw * dilation - pad
+                    if 0 <= h < H and 0 <= w < W:
+                        buf[ho, wo, kh, kw] = (h * W + w) * C_in
+    return buf.reshape(H_out * W_out, KH * KW).astype(np.int32)
+
+
+def im2col_elements(N, C_in, H, W, KH, KW, stride, pad, dilation=1) -> int:
+    """Entries of X_col: (N*H_out*W_out) * (C_in*KH*KW)."""
+    H_out = output_size(H, KH, stride, pad, dilation)
+    W_out = output_size(W, KW, stride, pad, dilation)
+    return N * H_out * W_out * C_in * KH * KW
+
+
+def im2win_elements(N, C_in, H, W, KH, KW, stride, pad, dilation=1) -> int:
+    """Entries of Win: N * H_out * W_used * KH * C_in."""
+    H_out = output_size(H, KH, stride, pad, dilation)
+    W_out = output_size(W, KW, stride, pad, dilation)
+    W_used = (W_out - 1) * stride + (KW - 1) * dilation + 1
+    return N * H_out * W_used * KH * C_in
+
+
+if __name__ == "__main__":  # pragma: no cover - manual build helper
+    print(build(force="--force" in sys.argv))
