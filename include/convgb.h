@@ -1,0 +1,233 @@
+/*
+ * convgb.h -- C ABI of the GB300 (sm_103a) forward-convolution library.
+ *
+ * The library computes the forward 2D convolution
+ *
+ *   Y[n,co,ho,wo] = bias[co] + sum_{ci,kh,kw} X[n,ci,ho*s+kh*d-p, wo*s+kw*d-p] * W[co,ci,kh,kw]
+ *
+ * ("Unifying Convolutions and GEMM", section 1, the 7-loop convolution; its
+ * section 5 adds zero padding and bias; "The Indirect Convolution Algorithm",
+ * Abstract, adds dilation) as an implicit GEMM of
+ *   M = N*H_out*W_out rows (output pixels), N_gemm = C_out columns,
+ *   K = KH*KW*C_in reduction
+ * ("Unifying Convolutions and GEMM", sections 2-3: Y_col = X_col * W_row^T),
+ * without ever materialising X_col (im2col).  The A operand is gathered
+ * through an indirection buffer ("The Indirect Convolution Algorithm",
+ * Abstract) straight into shared memory and fed to tcgen05 tensor-core MMA.
+ *
+ * Conventions for every entry point
+ *  - Layouts are channels-last: x is [N][H][W][C_in], w is [C_out][KH][KW][C_in],
+ *    y is [N][H_out][W_out][C_out], all dense; bias is [C_out].  Inputs are bf16
+ *    (raw 16-bit patterns); y is bf16 or fp32 (fp32 accumulation either way).
+ *  - Stride, padding and dilation are symmetric scalars: s >= 1, p >= 0, d >= 1.
+ *    H_out = floor((H + 2p - d(KH-1) - 1)/s) + 1, likewise W_out; a shape with
+ *    H_out < 1 or W_out < 1 is rejected.
+ *  - Pointers named x, w, bias, y, workspace, win, ibuf are DEVICE pointers
+ *    owned by the caller, who must keep them alive until the work queued on
+ *    `stream` has finished.  The library allocates no memory per call.
+ *    They must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  All work is queued asynchronously on it and on no other stream.
+ *  - Every argument, shape, alignment and workspace check happens before the
+ *    first launch; a failed check returns an error and queues nothing.
+ *    A failed launch returns CONVGB_ERR_CUDA.  Kernels never trap: a device-side
+ *    failure (a pipeline wait that timed out) is recorded in a device error word
+ *    that convgb_check_device_errors() reads.
+ *  - Calls on the same device may run concurrently only on distinct output and
+ *    workspace buffers.  Element counts are limited to what the int32 index
+ *    arithmetic allows: each of N*H*W*C_in, N*H_out*W_out*C_out and
+ *    C_out*KH*KW*C_in must be below 2^31.
+ */
+#ifndef CONVGB_H
+#define CONVGB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* Every entry point below is exported from libconvgb.so. */
+#if defined(__GNUC__)
+#define CONVGB_API __attribute__((visibility("default")))
+#else
+#define CONVGB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum convgb_status {
+    CONVGB_OK = 0,
+    CONVGB_ERR_INVALID_ARG = 1, /* bad shape, null pointer, unknown dtype or path */
+    CONVGB_ERR_UNSUPPORTED = 2, /* valid convolution this library does not handle */
+    CONVGB_ERR_WORKSPACE = 3,   /* workspace or output buffer smaller than required */
+    CONVGB_ERR_ALIGNMENT = 4,   /* a device pointer is not 16-byte aligned */
+    CONVGB_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+    CONVGB_ERR_INTERNAL = 6     /* device-side failure (wait timeout) reported by a kernel */
+} convgb_status;
+
+typedef enum convgb_dtype {
+    CONVGB_BF16 = 0,
+    CONVGB_F32 = 1
+} convgb_dtype;
+
+/* Kernel family conv2d_fwd_path() may be asked for; conv2d_fwd() picks one. */
+typedef enum convgb_path {
+    CONVGB_PATH_AUTO = 0,
+    CONVGB_PATH_GATHER = 1,   /* implicit GEMM, A gathered through the indirection buffer */
+    CONVGB_PATH_DENSE = 2,    /* plain GEMM: 1x1 stride-1 unpadded, or a kernel covering the
+                                 whole unpadded image (a dense layer); no workspace */
+    CONVGB_PATH_STEM = 3      /* tiny C_in (not a multiple of 8): channels padded to 8 */
+} convgb_path;
+
+/* Short English text for a status code; never NULL. */
+CONVGB_API const char* convgb_status_string(int status);
+
+/* Output extent of the convolution (the formula above).  Returns
+ * CONVGB_ERR_INVALID_ARG for a bad parameter or an empty output. */
+CONVGB_API convgb_status convgb_output_dims(int H, int W, int KH, int KW, int stride, int pad,
+                                 int dilation, int* H_out, int* W_out);
+
+/* The path conv2d_fwd() takes for this shape (a CONVGB_PATH_* value), or -1
+ * when the shape is invalid or unsupported. */
+CONVGB_API int convgb_select_path(int N, int C_in, int H, int W, int C_out, int KH, int KW,
+                       int stride, int pad, int dilation);
+
+/* Bytes of workspace conv2d_fwd() needs for this shape on the path it selects
+ * (0 for the dense path), or 0 for an invalid shape.  Always smaller than
+ * convgb_im2col_bytes() for the shapes this library accepts. */
+CONVGB_API size_t convgb_conv2d_fwd_workspace_size(int N, int C_in, int H, int W, int C_out, int KH,
+                                        int KW, int stride, int pad, int dilation);
+
+/* As above for an explicitly requested path. */
+CONVGB_API size_t convgb_conv2d_fwd_path_workspace_size(int path, int N, int C_in, int H, int W,
+                                             int C_out, int KH, int KW, int stride,
+                                             int pad, int dilation);
+
+/* Bytes an explicit bf16 im2col matrix would take: N*H_out*W_out*C_in*KH*KW*2
+ * ("Unifying Convolutions and GEMM", section 2: X_col has (N*H_out*W_out) rows
+ * of C_in*KH*KW entries).  The comparator for the workspace claim; 0 if invalid. */
+CONVGB_API size_t convgb_im2col_bytes(int N, int C_in, int H, int W, int KH, int KW, int stride,
+                           int pad, int dilation);
+
+/*
+ * conv2d_fwd -- forward convolution, y = conv(x, w) + bias.
+ *
+ * Defined by the formula at the top of this file.  Picks a path with
+ * convgb_select_path(): the indirection-buffer implicit GEMM in general, a
+ * plain GEMM for 1x1 stride-1 unpadded layers ("The Indirect Convolution
+ * Algorithm", Abstract: 1x1 convolutions are directly a GEMM) and for kernels
+ * that cover the whole unpadded image ("Unifying Convolutions and GEMM",
+ * section 4: such a convolution is a dense layer), and a channel-padding stem
+ * path when C_in is not a multiple of 8.
+ *
+ *   x         device, bf16 [N][H][W][C_in]
+ *   w         device, bf16 [C_out][KH][KW][C_in]
+ *   bias      device, bf16 [C_out], or NULL for no bias
+ *   y         device, [N][H_out][W_out][C_out] of y_dtype (CONVGB_BF16 rounds
+ *             the fp32 accumulator to nearest-even; CONVGB_F32 stores it)
+ *   workspace device scratch of at least convgb_conv2d_fwd_workspace_size()
+ *             bytes (may be NULL when that is 0); its contents on entry are
+ *             ignored and on exit are unspecified
+ * Returns CONVGB_OK once the work is queued on `stream`.
+ */
+CONVGB_API convgb_status conv2d_fwd(const void* x, const void* w, const void* bias, int N, int C_in,
+                         int H, int W, int C_out, int KH, int KW, int stride, int pad,
+                         int dilation, void* y, int y_dtype, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* conv2d_fwd on an explicitly chosen path (a CONVGB_PATH_* value; AUTO behaves
+ * like conv2d_fwd).  Returns CONVGB_ERR_UNSUPPORTED when that path cannot
+ * compute this shape.  Used to cross-check paths against each other. */
+CONVGB_API convgb_status conv2d_fwd_path(int path, const void* x, const void* w, const void* bias,
+                              int N, int C_in, int H, int W, int C_out, int KH, int KW,
+                              int stride, int pad, int dilation, void* y, int y_dtype,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * conv2d_fwd_indirect -- conv2d_fwd on the gather path with a caller-built
+ * indirection buffer, for layers whose geometry repeats across calls: build
+ * the buffer once with build_indirection_buffer() (same H, W, C_in, KH, KW,
+ * stride, pad, dilation) and pass it here; nothing else is launched.  "The
+ * Indirect Convolution Algorithm" (Abstract) builds the buffer once per
+ * layer setup in the same way.
+ *
+ *   ibuf  device, int32 [H_out*W_out][KH*KW] as written by build_indirection_buffer()
+ * Requires C_in % 8 == 0 (CONVGB_ERR_UNSUPPORTED otherwise).  Other arguments
+ * as conv2d_fwd; no workspace is needed.
+ */
+CONVGB_API convgb_status conv2d_fwd_indirect(const void* x, const void* w, const void* bias, int N,
+                                             int C_in, int H, int W, int C_out, int KH, int KW,
+                                             int stride, int pad, int dilation, const int32_t* ibuf,
+                                             size_t ibuf_bytes, void* y, int y_dtype, void* stream);
+
+/* Bytes of the indirection buffer: H_out*W_out*KH*KW*4 (0 if invalid). */
+CONVGB_API size_t convgb_indirection_buffer_bytes(int H, int W, int KH, int KW, int stride, int pad,
+                                       int dilation);
+
+/*
+ * build_indirection_buffer -- the indirection buffer of "The Indirect
+ * Convolution Algorithm" (Abstract: a buffer of pointers to the start of each
+ * row of image pixels), as int32 element offsets.
+ *
+ *   ibuf  device, int32 [H_out*W_out][KH*KW].  Entry (ho*W_out + wo, kh*KW + kw)
+ *         holds ((h*W) + w)*C_in with h = ho*s + kh*d - p, w = wo*s + kw*d - p,
+ *         the offset of that input pixel's C_in-vector inside one image, or -1
+ *         when (h, w) falls in the zero padding.  One buffer serves every image
+ *         of a batch (the image offset n*H*W*C_in is added by the consumer).
+ *   ibuf_bytes  capacity of ibuf; at least convgb_indirection_buffer_bytes().
+ * Requires H*W*C_in < 2^31.
+ */
+CONVGB_API convgb_status build_indirection_buffer(int H, int W, int C_in, int KH, int KW, int stride,
+                                       int pad, int dilation, int32_t* ibuf,
+                                       size_t ibuf_bytes, void* stream);
+
+/* Bytes of the im2win buffer: N*H_out*W_used*KH*C_in*2 with
+ * W_used = (W_out-1)*s + (KW-1)*d + 1 (0 if invalid). */
+CONVGB_API size_t convgb_im2win_bytes(int N, int C_in, int H, int W, int KH, int KW, int stride,
+                           int pad, int dilation);
+
+/*
+ * im2win_transform -- window-order re-layout of "Im2win: An Efficient
+ * Convolution Paradigm on GPU" (Abstract).  The abstract fixes no layout; this
+ * library writes
+ *
+ *   win[n][ho][wc][kh][ci] = x[n][ho*s + kh*d - p][wc - p][ci]   (0 outside the image)
+ *
+ * for wc in [0, W_used): the KH input rows that output row ho reads are
+ * interleaved column by column, so every output pixel's receptive window is
+ * one contiguous run of win (stride-1, undilated) and rows are written
+ * exactly once.  Bit-exact copy of bf16 values.
+ *
+ *   x    device, bf16 [N][H][W][C_in]
+ *   win  device, bf16, at least convgb_im2win_bytes() bytes
+ */
+CONVGB_API convgb_status im2win_transform(const void* x, int N, int C_in, int H, int W, int KH, int KW,
+                               int stride, int pad, int dilation, void* win,
+                               size_t win_bytes, void* stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns CONVGB_OK, CONVGB_ERR_INTERNAL when a kernel
+ * recorded a failure since the last call (its raw code in *code when code is
+ * not NULL), or CONVGB_ERR_CUDA when the synchronisation itself failed. */
+CONVGB_API convgb_status convgb_check_device_errors(void* stream, unsigned int* code);
+
+/* Upper bound, in nanoseconds, on any single pipeline wait inside the kernels
+ * (default 4e9).  A wait that runs past it makes the kernel record
+ * CONVGB_ERR_INTERNAL, drain its own copies and return instead of hanging.
+ * Applies to launches queued after the call, process-wide. */
+CONVGB_API void convgb_set_wait_timeout_ns(uint64_t ns);
+
+/* Failure-detection self-test: queues one tiny kernel whose mbarrier wait can
+ * never be satisfied, bounded by timeout_ns.  The kernel gives up, records the
+ * timeout in the device error word and returns; convgb_check_device_errors()
+ * then reports CONVGB_ERR_INTERNAL.  Nothing faults or traps. */
+CONVGB_API convgb_status convgb_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/* Library version, major*10000 + minor*100 + patch. */
+CONVGB_API int convgb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVGB_H */

@@ -1,0 +1,518 @@
+// api.cu -- the C ABI (include/convgb.h): argument checks, shape derivation,
+// path choice, workspace layout, TMA descriptors and launches.
+//
+// Nothing here computes on the host: every element of every output is
+// produced by the kernels in igemm.cu and relayout.cu.
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+
+namespace convgb {
+
+namespace {
+
+__device__ unsigned g_device_error;  // first device-side failure since the last check
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kAlign = 256;  // alignment of each workspace region
+
+std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_device()
+{
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+// Output extent along one axis; 0 when the window does not fit.
+long long out_extent(long long L, long long K, long long s, long long p, long long d)
+{
+    long long span = L + 2 * p - d * (K - 1) - 1;
+    if (span < 0) return 0;
+    return span / s + 1;
+}
+
+// Validates a shape and fills the derived extents.  INVALID_ARG for bad
+// parameters or an empty output, UNSUPPORTED when an index limit is exceeded.
+convgb_status make_shape(int N, int C_in, int H, int W, int C_out, int KH, int KW, int s, int p,
+                         int d, ConvShape* c)
+{
+    if (N < 1 || C_in < 1 || H < 1 || W < 1 || C_out < 1 || KH < 1 || KW < 1 || s < 1 || p < 0 ||
+        d < 1)
+        return CONVGB_ERR_INVALID_ARG;
+    long long Ho = out_extent(H, KH, s, p, d), Wo = out_extent(W, KW, s, p, d);
+    if (Ho < 1 || Wo < 1) return CONVGB_ERR_INVALID_ARG;
+    const long long lim = (1ll << 31) - 1;
+    long long x_elems = (long long)N * H * W * C_in;
+    long long y_elems = (long long)N * Ho * Wo * C_out;
+    long long w_elems = (long long)C_out * KH * KW * C_in;
+    if (x_elems > lim || y_elems > lim || w_elems > lim) return CONVGB_ERR_UNSUPPORTED;
+    if (Ho * Wo * KH * KW > lim) return CONVGB_ERR_UNSUPPORTED;      // indirection entries
+    c->N = N; c->C_in = C_in; c->H = H; c->W = W; c->C_out = C_out;
+    c->KH = KH; c->KW = KW; c->s = s; c->p = p; c->d = d;
+    c->H_out = (int)Ho; c->W_out = (int)Wo;
+    c->M = (long long)N * Ho * Wo;
+    c->K = (long long)KH * KW * C_in;
+    return CONVGB_OK;
+}
+
+bool is_pointwise(const ConvShape& c)
+{
+    return c.KH == 1 && c.KW == 1 && c.s == 1 && c.p == 0;
+}
+
+bool is_full_spatial(const ConvShape& c)
+{
+    return c.KH == c.H && c.KW == c.W && c.p == 0 && c.d == 1;  // H_out = W_out = 1
+}
+
+// Whether `path` can compute this shape.
+bool path_supports(int path, const ConvShape& c)
+{
+    switch (path) {
+    case CONVGB_PATH_GATHER: return c.C_in % 8 == 0;
+    case CONVGB_PATH_DENSE: return c.C_in % 8 == 0 && (is_pointwise(c) || is_full_spatial(c));
+    case CONVGB_PATH_STEM: return c.C_in % 8 != 0;
+    default: return false;
+    }
+}
+
+int select_path(const ConvShape& c)
+{
+    if (path_supports(CONVGB_PATH_DENSE, c)) return CONVGB_PATH_DENSE;
+    if (c.C_in % 8 != 0) return CONVGB_PATH_STEM;
+    return CONVGB_PATH_GATHER;
+}
+
+// Stem path: channels per tap in the packed K order (4 when C_in <= 4, else the
+// next multiple of 8), and the packed row length rounded to 8 elements so the
+// weight rows stay 16-byte aligned for TMA.
+int stem_cp(const ConvShape& c) { return c.C_in <= 4 ? 4 : (c.C_in + 7) / 8 * 8; }
+long long stem_kpad(const ConvShape& c)
+{
+    return ((long long)c.KH * c.KW * stem_cp(c) + 7) / 8 * 8;
+}
+
+// Workspace regions of each path, in order; every region starts 256-byte aligned.
+struct WsLayout {
+    size_t ibuf_off = 0, ibuf_bytes = 0;
+    size_t wpad_off = 0, wpad_bytes = 0;
+    size_t total = 0;
+};
+
+WsLayout workspace_layout(int path, const ConvShape& c)
+{
+    WsLayout L;
+    size_t at = 0;
+    if (path == CONVGB_PATH_GATHER || path == CONVGB_PATH_STEM) {
+        L.ibuf_off = at;
+        L.ibuf_bytes = (size_t)c.H_out * c.W_out * c.KH * c.KW * sizeof(int32_t);
+        at = align_up(at + L.ibuf_bytes, kAlign);
+    }
+    if (path == CONVGB_PATH_STEM) {
+        L.wpad_off = at;
+        L.wpad_bytes = (size_t)c.C_out * stem_kpad(c) * 2;
+        at = align_up(at + L.wpad_bytes, kAlign);
+    }
+    L.total = at;
+    return L;
+}
+
+// ------------------------------------------------------------ driver entry point
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [rows][cols] (cols contiguous), box [box_rows][64 cols],
+// 128-byte swizzle: exactly the K-major operand tile the MMA descriptors expect.
+bool encode_kmajor(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int pick_bn(int C_out)
+{
+    if (C_out <= 32) return 32;
+    if (C_out <= 64) return 64;
+    if (C_out <= 128) return 128;
+    return 256;
+}
+
+struct IgemmArgs {
+    int amode = kADense;
+    const void* a_dense = nullptr;  // dense mode: [M][K] bf16
+    const uint16_t* x = nullptr;    // gather modes
+    const int32_t* ibuf = nullptr;
+    const void* w = nullptr;        // [C_out][K] bf16
+    const void* bias = nullptr;
+    void* y = nullptr;
+    int y_f32 = 0;
+    long long M = 0, K = 0;
+    int C_out = 0, C_in = 1, cp = 1, taps = 1, HWo = 1;
+    long long k_valid = 0, img_elems = 0;
+};
+
+convgb_status run_igemm(const IgemmArgs& a, cudaStream_t st)
+{
+    if (a.K % 8 != 0) return CONVGB_ERR_UNSUPPORTED;  // TMA row pitch must be 16-byte aligned
+    const int bn = pick_bn(a.C_out);
+    CUtensorMap ta, tb;
+    memset(&ta, 0, sizeof ta);
+    if (!encode_kmajor(&tb, a.w, a.C_out, a.K, bn)) return CONVGB_ERR_CUDA;
+    if (a.amode == kADense && !encode_kmajor(&ta, a.a_dense, a.M, a.K, 128))
+        return CONVGB_ERR_CUDA;
+    unsigned* err = device_error_word();
+    if (!err) return CONVGB_ERR_CUDA;
+    IgemmParams p;
+    memset(&p, 0, sizeof p);
+    p.x = a.x;
+    p.ibuf = a.ibuf;
+    p.bias = static_cast<const uint16_t*>(a.bias);
+    p.y = a.y;
+    p.M = (int)a.M;
+    p.K = (int)a.K;
+    p.C_out = a.C_out;
+    p.C_in = a.C_in;
+    p.cp = a.cp;
+    p.k_valid = (int)a.k_valid;
+    p.taps = a.taps;
+    p.cin_div = FastDiv((uint32_t)(a.amode == kANarrow ? a.cp : a.C_in));
+    p.hwo_div = FastDiv((uint32_t)a.HWo);
+    p.img_elems = a.img_elems;
+    p.num_kb = (int)((a.K + 63) / 64);
+    p.m_tiles = (int)((a.M + 127) / 128);
+    p.n_tiles = (a.C_out + bn - 1) / bn;
+    p.y_f32 = a.y_f32;
+    p.timeout_ns = g_timeout_ns.load();
+    p.err = err;
+    return launch_igemm(a.amode, bn, ta, tb, p, st) == cudaSuccess ? CONVGB_OK : CONVGB_ERR_CUDA;
+}
+
+convgb_status conv_impl(int path, const void* x, const void* w, const void* bias, int N, int C_in,
+                        int H, int W, int C_out, int KH, int KW, int s, int p, int d, void* y,
+                        int y_dtype, void* ws, size_t ws_bytes, void* stream)
+{
+    ConvShape c;
+    convgb_status st = make_shape(N, C_in, H, W, C_out, KH, KW, s, p, d, &c);
+    if (st != CONVGB_OK) return st;
+    if (!x || !w || !y) return CONVGB_ERR_INVALID_ARG;
+    if (y_dtype != CONVGB_BF16 && y_dtype != CONVGB_F32) return CONVGB_ERR_INVALID_ARG;
+    if (path == CONVGB_PATH_AUTO) path = select_path(c);
+    if (path != CONVGB_PATH_GATHER && path != CONVGB_PATH_DENSE && path != CONVGB_PATH_STEM)
+        return CONVGB_ERR_INVALID_ARG;
+    if (!path_supports(path, c)) return CONVGB_ERR_UNSUPPORTED;
+    WsLayout L = workspace_layout(path, c);
+    if (ws_bytes < L.total) return CONVGB_ERR_WORKSPACE;
+    if (L.total > 0 && !ws) return CONVGB_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        (ws && !aligned16(ws)))
+        return CONVGB_ERR_ALIGNMENT;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+
+    IgemmArgs a;
+    a.w = w;
+    a.bias = bias;
+    a.y = y;
+    a.y_f32 = y_dtype == CONVGB_F32 ? 1 : 0;
+    a.M = c.M;
+    a.C_out = C_out;
+    if (path == CONVGB_PATH_DENSE) {
+        // 1x1 stride-1: A = x as [N*H*W][C_in]; full-spatial: A = x as [N][H*W*C_in].
+        a.amode = kADense;
+        a.a_dense = x;
+        a.K = c.K;
+        return run_igemm(a, cs);
+    }
+    int32_t* ibuf = reinterpret_cast<int32_t*>(wsb + L.ibuf_off);
+    if (launch_build_indirection(c, ibuf, cs) != cudaSuccess) return CONVGB_ERR_CUDA;
+    a.x = static_cast<const uint16_t*>(x);
+    a.ibuf = ibuf;
+    a.C_in = C_in;
+    a.taps = KH * KW;
+    a.HWo = c.H_out * c.W_out;
+    a.img_elems = (long long)H * W * C_in;
+    if (path == CONVGB_PATH_GATHER) {
+        a.amode = kAGather;
+        a.K = c.K;
+        return run_igemm(a, cs);
+    }
+    // Stem: weights re-packed with each tap's channels padded to cp.
+    a.amode = kANarrow;
+    a.cp = stem_cp(c);
+    a.k_valid = (long long)a.taps * a.cp;
+    a.K = stem_kpad(c);
+    uint16_t* wpad = reinterpret_cast<uint16_t*>(wsb + L.wpad_off);
+    if (launch_pack_padded_weights(static_cast<const uint16_t*>(w), wpad, C_out, a.taps, C_in,
+                                   a.cp, (int)a.K, cs) != cudaSuccess)
+        return CONVGB_ERR_CUDA;
+    a.w = wpad;
+    return run_igemm(a, cs);
+}
+
+}  // namespace
+
+unsigned* device_error_word()
+{
+    static unsigned* addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned*>(a);
+    }
+    return addr[dev];
+}
+
+int num_sms()
+{
+    static int sms[kMaxDevices] = {};
+    int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 148;
+    if (sms[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+            v = 148;
+        sms[dev] = v;
+    }
+    return sms[dev];
+}
+
+}  // namespace convgb
+
+using namespace convgb;
+
+extern "C" {
+
+const char* convgb_status_string(int s)
+{
+    switch (s) {
+    case CONVGB_OK: return "ok";
+    case CONVGB_ERR_INVALID_ARG: return "invalid argument";
+    case CONVGB_ERR_UNSUPPORTED: return "unsupported shape or path";
+    case CONVGB_ERR_WORKSPACE: return "workspace or buffer too small";
+    case CONVGB_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    case CONVGB_ERR_CUDA: return "CUDA runtime or launch failure";
+    case CONVGB_ERR_INTERNAL: return "device-side failure (pipeline wait timed out)";
+    default: return "unknown status";
+    }
+}
+
+convgb_status convgb_output_dims(int H, int W, int KH, int KW, int stride, int pad, int dilation,
+                                 int* H_out, int* W_out)
+{
+    if (H < 1 || W < 1 || KH < 1 || KW < 1 || stride < 1 || pad < 0 || dilation < 1)
+        return CONVGB_ERR_INVALID_ARG;
+    long long ho = out_extent(H, KH, stride, pad, dilation);
+    long long wo = out_extent(W, KW, stride, pad, dilation);
+    if (ho < 1 || wo < 1) return CONVGB_ERR_INVALID_ARG;
+    if (H_out) *H_out = (int)ho;
+    if (W_out) *W_out = (int)wo;
+    return CONVGB_OK;
+}
+
+int convgb_select_path(int N, int C_in, int H, int W, int C_out, int KH, int KW, int stride,
+                       int pad, int dilation)
+{
+    ConvShape c;
+    if (make_shape(N, C_in, H, W, C_out, KH, KW, stride, pad, dilation, &c) != CONVGB_OK) return -1;
+    return select_path(c);
+}
+
+size_t convgb_conv2d_fwd_path_workspace_size(int path, int N, int C_in, int H, int W, int C_out,
+                                             int KH, int KW, int stride, int pad, int dilation)
+{
+    ConvShape c;
+    if (make_shape(N, C_in, H, W, C_out, KH, KW, stride, pad, dilation, &c) != CONVGB_OK) return 0;
+    if (path == CONVGB_PATH_AUTO) path = select_path(c);
+    if (!path_supports(path, c)) return 0;
+    return workspace_layout(path, c).total;
+}
+
+size_t convgb_conv2d_fwd_workspace_size(int N, int C_in, int H, int W, int C_out, int KH, int KW,
+                                        int stride, int pad, int dilation)
+{
+    return convgb_conv2d_fwd_path_workspace_size(CONVGB_PATH_AUTO, N, C_in, H, W, C_out, KH, KW,
+                                                 stride, pad, dilation);
+}
+
+size_t convgb_im2col_bytes(int N, int C_in, int H, int W, int KH, int KW, int stride, int pad,
+                           int dilation)
+{
+    ConvShape c;
+    if (make_shape(N, C_in, H, W, 1, KH, KW, stride, pad, dilation, &c) != CONVGB_OK) return 0;
+    return (size_t)c.M * (size_t)c.K * 2;
+}
+
+convgb_status conv2d_fwd(const void* x, const void* w, const void* bias, int N, int C_in, int H,
+                         int W, int C_out, int KH, int KW, int stride, int pad, int dilation,
+                         void* y, int y_dtype, void* workspace, size_t workspace_bytes,
+                         void* stream)
+{
+    return conv_impl(CONVGB_PATH_AUTO, x, w, bias, N, C_in, H, W, C_out, KH, KW, stride, pad,
+                     dilation, y, y_dtype, workspace, workspace_bytes, stream);
+}
+
+convgb_status conv2d_fwd_path(int path, const void* x, const void* w, const void* bias, int N,
+                              int C_in, int H, int W, int C_out, int KH, int KW, int stride,
+                              int pad, int dilation, void* y, int y_dtype, void* workspace,
+                              size_t workspace_bytes, void* stream)
+{
+    return conv_impl(path, x, w, bias, N, C_in, H, W, C_out, KH, KW, stride, pad, dilation, y,
+                     y_dtype, workspace, workspace_bytes, stream);
+}
+
+convgb_status conv2d_fwd_indirect(const void* x, const void* w, const void* bias, int N, int C_in,
+                                  int H, int W, int C_out, int KH, int KW, int stride, int pad,
+                                  int dilation, const int32_t* ibuf, size_t ibuf_bytes, void* y,
+                                  int y_dtype, void* stream)
+{
+    ConvShape c;
+    convgb_status st = make_shape(N, C_in, H, W, C_out, KH, KW, stride, pad, dilation, &c);
+    if (st != CONVGB_OK) return st;
+    if (!x || !w || !y || !ibuf) return CONVGB_ERR_INVALID_ARG;
+    if (y_dtype != CONVGB_BF16 && y_dtype != CONVGB_F32) return CONVGB_ERR_INVALID_ARG;
+    if (!path_supports(CONVGB_PATH_GATHER, c)) return CONVGB_ERR_UNSUPPORTED;
+    if (ibuf_bytes < (size_t)c.H_out * c.W_out * KH * KW * sizeof(int32_t))
+        return CONVGB_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        !aligned16(ibuf))
+        return CONVGB_ERR_ALIGNMENT;
+    IgemmArgs a;
+    a.amode = kAGather;
+    a.x = static_cast<const uint16_t*>(x);
+    a.ibuf = ibuf;
+    a.w = w;
+    a.bias = bias;
+    a.y = y;
+    a.y_f32 = y_dtype == CONVGB_F32 ? 1 : 0;
+    a.M = c.M;
+    a.K = c.K;
+    a.C_out = C_out;
+    a.C_in = C_in;
+    a.taps = KH * KW;
+    a.HWo = c.H_out * c.W_out;
+    a.img_elems = (long long)H * W * C_in;
+    return run_igemm(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t convgb_indirection_buffer_bytes(int H, int W, int KH, int KW, int stride, int pad,
+                                       int dilation)
+{
+    int ho = 0, wo = 0;
+    if (convgb_output_dims(H, W, KH, KW, stride, pad, dilation, &ho, &wo) != CONVGB_OK) return 0;
+    return (size_t)ho * wo * KH * KW * sizeof(int32_t);
+}
+
+convgb_status build_indirection_buffer(int H, int W, int C_in, int KH, int KW, int stride, int pad,
+                                       int dilation, int32_t* ibuf, size_t ibuf_bytes,
+                                       void* stream)
+{
+    ConvShape c;
+    convgb_status st = make_shape(1, C_in, H, W, 1, KH, KW, stride, pad, dilation, &c);
+    if (st != CONVGB_OK) return st;
+    if (!ibuf) return CONVGB_ERR_INVALID_ARG;
+    if (!aligned16(ibuf)) return CONVGB_ERR_ALIGNMENT;
+    if (ibuf_bytes < (size_t)c.H_out * c.W_out * KH * KW * sizeof(int32_t))
+        return CONVGB_ERR_WORKSPACE;
+    return launch_build_indirection(c, ibuf, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? CONVGB_OK
+               : CONVGB_ERR_CUDA;
+}
+
+size_t convgb_im2win_bytes(int N, int C_in, int H, int W, int KH, int KW, int stride, int pad,
+                           int dilation)
+{
+    ConvShape c;
+    if (make_shape(N, C_in, H, W, 1, KH, KW, stride, pad, dilation, &c) != CONVGB_OK) return 0;
+    size_t w_used = (size_t)(c.W_out - 1) * stride + (size_t)(KW - 1) * dilation + 1;
+    return (size_t)N * c.H_out * w_used * KH * C_in * 2;
+}
+
+convgb_status im2win_transform(const void* x, int N, int C_in, int H, int W, int KH, int KW,
+                               int stride, int pad, int dilation, void* win, size_t win_bytes,
+                               void* stream)
+{
+    ConvShape c;
+    convgb_status st = make_shape(N, C_in, H, W, 1, KH, KW, stride, pad, dilation, &c);
+    if (st != CONVGB_OK) return st;
+    if (!x || !win) return CONVGB_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(win)) return CONVGB_ERR_ALIGNMENT;
+    size_t need = convgb_im2win_bytes(N, C_in, H, W, KH, KW, stride, pad, dilation);
+    if (win_bytes < need) return CONVGB_ERR_WORKSPACE;
+    size_t count = C_in % 8 == 0 ? need / 16 : need / 2;  // loop trips of the kernel
+    if (count > (size_t)INT32_MAX) return CONVGB_ERR_UNSUPPORTED;
+    return launch_im2win(c, static_cast<const uint16_t*>(x), static_cast<uint16_t*>(win),
+                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? CONVGB_OK
+               : CONVGB_ERR_CUDA;
+}
+
+convgb_status convgb_check_device_errors(void* stream, unsigned int* code)
+{
+    if (code) *code = 0;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return CONVGB_ERR_CUDA;
+    unsigned* addr = device_error_word();
+    if (!addr) return CONVGB_ERR_CUDA;
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpy(&v, addr, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return CONVGB_ERR_CUDA;
+    if (v == 0) return CONVGB_OK;
+    if (cudaMemcpy(addr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return CONVGB_ERR_CUDA;
+    if (code) *code = v;
+    return CONVGB_ERR_INTERNAL;
+}
+
+void convgb_set_wait_timeout_ns(uint64_t ns)
+{
+    g_timeout_ns.store(ns ? ns : 1ull);
+}
+
+convgb_status convgb_selftest_wait_timeout(uint64_t timeout_ns, void* stream)
+{
+    unsigned* err = device_error_word();
+    if (!err) return CONVGB_ERR_CUDA;
+    return launch_selftest_timeout(timeout_ns, err, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? CONVGB_OK
+               : CONVGB_ERR_CUDA;
+}
+
+int convgb_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,498 @@
+// igemm.cu -- the tcgen05 implicit-GEMM convolution kernel for sm_103a.
+//
+// Computes Y_col = X_col * W_row^T + bias ("Unifying Convolutions and GEMM",
+// sections 2-3 and 5) without forming X_col: row m of X_col (output pixel
+// (n, ho, wo)) and K block kb are gathered on the fly, through the
+// indirection buffer of "The Indirect Convolution Algorithm" (Abstract: the
+// modified GEMM reads its A rows through pointers to input pixel rows), into a
+// 128-byte-swizzled shared-memory tile; W_row tiles arrive by TMA.  The GEMM
+// itself runs on the fifth-generation tensor cores: one thread issues
+// tcgen05.mma (bf16 x bf16 -> fp32) into a double-buffered accumulator in
+// tensor memory, and four epilogue warps read it back with tcgen05.ld, add the
+// bias and store channels-last y.  The dense variant (1x1 stride-1 layers and
+// kernels that cover the whole image) loads A by TMA as well.
+//
+// CTA layout (320 threads, one persistent CTA per SM):
+//   warps 0-3  epilogue: TMEM -> registers -> +bias -> bf16/fp32 -> global
+//   warps 4-7  A gather: cp.async 16-byte chunks through the indirection buffer
+//   warp  8    TMEM allocation and the MMA-issuing thread
+//   warp  9    TMA producer for B (and for A in the dense variant)
+// Stages cycle through full/empty mbarrier pairs; every wait is bounded in
+// time and a timeout makes the whole CTA drain and return with an error code.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace convgb {
+namespace {
+
+constexpr int BM = 128;           // GEMM rows per tile (TMEM lanes)
+constexpr int BK = 64;            // K elements per stage: one 128-byte swizzle row
+constexpr int kEpiWarps = 4;
+constexpr int kGatherWarps = 4;
+constexpr int kMmaWarp = kEpiWarps + kGatherWarps;  // 8
+constexpr int kTmaWarp = kMmaWarp + 1;              // 9
+constexpr int kThreads = (kTmaWarp + 1) * 32;       // 320
+constexpr int kGatherThreads = kGatherWarps * 32;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kGatherLag = 2;     // cp.async groups each gather thread keeps in flight
+constexpr int kRowsPerGatherThread = BM * (BK / 8) / kGatherThreads;  // 8
+
+template <int BN>
+struct Cfg {
+    static constexpr int kABytes = BM * BK * 2;
+    static constexpr int kBBytes = BN * BK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    static constexpr int kTmemCols = 2 * BN;  // two accumulators
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarBytes;
+    static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
+    static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation must be a power of 2");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+    static_assert((3 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
+};
+
+// Shared state every role needs for bounded waits.
+struct WaitCtx {
+    volatile uint32_t* abort;  // shared flag: some role gave up
+    unsigned* err;
+    unsigned long long timeout_ns;
+};
+
+// Waits for the phase of `bar` with the given parity.  Returns false (and the
+// caller must unwind) when the wait exceeds the time limit or another role
+// of this CTA has already given up.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const WaitCtx& w,
+                                         unsigned role)
+{
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = ptx::globaltimer();
+    for (uint32_t spins = 1;; ++spins) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*w.abort) return false;
+        if ((spins & 31u) == 0 && ptx::globaltimer() - t0 > w.timeout_ns) {
+            *w.abort = 1u;
+            atomicCAS(w.err, 0u, kErrWaitTimeout | (role << 8));
+            return false;
+        }
+    }
+}
+
+// Bounded wait used while unwinding: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
+                                           unsigned long long limit_ns)
+{
+    if (ptx::mbar_try_wait(bar, parity)) return;
+    const unsigned long long t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (ptx::globaltimer() - t0 > limit_ns) return;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b)
+{
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Stores 32 accumulator columns [co0, co0+32) of row m, adding the bias.
+__device__ __forceinline__ void store_chunk(const IgemmParams& p, int m, int co0,
+                                            const uint32_t (&r)[32])
+{
+    float v[32];
+    const int ncols = min(32, p.C_out - co0);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    if (p.bias != nullptr) {
+        if (ncols == 32 && (p.C_out & 7) == 0) {
+            const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + co0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 b = __ldg(b4 + q);
+                uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[q * 8 + 2 * e] += bf16_bits_to_float(static_cast<uint16_t>(w[e] & 0xFFFFu));
+                    v[q * 8 + 2 * e + 1] += bf16_bits_to_float(static_cast<uint16_t>(w[e] >> 16));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncols) v[i] += bf16_bits_to_float(__ldg(p.bias + co0 + i));
+        }
+    }
+    const long long row = static_cast<long long>(m) * p.C_out + co0;
+    if (p.y_f32) {
+        float* out = static_cast<float*>(p.y) + row;
+        if (ncols == 32 && (p.C_out & 3) == 0) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(out)[q] =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncols) out[i] = v[i];
+        }
+    } else {
+        uint16_t* out = static_cast<uint16_t*>(p.y) + row;
+        if (ncols == 32 && (p.C_out & 7) == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                reinterpret_cast<uint4*>(out)[q] =
+                    make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
+                               pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                               pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncols) {
+                    __nv_bfloat16 b = __float2bfloat16_rn(v[i]);
+                    out[i] = *reinterpret_cast<uint16_t*>(&b);
+                }
+        }
+    }
+}
+
+template <int BN, int AMODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    igemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                 const __grid_constant__ CUtensorMap tmap_b, const IgemmParams p)
+{
+    using C = Cfg<BN>;
+    constexpr int S = C::kStages;
+    constexpr bool GATHER = AMODE != kADense;
+    extern __shared__ uint8_t smem_raw[];
+    // The 128-byte swizzle is a function of shared-memory address bits, so the
+    // stage buffers must start on 1024-byte boundaries of the shared window.
+    uint8_t* smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + S * C::kABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::kBBytes);
+    uint64_t* full_a = bars;          // gather threads' stage-ready, count kGatherThreads
+    uint64_t* full_b = bars + S;      // TMA stage-ready (tx bytes), count 1
+    uint64_t* empty = bars + 2 * S;   // MMA done with stage, count 1 (tcgen05.commit)
+    uint64_t* tfull = bars + 3 * S;   // accumulator ready, count 1 (tcgen05.commit)
+    uint64_t* tempty = tfull + 2;     // accumulator drained, count kEpiThreads
+    uint64_t* drain = tempty + 2;     // MMA unwinding, count 1
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(&full_a[s], kGatherThreads);
+            ptx::mbar_init(&full_b[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&tfull[i], 1);
+            ptx::mbar_init(&tempty[i], kEpiThreads);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kTmaWarp && lane == 0) {
+        if (!GATHER) ptx::prefetch_tensormap(&tmap_a);
+        ptx::prefetch_tensormap(&tmap_b);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(tmem_slot, C::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+    const int total_tiles = p.m_tiles * p.n_tiles;
+
+    if (warp < kEpiWarps) {
+        // ------------------------------------------------------------ epilogue
+        uint32_t lt = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
+            const int m0 = (tile / p.n_tiles) * BM;
+            const int n0 = (tile % p.n_tiles) * BN;
+            const uint32_t acc = lt & 1u, use = lt >> 1;
+            // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds.
+            const bool ready = wait_bar(&tfull[acc], use & 1u, wc, kRoleEpilogue);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            ptx::tc_fence_after();
+            const int m = m0 + warp * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                ptx::tmem_ld_wait();
+                const int co0 = n0 + ch * 32;
+                if (m < p.M && co0 < p.C_out) store_chunk(p, m, co0, r);
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tempty[acc]);
+        }
+    } else if (warp < kEpiWarps + kGatherWarps) {
+        // ------------------------------------------------------------ A gather
+        // Thread gt owns 16-byte chunk c (8 consecutive K columns) of rows
+        // rg, rg+16, ..., rg+112 of every A tile: 8 threads cover one 128-byte row.
+        if (GATHER) {
+            const int gt = threadIdx.x - kEpiThreads;  // 0..127
+            const int c = gt & 7;
+            const int rg = gt >> 3;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const int m0 = (tile / p.n_tiles) * BM;
+                int ib[kRowsPerGatherThread];        // pixel's first ibuf entry, or -1
+                long long xb[kRowsPerGatherThread];  // image base (elements)
+#pragma unroll
+                for (int j = 0; j < kRowsPerGatherThread; ++j) {
+                    const int m = m0 + rg + 16 * j;
+                    ib[j] = -1;
+                    xb[j] = 0;
+                    if (m < p.M) {
+                        uint32_t n, pix;
+                        p.hwo_div.divmod(static_cast<uint32_t>(m), n, pix);
+                        ib[j] = static_cast<int>(pix) * p.taps;
+                        xb[j] = static_cast<long long>(n) * p.img_elems;
+                    }
+                }
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const uint32_t stage = it % S, round = it / S;
+                    if (!wait_bar(&empty[stage], (round & 1u) ^ 1u, wc, kRoleGather)) {
+                        ok = false;
+                        break;
+                    }
+                    const int k = kb * BK + c * 8;
+                    const uint32_t dst0 = ptx::smem_addr(sA + stage * C::kABytes);
+                    if (AMODE == kAGather) {
+                        // C_in % 8 == 0: the chunk is 8 channels of one tap's pixel.
+                        const bool kval = k < p.K;
+                        uint32_t tap = 0, ci = 0;
+                        if (kval) p.cin_div.divmod(static_cast<uint32_t>(k), tap, ci);
+                        int off[kRowsPerGatherThread];
+#pragma unroll
+                        for (int j = 0; j < kRowsPerGatherThread; ++j)
+                            off[j] = (kval && ib[j] >= 0) ? __ldg(p.ibuf + ib[j] + tap) : -1;
+#pragma unroll
+                        for (int j = 0; j < kRowsPerGatherThread; ++j) {
+                            const int r = rg + 16 * j;
+                            const uint32_t dst = dst0 + r * 128 + ((c ^ (r & 7)) << 4);
+                            const bool live = off[j] >= 0;
+                            const uint16_t* src = live ? p.x + xb[j] + off[j] + ci : p.x;
+                            ptx::cp_async_16(dst, src, live ? 16u : 0u);
+                        }
+                        ptx::cp_async_commit();
+                        if (it >= kGatherLag) {
+                            ptx::cp_async_wait_group<kGatherLag>();
+                            ptx::fence_proxy_async_smem();
+                            ptx::mbar_arrive(&full_a[(it - kGatherLag) % S]);
+                        }
+                    } else {
+                        // Narrow C_in: K columns are (tap, channel) with channels padded
+                        // to cp (4, or a multiple of 8).  cp == 4: the chunk spans taps
+                        // t0 and t0+1; otherwise channels [c0, c0+8) of tap t0.
+                        const bool two = p.cp == 4;
+                        uint32_t t0 = 0, c0 = 0;
+                        if (k < p.k_valid) p.cin_div.divmod(static_cast<uint32_t>(k), t0, c0);
+                        const bool v0 = k < p.k_valid;
+                        const bool v1 = two && (k + 4) < p.k_valid;
+#pragma unroll
+                        for (int j = 0; j < kRowsPerGatherThread; ++j) {
+                            const int o0 = (v0 && ib[j] >= 0) ? __ldg(p.ibuf + ib[j] + t0) : -1;
+                            const int o1 = (v1 && ib[j] >= 0) ? __ldg(p.ibuf + ib[j] + t0 + 1) : -1;
+                            uint16_t e[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const int o = (two && q >= 4) ? o1 : o0;
+                                const int ch = two ? (q & 3) : static_cast<int>(c0) + q;
+                                e[q] = (o >= 0 && ch < p.C_in) ? p.x[xb[j] + o + ch] : (uint16_t)0;
+                            }
+                            const int r = rg + 16 * j;
+                            uint4 v;
+                            v.x = (uint32_t)e[0] | ((uint32_t)e[1] << 16);
+                            v.y = (uint32_t)e[2] | ((uint32_t)e[3] << 16);
+                            v.z = (uint32_t)e[4] | ((uint32_t)e[5] << 16);
+                            v.w = (uint32_t)e[6] | ((uint32_t)e[7] << 16);
+                            *reinterpret_cast<uint4*>(sA + stage * C::kABytes + r * 128 +
+                                                      ((c ^ (r & 7)) << 4)) = v;
+                        }
+                        ptx::fence_proxy_async_smem();
+                        ptx::mbar_arrive(&full_a[stage]);
+                    }
+                }
+            }
+            if (AMODE == kAGather) {
+                // Release the stages still in flight (also on the abort path, so
+                // that no copy is outstanding when the CTA exits).
+                ptx::cp_async_wait_all();
+                ptx::fence_proxy_async_smem();
+                for (uint32_t i = it > kGatherLag ? it - kGatherLag : 0; i < it; ++i)
+                    ptx::mbar_arrive(&full_a[i % S]);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+            uint32_t it = 0, lt = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++lt) {
+                const uint32_t acc = lt & 1u, use = lt >> 1;
+                if (!wait_bar(&tempty[acc], (use & 1u) ^ 1u, wc, kRoleMma)) break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const uint32_t stage = it % S, round = it / S;
+                    if (GATHER && !wait_bar(&full_a[stage], round & 1u, wc, kRoleMma)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!wait_bar(&full_b[stage], round & 1u, wc, kRoleMma)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t adesc =
+                        ptx::sdesc_k_major_sw128(ptx::smem_addr(sA + stage * C::kABytes));
+                    const uint64_t bdesc =
+                        ptx::sdesc_k_major_sw128(ptx::smem_addr(sB + stage * C::kBBytes));
+                    // The last K block may hold fewer than 64 columns: skip the
+                    // all-zero 16-column steps.
+                    const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        if (kk < ksteps)
+                            ptx::mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                          (kb | kk) != 0 ? 1u : 0u);
+                    ptx::mma_commit(&empty[stage]);
+                }
+                if (ok) ptx::mma_commit(&tfull[acc]);
+            }
+            // Make sure no MMA is still reading shared memory or writing TMEM.
+            ptx::mma_commit(drain);
+            drain_wait(drain, 0, 1000000000ull);
+        }
+    } else if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            constexpr uint32_t kTx = GATHER ? C::kBBytes : C::kABytes + C::kBBytes;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const int m0 = (tile / p.n_tiles) * BM;
+                const int n0 = (tile % p.n_tiles) * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const uint32_t stage = it % S, round = it / S;
+                    if (!wait_bar(&empty[stage], (round & 1u) ^ 1u, wc, kRoleTma)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full_b[stage], kTx);
+                    if (!GATHER)
+                        ptx::tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full_b[stage],
+                                         kb * BK, m0);
+                    ptx::tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full_b[stage], kb * BK,
+                                     n0);
+                }
+            }
+            // Wait (bounded) for the last loads so none lands after the CTA exits.
+            for (uint32_t i = it > (uint32_t)S ? it - S : 0; i < it; ++i)
+                drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// A wait nothing will ever satisfy, bounded by the time limit: exercises the
+// failure path without faulting or hanging the GPU.
+__global__ void selftest_timeout_kernel(unsigned long long timeout_ns, unsigned* err)
+{
+    __shared__ uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        abort_flag = 0u;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const WaitCtx wc{&abort_flag, err, timeout_ns};
+        (void)wait_bar(&bar, 0u, wc, kRoleSelftest);
+    }
+}
+
+template <int BN, int AMODE>
+cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const IgemmParams& p,
+                      cudaStream_t st)
+{
+    using C = Cfg<BN>;
+    auto kern = igemm_kernel<BN, AMODE>;
+    static int configured_for = -1;  // device for which the smem attribute was set
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_for != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_for = dev;
+    }
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    kern<<<grid, kThreads, C::kSmemBytes, st>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+template <int AMODE>
+cudaError_t launch_mode(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const IgemmParams& p,
+                        cudaStream_t st)
+{
+    switch (bn) {
+    case 32: return launch_bn<32, AMODE>(ta, tb, p, st);
+    case 64: return launch_bn<64, AMODE>(ta, tb, p, st);
+    case 128: return launch_bn<128, AMODE>(ta, tb, p, st);
+    case 256: return launch_bn<256, AMODE>(ta, tb, p, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtensorMap& tb,
+                         const IgemmParams& p, cudaStream_t st)
+{
+    switch (amode) {
+    case kADense: return launch_mode<kADense>(bn, ta, tb, p, st);
+    case kAGather: return launch_mode<kAGather>(bn, ta, tb, p, st);
+    case kANarrow: return launch_mode<kANarrow>(bn, ta, tb, p, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_selftest_timeout(unsigned long long timeout_ns, unsigned* err, cudaStream_t st)
+{
+    selftest_timeout_kernel<<<1, 32, 0, st>>>(timeout_ns, err);
+    return cudaGetLastError();
+}
+
+}  // namespace convgb

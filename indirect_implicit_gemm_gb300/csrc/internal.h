@@ -1,0 +1,82 @@
+// internal.h -- declarations shared by the library's translation units.
+//
+// Host-side shape record, kernel parameter blocks and the launchers each
+// kernel file exports to the C-ABI file.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/convgb.h"
+#include "fastdiv.h"
+
+namespace convgb {
+
+// Device error word codes (low byte: what failed; upper bits: role).
+enum DeviceErr : unsigned {
+    kErrWaitTimeout = 1u,
+};
+
+// Role tags stored in bits 8..15 of the error word.
+enum Role : unsigned {
+    kRoleEpilogue = 1u,
+    kRoleGather = 2u,
+    kRoleMma = 3u,
+    kRoleTma = 4u,
+    kRoleSelftest = 5u,
+};
+
+// One convolution, with the derived GEMM extents.
+struct ConvShape {
+    int N, C_in, H, W, C_out, KH, KW, s, p, d;
+    int H_out, W_out;
+    long long M;   // N * H_out * W_out
+    long long K;   // KH * KW * C_in
+};
+
+// Parameters of the implicit-GEMM kernel (A gathered or TMA-loaded, B TMA-loaded).
+struct IgemmParams {
+    const uint16_t* x;       // bf16 [N][H][W][C_in] (gather mode)
+    const int32_t* ibuf;     // [H_out*W_out][KH*KW] element offsets or -1 (gather mode)
+    const uint16_t* bias;    // bf16 [C_out] or nullptr
+    void* y;                 // [M][C_out], bf16 or fp32
+    int M;                   // GEMM rows
+    int K;                   // GEMM reduction length (elements)
+    int C_out;               // GEMM columns
+    int C_in;                // channels per tap of x (gather modes)
+    int cp;                  // padded channels per tap in K (narrow mode: 4 or a multiple of 8)
+    int k_valid;             // taps*cp: K columns that hold data (narrow mode)
+    int taps;                // KH*KW (gather modes)
+    FastDiv cin_div;         // divides a K index by C_in (gather) or by cp (narrow)
+    FastDiv hwo_div;         // divides a row index by H_out*W_out (gather mode)
+    long long img_elems;     // H*W*C_in (gather mode)
+    int num_kb;              // ceil(K / 64)
+    int m_tiles, n_tiles;
+    int y_f32;               // 1: fp32 output, 0: bf16
+    unsigned long long timeout_ns;
+    unsigned* err;           // device error word
+};
+
+// Launchers (return cudaGetLastError() of the launch).
+cudaError_t launch_build_indirection(const ConvShape& c, int32_t* ibuf, cudaStream_t st);
+cudaError_t launch_im2win(const ConvShape& c, const uint16_t* x, uint16_t* win, cudaStream_t st);
+cudaError_t launch_pack_padded_weights(const uint16_t* w, uint16_t* wp, int C_out, int taps,
+                                       int C_in, int cp, int k_pad, cudaStream_t st);
+
+// How the A operand reaches shared memory.
+enum AMode : int {
+    kADense = 0,   // TMA tiles of a dense [M][K] matrix (1x1 stride-1, full-spatial)
+    kAGather = 1,  // cp.async 16-byte pixel chunks through the indirection buffer (C_in % 8 == 0)
+    kANarrow = 2,  // scalar loads through the indirection buffer, channels padded to cp (stem)
+};
+cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& tmap_a,
+                         const CUtensorMap& tmap_b, const IgemmParams& p, cudaStream_t st);
+cudaError_t launch_selftest_timeout(unsigned long long timeout_ns, unsigned* err,
+                                    cudaStream_t st);
+
+// Shared helpers from api.cu.
+unsigned* device_error_word();  // address of this device's error word (host-visible pointer)
+int num_sms();
+
+}  // namespace convgb

@@ -1,0 +1,154 @@
+// relayout.cu -- the two memory-bound re-layout kernels and the stem's
+// channel padding.
+//
+//  * build_indirection: the indirection buffer of "The Indirect Convolution
+//    Algorithm" (Abstract), one int32 element offset per (output pixel, tap).
+//  * im2win: the window-order buffer of "Im2win: An Efficient Convolution
+//    Paradigm on GPU" (Abstract), win[n][ho][wc][kh][ci].
+//  * pack_padded_weights: the stem path's weight matrix with every tap's
+//    channels padded to the gather granule (zero weights on the padding).
+//
+// All three are bandwidth kernels: grid-stride loops over the output, 16-byte
+// vector accesses where the layout allows, grids sized in whole waves of the
+// SM count.
+#include "fastdiv.h"
+#include "internal.h"
+
+namespace convgb {
+namespace {
+
+constexpr int kThreads = 256;
+
+int grid_for(long long work_items, int per_thread)
+{
+    long long blocks = (work_items + (long long)kThreads * per_thread - 1) /
+                       ((long long)kThreads * per_thread);
+    long long cap = (long long)num_sms() * 8;  // 8 resident 256-thread CTAs per SM
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return (int)blocks;
+}
+
+// ibuf[pix][tap] = ((h*W)+w)*C_in, or -1 in the padding.
+__global__ void __launch_bounds__(kThreads) build_indirection_kernel(
+    int32_t* __restrict__ ibuf, int total, FastDiv taps, FastDiv kw_div, FastDiv wo_div, int H,
+    int W, int C_in, int s, int p, int d)
+{
+    for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < (uint32_t)total;
+         e += gridDim.x * blockDim.x) {
+        uint32_t pix, tap, ho, wo, kh, kw;
+        taps.divmod(e, pix, tap);
+        wo_div.divmod(pix, ho, wo);
+        kw_div.divmod(tap, kh, kw);
+        int h = (int)ho * s + (int)kh * d - p;
+        int w = (int)wo * s + (int)kw * d - p;
+        int32_t v = -1;
+        if (h >= 0 && h < H && w >= 0 && w < W) v = (h * W + w) * C_in;
+        ibuf[e] = v;
+    }
+}
+
+// One 16-byte vector (8 channels) of win per loop trip; C_in % 8 == 0.
+__global__ void __launch_bounds__(kThreads) im2win_vec_kernel(
+    const uint4* __restrict__ x, uint4* __restrict__ win, int total, FastDiv cv_div,
+    FastDiv kh_div, FastDiv wu_div, FastDiv ho_div, int H, int W, int s, int p, int d)
+{
+    const uint32_t CV = cv_div.d;
+    // v = (((n*H_out + ho)*W_used + wc)*KH + kh)*CV + cv; total < 2^31 (checked on the host).
+    for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < (uint32_t)total;
+         v += gridDim.x * blockDim.x) {
+        uint32_t r0, cv, r1, kh, r2, wc, n, ho;
+        cv_div.divmod(v, r0, cv);
+        kh_div.divmod(r0, r1, kh);
+        wu_div.divmod(r1, r2, wc);
+        ho_div.divmod(r2, n, ho);
+        int h = (int)ho * s + (int)kh * d - p;
+        int w = (int)wc - p;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (h >= 0 && h < H && w >= 0 && w < W)
+            val = __ldg(&x[(((long long)n * H + h) * W + w) * CV + cv]);
+        win[v] = val;
+    }
+}
+
+// Element-wise fallback for C_in not a multiple of 8.
+__global__ void __launch_bounds__(kThreads) im2win_elem_kernel(
+    const uint16_t* __restrict__ x, uint16_t* __restrict__ win, int total, FastDiv ci_div,
+    FastDiv kh_div, FastDiv wu_div, FastDiv ho_div, int H, int W, int s, int p, int d)
+{
+    const int C_in = (int)ci_div.d;
+    for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < (uint32_t)total;
+         v += gridDim.x * blockDim.x) {
+        uint32_t r0, ci, r1, kh, r2, wc, n, ho;
+        ci_div.divmod(v, r0, ci);
+        kh_div.divmod(r0, r1, kh);
+        wu_div.divmod(r1, r2, wc);
+        ho_div.divmod(r2, n, ho);
+        int h = (int)ho * s + (int)kh * d - p;
+        int w = (int)wc - p;
+        uint16_t val = 0;
+        if (h >= 0 && h < H && w >= 0 && w < W)
+            val = x[(((long long)n * H + h) * W + w) * C_in + ci];
+        win[v] = val;
+    }
+}
+
+// Weights [C_out][T][C_in] -> [C_out][k_pad] with each tap's channels padded
+// to cp (zero weights on the padding) and the row padded with zeros from
+// T*cp to k_pad: wp[co][t*cp + c] = w[co][t][c] for c < C_in.
+__global__ void __launch_bounds__(kThreads) pack_padded_weights_kernel(
+    const uint16_t* __restrict__ w, uint16_t* __restrict__ wp, int total, FastDiv kpad_div,
+    int taps, int C_in, int cp)
+{
+    for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < (uint32_t)total;
+         e += gridDim.x * blockDim.x) {
+        uint32_t co, k;
+        kpad_div.divmod(e, co, k);
+        const int t = (int)k / cp, c = (int)k - t * cp;
+        uint16_t v = 0;
+        if (t < taps && c < C_in) v = w[((long long)co * taps + t) * C_in + c];
+        wp[e] = v;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_build_indirection(const ConvShape& c, int32_t* ibuf, cudaStream_t st)
+{
+    int taps = c.KH * c.KW;
+    int total = c.H_out * c.W_out * taps;
+    build_indirection_kernel<<<grid_for(total, 4), kThreads, 0, st>>>(
+        ibuf, total, FastDiv(taps), FastDiv(c.KW), FastDiv(c.W_out), c.H, c.W, c.C_in, c.s,
+        c.p, c.d);
+    return cudaGetLastError();
+}
+
+// The caller guarantees the element count of win (vector count when C_in % 8 == 0) is < 2^31.
+cudaError_t launch_im2win(const ConvShape& c, const uint16_t* x, uint16_t* win, cudaStream_t st)
+{
+    int W_used = (c.W_out - 1) * c.s + (c.KW - 1) * c.d + 1;
+    if (c.C_in % 8 == 0) {
+        int total = (int)((long long)c.N * c.H_out * W_used * c.KH * (c.C_in / 8));
+        im2win_vec_kernel<<<grid_for(total, 4), kThreads, 0, st>>>(
+            reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(win), total,
+            FastDiv(c.C_in / 8), FastDiv(c.KH), FastDiv(W_used), FastDiv(c.H_out), c.H, c.W,
+            c.s, c.p, c.d);
+    } else {
+        int total = (int)((long long)c.N * c.H_out * W_used * c.KH * c.C_in);
+        im2win_elem_kernel<<<grid_for(total, 4), kThreads, 0, st>>>(
+            x, win, total, FastDiv(c.C_in), FastDiv(c.KH), FastDiv(W_used), FastDiv(c.H_out), c.H, c.W,
+            c.s, c.p, c.d);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_padded_weights(const uint16_t* w, uint16_t* wp, int C_out, int taps,
+                                       int C_in, int cp, int k_pad, cudaStream_t st)
+{
+    int total = C_out * k_pad;
+    pack_padded_weights_kernel<<<grid_for(total, 4), kThreads, 0, st>>>(
+        w, wp, total, FastDiv(k_pad), taps, C_in, cp);
+    return cudaGetLastError();
+}
+
+}  // namespace convgb

@@ -1,0 +1,148 @@
+"""Host-side tests of the C ABI: no kernel is launched and no GPU is needed.
+
+The library must load, export every entry point include/convgb.h declares,
+derive shapes, sizes and paths exactly as the oracle and the pages say, and
+reject bad arguments before touching the GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import indirect_implicit_gemm_gb300 as g
+    return g
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "convgb.h")).read()
+    return sorted(set(re.findall(r"^CONVGB_API [^(]*?\b([a-z_0-9]+)\(", text, re.M)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = header_symbols()
+    assert len(declared) >= 16
+    assert sorted(lib.EXPORTED_SYMBOLS) == declared
+    so = ctypes.CDLL(lib.library_path)
+    for name in declared:
+        assert hasattr(so, name), name
+
+
+def test_library_has_no_libcuda_link_dependency(lib):
+    """The driver API is reached at run time; loading needs no libcuda.so here."""
+    import subprocess
+    out = subprocess.run(["readelf", "-d", lib.library_path], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out
+
+
+def test_status_strings(lib):
+    so = lib.load()
+    for s in range(7):
+        assert so.convgb_status_string(s)
+    assert so.convgb_status_string(99) == b"unknown status"
+    assert so.convgb_version() >= 100
+
+
+SHAPES = [(56, 3, 1, 1, 1), (224, 7, 2, 3, 1), (224, 11, 4, 2, 1), (28, 3, 1, 2, 2), (7, 7, 1, 0, 1),
+          (27, 5, 1, 2, 1), (56, 1, 2, 0, 1), (150, 3, 1, 1, 1), (5, 3, 1, 0, 2), (10, 4, 3, 1, 2),
+          (1, 1, 1, 0, 1), (9, 2, 5, 0, 3), (13, 6, 3, 4, 2)]
+
+
+@pytest.mark.parametrize("L,K,s,p,d", SHAPES)
+def test_output_dims_match_oracle(lib, L, K, s, p, d):
+    ho, wo = lib.output_dims(L, L + 1, K, K, s, p, d)
+    assert ho == oracle.output_size(L, K, s, p, d)
+    assert wo == oracle.output_size(L + 1, K, s, p, d)
+
+
+def test_output_dims_reject_empty(lib):
+    with pytest.raises(lib.ConvgbError):
+        lib.output_dims(3, 3, 5, 5, 1, 0, 1)
+    with pytest.raises(lib.ConvgbError):
+        lib.output_dims(8, 8, 3, 3, 0, 1, 1)
+
+
+@pytest.mark.parametrize("cfg", workloads.ALL, ids=lambda c: c.name)
+def test_sizes_and_workspace_below_im2col(lib, cfg):
+    a = (cfg.N, cfg.C_in, cfg.H, cfg.W)
+    geo = (cfg.KH, cfg.KW, cfg.stride, cfg.pad, cfg.dilation)
+    im2col = lib.im2col_bytes(*a, *geo)
+    assert im2col == 2 * oracle.im2col_elements(*a, *geo)
+    assert lib.im2win_bytes(*a, *geo) == 2 * oracle.im2win_elements(*a, *geo)
+    ho, wo = oracle.output_size(cfg.H, cfg.KH, cfg.stride, cfg.pad, cfg.dilation), \
+        oracle.output_size(cfg.W, cfg.KW, cfg.stride, cfg.pad, cfg.dilation)
+    assert lib.indirection_buffer_bytes(cfg.H, cfg.W, *geo) == ho * wo * cfg.KH * cfg.KW * 4
+    ws = lib.workspace_size(cfg.N, cfg.C_in, cfg.H, cfg.W, cfg.C_out, *geo)
+    assert ws < im2col, (ws, im2col)
+
+
+@pytest.mark.parametrize("cfg,path", [
+    (workloads.TINY, 3), (workloads.RESNET_3X3, 1), (workloads.POINTWISE_S1, 2),
+    (workloads.POINTWISE_S2, 1), (workloads.STEM_7X7, 3), (workloads.STRIDED_3X3, 1),
+] + [(c, 2 if (c.KH == 1 or "fullspatial" in c.name) else (3 if c.C_in % 8 else 1))
+     for c in workloads.SWEEP], ids=lambda v: getattr(v, "name", str(v)))
+def test_path_selection(lib, cfg, path):
+    got = lib.select_path(cfg.N, cfg.C_in, cfg.H, cfg.W, cfg.C_out, cfg.KH, cfg.KW, cfg.stride,
+                          cfg.pad, cfg.dilation)
+    assert got == path
+
+
+def test_dense_path_needs_no_workspace(lib):
+    assert lib.workspace_size(32, 256, 56, 56, 64, 1, 1, 1, 0, 1) == 0
+    assert lib.workspace_size(128, 512, 7, 7, 4096, 7, 7, 1, 0, 1) == 0
+    # asking for the gather path on a 1x1 layer costs only the indirection buffer
+    assert lib.workspace_size(32, 256, 56, 56, 64, 1, 1, 1, 0, 1, path=lib.PATH_GATHER) == \
+        56 * 56 * 4
+
+
+def test_path_support_matrix(lib):
+    # stem path needs C_in % 8 != 0; gather and dense need C_in % 8 == 0
+    assert lib.workspace_size(1, 3, 8, 8, 4, 3, 3, 1, 1, 1, path=lib.PATH_GATHER) == 0
+    assert lib.workspace_size(1, 8, 8, 8, 4, 3, 3, 1, 1, 1, path=lib.PATH_STEM) == 0
+    assert lib.workspace_size(1, 8, 8, 8, 4, 3, 3, 1, 1, 1, path=lib.PATH_DENSE) == 0
+    assert lib.workspace_size(1, 3, 8, 8, 4, 3, 3, 1, 1, 1, path=lib.PATH_STEM) > 0
+
+
+def call(lib, **kw):
+    """Raw conv2d_fwd_path with fake (never dereferenced) pointers."""
+    a = dict(path=0, x=0x1000, w=0x2000, b=0, N=1, C_in=8, H=8, W=8, C_out=8, KH=3, KW=3, s=1,
+             p=1, d=1, y=0x3000, yd=0, ws=0x4000, wsb=1 << 20)
+    a.update(kw)
+    so = lib.load()
+    P = ctypes.c_void_p
+    return so.conv2d_fwd_path(a["path"], P(a["x"]), P(a["w"]), P(a["b"]), a["N"], a["C_in"],
+                              a["H"], a["W"], a["C_out"], a["KH"], a["KW"], a["s"], a["p"],
+                              a["d"], P(a["y"]), a["yd"], P(a["ws"]), a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(N=0), 1), (dict(C_in=0), 1), (dict(KH=0), 1), (dict(s=0), 1), (dict(p=-1), 1),
+    (dict(d=0), 1), (dict(H=2, p=0), 1), (dict(x=0), 1), (dict(w=0), 1), (dict(y=0), 1),
+    (dict(yd=7), 1), (dict(path=9), 1), (dict(path=2), 2), (dict(path=3), 2),
+    (dict(wsb=16), 3), (dict(ws=0), 1), (dict(x=0x1008), 4), (dict(y=0x3004), 4),
+    (dict(b=0x5002), 4), (dict(N=1 << 20, H=1 << 10, W=1 << 10), 2),
+])
+def test_bad_arguments_are_rejected_before_launch(lib, kw, status):
+    assert call(lib, **kw) == status
+
+
+def test_other_entry_points_reject_bad_arguments(lib):
+    so = lib.load()
+    P = ctypes.c_void_p
+    assert so.build_indirection_buffer(8, 8, 8, 3, 3, 1, 1, 1, None, 1 << 20, None) == 1
+    assert so.build_indirection_buffer(8, 8, 8, 3, 3, 1, 1, 1, P(0x1004), 1 << 20, None) == 4
+    assert so.build_indirection_buffer(8, 8, 8, 3, 3, 1, 1, 1, P(0x1000), 16, None) == 3
+    assert so.build_indirection_buffer(2, 2, 8, 3, 3, 1, 0, 1, P(0x1000), 1 << 20, None) == 1
+    assert so.im2win_transform(None, 1, 8, 8, 8, 3, 3, 1, 1, 1, P(0x1000), 1 << 20, None) == 1
+    assert so.im2win_transform(P(0x1000), 1, 8, 8, 8, 3, 3, 1, 1, 1, P(0x2000), 64, None) == 3
+    assert so.im2win_transform(P(0x1002), 1, 8, 8, 8, 3, 3, 1, 1, 1, P(0x2000), 1 << 20, None) == 4

@@ -1,0 +1,186 @@
+"""GPU parity: every kernel, through the C ABI, against the CPU oracle.
+
+Bars: the two re-layout kernels are compared bit for bit; the convolution
+must satisfy, per element, |y - y_ref| <= 1e-2 * (|bias| + sum |x*w|) and, over
+the tensor (or the sampled outputs), ||y - y_ref||_2 / ||y_ref||_2 <= 5e-3,
+with y_ref the fp64 oracle on the same bf16 inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_ELEM = 1e-2
+TOL_REL_L2 = 5e-3
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def check(got, ref, mag, what=""):
+    got = np.asarray(got, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), what + ": non-finite output"
+    err = np.abs(got - ref)
+    bad = err > TOL_ELEM * mag
+    assert not bad.any(), "%s: %d elements out of bound, worst err %.3g (bound %.3g)" % (
+        what, bad.sum(), err[bad].max(), (TOL_ELEM * mag)[bad][np.argmax(err[bad])])
+    nref = np.linalg.norm(ref)
+    rel = np.linalg.norm(got - ref) / nref if nref > 0 else np.linalg.norm(got)
+    assert rel <= TOL_REL_L2, "%s: relative L2 %.3g" % (what, rel)
+    return err.max(), rel
+
+
+def run_full(g, shape, path=0, out_dtype=torch.bfloat16, with_bias=True, seed=None):
+    x, w, b = workloads.make_inputs(shape, seed=seed)
+    if not with_bias:
+        b = None
+    y = g.conv2d_fwd_path(path, x.to(dev()), w.to(dev()), None if b is None else b.to(dev()),
+                          shape.stride, shape.pad, shape.dilation, out_dtype=out_dtype)
+    st, code = g.check_device_errors()
+    assert st == 0, "device error word %#x" % code
+    ref, mag = oracle.conv2d_direct(workloads.bits(x), workloads.bits(w),
+                                    None if b is None else workloads.bits(b),
+                                    shape.stride, shape.pad, shape.dilation)
+    return y.float().cpu().numpy(), ref, mag
+
+
+def S(name, **kw):
+    d = dict(N=1, C_in=8, H=8, W=8, C_out=8, KH=3, KW=3, stride=1, pad=1, dilation=1, seed=11)
+    d.update(kw)
+    return workloads.ConvShape(name, **d)
+
+
+# Small shapes that span several tiles, ragged M/N/K tails, every path and BN variant.
+SMALL = [
+    S("gather_3x3_ragged", N=2, C_in=16, H=13, W=11, C_out=24),
+    S("gather_cout_100", N=1, C_in=64, H=15, W=17, C_out=100, seed=12),
+    S("gather_cout_200", N=1, C_in=32, H=9, W=21, C_out=200, seed=13),
+    S("gather_cout_300_k_tail", N=1, C_in=40, H=10, W=10, C_out=300, seed=14),
+    S("gather_stride2_dil2", N=2, C_in=24, H=17, W=15, C_out=48, stride=2, pad=2, dilation=2, seed=15),
+    S("gather_5x5_c96", N=1, C_in=96, H=12, W=12, C_out=64, KH=5, KW=5, pad=2, seed=16),
+    S("gather_asym_kernel", N=3, C_in=8, H=9, W=14, C_out=16, KH=2, KW=4, stride=1, pad=1, seed=17),
+    S("gather_1x1_pad", N=2, C_in=16, H=7, W=7, C_out=32, KH=1, KW=1, pad=1, seed=18),
+    S("gather_1x1_s2", N=2, C_in=64, H=14, W=14, C_out=128, KH=1, KW=1, stride=2, pad=0, seed=19),
+    S("dense_1x1", N=3, C_in=64, H=11, W=13, C_out=96, KH=1, KW=1, pad=0, seed=20),
+    S("dense_1x1_ktail", N=2, C_in=72, H=9, W=9, C_out=40, KH=1, KW=1, pad=0, seed=21),
+    S("dense_fullspatial", N=5, C_in=16, H=5, W=6, C_out=130, KH=5, KW=6, pad=0, seed=22),
+    S("stem_c3_7x7_s2", N=2, C_in=3, H=30, W=26, C_out=64, KH=7, KW=7, stride=2, pad=3, seed=23),
+    S("stem_c1", N=2, C_in=1, H=12, W=12, C_out=16, seed=24),
+    S("stem_c5", N=1, C_in=5, H=10, W=11, C_out=40, seed=25),
+    S("stem_c12", N=1, C_in=12, H=9, W=9, C_out=32, KH=3, KW=3, seed=26),
+    S("stem_11x11_s4", N=1, C_in=3, H=47, W=45, C_out=64, KH=11, KW=11, stride=4, pad=2, seed=27),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_conv_small_shapes_match_oracle(gpu_lib, shape, out_dtype):
+    got, ref, mag = run_full(gpu_lib, shape, out_dtype=out_dtype)
+    check(got, ref, mag, shape.name)
+
+
+@pytest.mark.parametrize("shape", SMALL[:3] + SMALL[9:13], ids=lambda s: s.name)
+def test_conv_without_bias(gpu_lib, shape):
+    got, ref, mag = run_full(gpu_lib, shape, with_bias=False)
+    check(got, ref, mag, shape.name)
+
+
+def test_tiny_config_full_output(gpu_lib):
+    """3 -> 4 channels, 8x8, 3x3, fp32 output: every output element."""
+    shape = workloads.TINY
+    got, ref, mag = run_full(gpu_lib, shape, out_dtype=torch.float32)
+    check(got, ref, mag, shape.name)
+
+
+@pytest.mark.parametrize("shape", [SMALL[8], SMALL[9], SMALL[11]], ids=lambda s: s.name)
+def test_paths_agree(gpu_lib, shape):
+    """The gather path computes what the dense path computes (1x1 and full-spatial)."""
+    x, w, b = workloads.make_inputs(shape)
+    args = (x.to(dev()), w.to(dev()), b.to(dev()), shape.stride, shape.pad, shape.dilation)
+    ys = {}
+    for path in (gpu_lib.PATH_GATHER, gpu_lib.PATH_DENSE):
+        try:
+            ys[path] = gpu_lib.conv2d_fwd_path(path, *args, out_dtype=torch.float32)
+        except gpu_lib.ConvgbError as e:
+            assert e.status == 2  # dense path does not apply to this shape
+    if len(ys) == 2:
+        a, c = ys[gpu_lib.PATH_GATHER], ys[gpu_lib.PATH_DENSE]
+        assert torch.allclose(a, c, rtol=1e-5, atol=1e-5)
+
+
+def test_repeat_calls_are_deterministic(gpu_lib):
+    shape = SMALL[1]
+    x, w, b = workloads.make_inputs(shape)
+    args = (x.to(dev()), w.to(dev()), b.to(dev()), shape.stride, shape.pad, shape.dilation)
+    y1 = gpu_lib.conv2d_fwd(*args)
+    y2 = gpu_lib.conv2d_fwd(*args)
+    assert torch.equal(y1, y2)
+
+
+def test_output_guard_bands_untouched(gpu_lib):
+    """Writes stay inside y: canaries before and after the output survive."""
+    shape = SMALL[3]
+    x, w, b = workloads.make_inputs(shape)
+    Ho = oracle.output_size(shape.H, shape.KH, shape.stride, shape.pad, shape.dilation)
+    Wo = oracle.output_size(shape.W, shape.KW, shape.stride, shape.pad, shape.dilation)
+    n = shape.N * Ho * Wo * shape.C_out
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 12345.0, dtype=torch.float32, device=dev())
+    y = buf[guard:guard + n].view(shape.N, Ho, Wo, shape.C_out)
+    gpu_lib.conv2d_fwd(x.to(dev()), w.to(dev()), b.to(dev()), shape.stride, shape.pad,
+                       shape.dilation, out_dtype=torch.float32, y=y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:guard] == 12345.0) and torch.all(buf[guard + n:] == 12345.0)
+
+
+INDIR_GEOMS = [(8, 8, 8, 3, 3, 1, 1, 1), (13, 11, 16, 3, 3, 2, 1, 1), (56, 56, 64, 3, 3, 1, 1, 1),
+               (224, 224, 3, 7, 7, 2, 3, 1), (28, 28, 256, 3, 3, 1, 2, 2),
+               (27, 27, 96, 5, 5, 1, 2, 1), (224, 224, 3, 11, 11, 4, 2, 1), (7, 7, 512, 7, 7, 1, 0, 1),
+               (9, 14, 8, 2, 4, 3, 3, 2)]
+
+
+@pytest.mark.parametrize("geom", INDIR_GEOMS, ids=str)
+def test_indirection_buffer_bit_exact(gpu_lib, geom):
+    H, W, C, KH, KW, s, p, d = geom
+    got = gpu_lib.build_indirection_buffer(H, W, C, KH, KW, s, p, d, device=dev()).cpu().numpy()
+    ref = oracle.indirection_buffer(H, W, C, KH, KW, s, p, d)
+    np.testing.assert_array_equal(got, ref)
+
+
+IM2WIN = [S("w_3x3", N=2, C_in=16, H=9, W=10), S("w_s2d2", N=2, C_in=8, H=17, W=15, stride=2, pad=2,
+                                                dilation=2),
+          S("w_5x5_c96", N=1, C_in=96, H=12, W=12, KH=5, KW=5, pad=2),
+          S("w_c3_7x7", N=2, C_in=3, H=30, W=26, KH=7, KW=7, stride=2, pad=3),
+          S("w_c5", N=1, C_in=5, H=10, W=11), S("w_resnet", N=4, C_in=64, H=56, W=56)]
+
+
+@pytest.mark.parametrize("shape", IM2WIN, ids=lambda s: s.name)
+def test_im2win_bit_exact(gpu_lib, shape):
+    x, _, _ = workloads.make_inputs(shape)
+    win = gpu_lib.im2win_transform(x.to(dev()), shape.KH, shape.KW, shape.stride, shape.pad,
+                                   shape.dilation)
+    got = win.cpu().view(torch.int16).numpy().view(np.uint16)
+    ref = oracle.im2win(workloads.bits(x), shape.KH, shape.KW, shape.stride, shape.pad,
+                        shape.dilation)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_wait_timeout_is_reported_not_hung(gpu_lib):
+    """A wait nothing satisfies gives up after its limit and reports INTERNAL."""
+    st, _ = gpu_lib.check_device_errors()
+    assert st == 0
+    gpu_lib.selftest_wait_timeout(2_000_000)  # 2 ms
+    st, code = gpu_lib.check_device_errors()
+    assert st == gpu_lib.ERR_INTERNAL
+    assert code & 0xFF == 1 and (code >> 8) == 5
+    # the context stays usable and the word is cleared
+    st, _ = gpu_lib.check_device_errors()
+    assert st == 0
+    got, ref, mag = run_full(gpu_lib, SMALL[0])
+    check(got, ref, mag, "after timeout")

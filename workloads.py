@@ -98,17 +98,19 @@ ALL = [c for g in GROUPS.values() for c in g]
 BY_NAME = {c.name: c for c in ALL}
 
 
-def make_inputs(shape: ConvShape, seed: int | None = None):
-    """(x, w, bias) as CPU bf16 tensors: x [N,H,W,C_in], w [C_out,KH,KW,C_in], bias [C_out].
+def make_inputs(shape: ConvShape, seed: int | None = None, device="cpu"):
+    """(x, w, bias) as bf16 tensors: x [N,H,W,C_in], w [C_out,KH,KW,C_in], bias [C_out].
 
-    bias is None when the shape has bias=False.
+    bias is None when the shape has bias=False.  The draws come from a
+    generator on `device` (the CPU by default, which the parity tests use; a
+    CUDA generator gives the same distributions, not the same values).
     """
-    g = torch.Generator().manual_seed(shape.seed if seed is None else seed)
-    x = torch.randn(shape.N, shape.C_in, shape.H, shape.W, generator=g, dtype=torch.float32)
-    w = torch.randn(shape.C_out, shape.C_in, shape.KH, shape.KW, generator=g,
-                    dtype=torch.float32)
+    g = torch.Generator(device=device).manual_seed(shape.seed if seed is None else seed)
+    kw = dict(generator=g, dtype=torch.float32, device=device)
+    x = torch.randn(shape.N, shape.C_in, shape.H, shape.W, **kw)
+    w = torch.randn(shape.C_out, shape.C_in, shape.KH, shape.KW, **kw)
     w = w * (1.0 / (shape.C_in * shape.KH * shape.KW)) ** 0.5
-    b = torch.randn(shape.C_out, generator=g, dtype=torch.float32) * 0.1
+    b = torch.randn(shape.C_out, **kw) * 0.1
     x = x.to(torch.bfloat16).permute(0, 2, 3, 1).contiguous()
     w = w.to(torch.bfloat16).permute(0, 2, 3, 1).contiguous()
     b = b.to(torch.bfloat16) if shape.bias else None
