@@ -7,7 +7,8 @@ C_in=64 -> C_out=128, 56x56, stride 1, pad 1, bf16 in, fp32 accumulate, bf16
 out): the indirection-buffer build plus the tcgen05 implicit-GEMM kernel.
 Inputs are seeded synthetic tensors already resident in HBM; successive steps
 rotate through enough input/output sets that each step's data has left the
-129 MB L2 before it is used again.
+129 MB L2 before it is used again.  The K timed steps are captured once into a
+CUDA graph and replayed, so host-side call overhead is not timed.
 
 The JSON line (rank 0) also carries:
   roofline      the implicit-GEMM kernel alone (CUDA events around launches of
@@ -57,6 +58,15 @@ def load_peaks():
         return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
     except Exception:
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def reduce_max(value: float, dist=None, device="cpu") -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def dist_env():
@@ -163,6 +173,34 @@ def rotation_sets(per_set_bytes, cap_bytes=8 << 30):
     return int(max(1, min(n, cap_bytes // max(per_set_bytes, 1))))
 
 
+def graph_time_ms(fn, steps, stream):
+    """Time `steps` calls of fn(i) replayed from one CUDA graph (no host overhead).
+
+    The calls are captured once, replayed once untimed, then timed as one
+    replay bracketed by CUDA events on the capturing stream.
+    """
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(steps):
+                fn(i)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    s = torch.cuda.current_stream()
+    start.record(s)
+    graph.replay()
+    end.record(s)
+    torch.cuda.synchronize()
+    del graph
+    return start.elapsed_time(end)
+
+
 def event_time_ms(fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -214,7 +252,7 @@ class Layer:
 def time_layer(layer, steps, warmup, stream):
     for i in range(warmup):
         layer.step(i)
-    ms = event_time_ms(layer.step, steps, stream)
+    ms = graph_time_ms(layer.step, steps, stream)
     return ms / steps
 
 
@@ -226,7 +264,7 @@ def time_gemm_kernel(layer, steps, warmup, stream):
                                                   c.dilation, device=layer.dev)
     for i in range(warmup):
         layer.gemm_only(i)
-    return event_time_ms(layer.gemm_only, steps, stream) / steps
+    return graph_time_ms(layer.gemm_only, steps, stream) / steps
 
 
 def time_e2e(g, c, steps, warmup, dev, stream):
@@ -275,7 +313,7 @@ def time_im2win(g, c, steps, warmup, dev, stream):
 
     for i in range(warmup):
         one(i)
-    ms = event_time_ms(one, steps, stream) / steps
+    ms = graph_time_ms(one, steps, stream) / steps
     moved = x.numel() * 2 + nb  # read x once, write the buffer once
     return ms, moved
 
@@ -347,6 +385,13 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--sweep-steps", type=int, default=30)
+    ap.add_argument("--profile-launches", type=int, default=0,
+                    help="profiling mode: run this many eager conv2d_fwd calls of --config "
+                         "(batch --batch) and exit without timing or output")
+    ap.add_argument("--batch", type=int, default=0, help="override N of --config (profiling)")
+    ap.add_argument("--clock-probe-s", type=float, default=0.5,
+                    help="seconds of untimed steps before the timed region, so the clock "
+                         "sampler sees the GPU under load (0 disables)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -367,6 +412,15 @@ def main():
     g.load()
     peaks, peak_src = load_peaks()
     c = workloads.BY_NAME[args.config]
+    if args.batch:
+        c = c.scaled(args.batch, "_n%d" % args.batch)
+    if args.profile_launches:
+        layer = Layer(g, c, dev, sets=1)
+        for i in range(args.profile_launches):
+            layer.step(i)
+        torch.cuda.synchronize()
+        st, code = g.check_device_errors()
+        return 0 if st == 0 else 1
     stream = torch.cuda.current_stream()
     layer = Layer(g, c, dev)
     num = layer.num
@@ -379,9 +433,9 @@ def main():
         pg.barrier()
     with ClockSampler(local) as clk:
         # keep the GPU busy long enough for the sampler to see load
-        t_end = time.perf_counter() + 0.5
+        t_end = time.perf_counter() + args.clock_probe_s
         i = 0
-        while time.perf_counter() < t_end:
+        while time.perf_counter() < t_end and i < 20000:
             layer.step(i)
             i += 1
             if i % 64 == 0:
@@ -389,15 +443,11 @@ def main():
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
-        ms_total = event_time_ms(layer.step, args.steps, stream)
+        ms_total = graph_time_ms(layer.step, args.steps, stream)
         if pg:
             pg.barrier()
     clocks = clk.summary()
-    ms_step = ms_total / args.steps
-    if pg:
-        t = torch.tensor([ms_step], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = reduce_max(ms_total / args.steps, pg, dev)
     value = world * num["flops"] / (ms_step * 1e-3) / 1e12
 
     # the dominant kernel alone (implicit GEMM), for the roofline

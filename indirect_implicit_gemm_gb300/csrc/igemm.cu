@@ -36,7 +36,6 @@ constexpr int kTmaWarp = kMmaWarp + 1;              // 9
 constexpr int kThreads = (kTmaWarp + 1) * 32;       // 320
 constexpr int kGatherThreads = kGatherWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kGatherLag = 2;     // cp.async groups each gather thread keeps in flight
 constexpr int kRowsPerGatherThread = BM * (BK / 8) / kGatherThreads;  // 8
 
 template <int BN>
@@ -171,6 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<BN>;
     constexpr int S = C::kStages;
     constexpr bool GATHER = AMODE != kADense;
+    // cp.async groups each gather thread keeps in flight: all stages but one
+    // (S would deadlock: the stage it waits to refill could not be released).
+    constexpr int kLag = S - 1;
     extern __shared__ uint8_t smem_raw[];
     // The 128-byte swizzle is a function of shared-memory address bits, so the
     // stage buffers must start on 1024-byte boundaries of the shared window.
@@ -270,6 +272,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         xb[j] = static_cast<long long>(n) * p.img_elems;
                     }
                 }
+                // Indirection entries of K block `kb` for this thread's rows
+                // (gather mode), fetched one block ahead of their use.
+                int off[kRowsPerGatherThread], nxt[kRowsPerGatherThread];
+                uint32_t nxt_ci = 0;
+                auto load_offsets = [&](int kb_next) {
+                    const int kn = kb_next * BK + c * 8;
+                    const bool kval = kb_next < p.num_kb && kn < p.K;
+                    uint32_t tap = 0;
+                    nxt_ci = 0;
+                    if (kval) p.cin_div.divmod(static_cast<uint32_t>(kn), tap, nxt_ci);
+#pragma unroll
+                    for (int j = 0; j < kRowsPerGatherThread; ++j)
+                        nxt[j] = (kval && ib[j] >= 0) ? __ldg(p.ibuf + ib[j] + tap) : -1;
+                };
+                if (AMODE == kAGather) load_offsets(0);
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                     const uint32_t stage = it % S, round = it / S;
                     if (!wait_bar(&empty[stage], (round & 1u) ^ 1u, wc, kRoleGather)) {
@@ -280,13 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t dst0 = ptx::smem_addr(sA + stage * C::kABytes);
                     if (AMODE == kAGather) {
                         // C_in % 8 == 0: the chunk is 8 channels of one tap's pixel.
-                        const bool kval = k < p.K;
-                        uint32_t tap = 0, ci = 0;
-                        if (kval) p.cin_div.divmod(static_cast<uint32_t>(k), tap, ci);
-                        int off[kRowsPerGatherThread];
+                        // The indirection entries of this K block were loaded one
+                        // block ahead; fetch the next block's now, then copy.
+                        const uint32_t ci = nxt_ci;
 #pragma unroll
-                        for (int j = 0; j < kRowsPerGatherThread; ++j)
-                            off[j] = (kval && ib[j] >= 0) ? __ldg(p.ibuf + ib[j] + tap) : -1;
+                        for (int j = 0; j < kRowsPerGatherThread; ++j) off[j] = nxt[j];
+                        load_offsets(kb + 1);
 #pragma unroll
                         for (int j = 0; j < kRowsPerGatherThread; ++j) {
                             const int r = rg + 16 * j;
@@ -296,10 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::cp_async_16(dst, src, live ? 16u : 0u);
                         }
                         ptx::cp_async_commit();
-                        if (it >= kGatherLag) {
-                            ptx::cp_async_wait_group<kGatherLag>();
+                        // Keep kLag groups in flight; the oldest one is complete now.
+                        if (it >= (uint32_t)kLag) {
+                            ptx::cp_async_wait_group<kLag>();
                             ptx::fence_proxy_async_smem();
-                            ptx::mbar_arrive(&full_a[(it - kGatherLag) % S]);
+                            ptx::mbar_arrive(&full_a[(it - kLag) % S]);
                         }
                     } else {
                         // Narrow C_in: K columns are (tap, channel) with channels padded
@@ -340,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // that no copy is outstanding when the CTA exits).
                 ptx::cp_async_wait_all();
                 ptx::fence_proxy_async_smem();
-                for (uint32_t i = it > kGatherLag ? it - kGatherLag : 0; i < it; ++i)
+                for (uint32_t i = it > (uint32_t)kLag ? it - kLag : 0; i < it; ++i)
                     ptx::mbar_arrive(&full_a[i % S]);
             }
         }
