@@ -160,6 +160,35 @@ CONVGB_API convgb_status conv2d_fwd_indirect(const void* x, const void* w, const
                                              int stride, int pad, int dilation, const int32_t* ibuf,
                                              size_t ibuf_bytes, void* y, int y_dtype, void* stream);
 
+/*
+ * conv2d_fwd_noalloc -- conv2d_fwd's gather path for callers that cannot
+ * provide a workspace.  (Not from the pages, which have no counterpart: it is
+ * an interface convenience of this library.)
+ *
+ * Who needs it: callers whose device memory is planned and owned by a host
+ * framework that offers no allocation hook, and latency-critical loops that
+ * must never call cudaMalloc/cudaFree (which can synchronise the device).
+ * This call allocates nothing: its scratch (the indirection buffer) lives in
+ * a fixed 4 MiB array in the library's device image, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Arguments, layouts and results as conv2d_fwd (the caller still passes x, w,
+ * bias and y).  Requires C_in % 8 == 0 (CONVGB_ERR_UNSUPPORTED otherwise) and
+ * H_out*W_out*KH*KW <= 1,048,576 indirection entries (4 MiB); larger shapes
+ * return CONVGB_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  Every call on a device shares the one array and rewrites all of
+ * it that it uses, so nothing needs clearing; calls that may overlap on the
+ * GPU (other streams, other host threads) race on it and must be serialised
+ * by the caller.
+ */
+CONVGB_API convgb_status conv2d_fwd_noalloc(const void* x, const void* w, const void* bias, int N,
+                                            int C_in, int H, int W, int C_out, int KH, int KW,
+                                            int stride, int pad, int dilation, void* y,
+                                            int y_dtype, void* stream);
+
 /* Bytes of the indirection buffer: H_out*W_out*KH*KW*4 (0 if invalid). */
 CONVGB_API size_t convgb_indirection_buffer_bytes(int H, int W, int KH, int KW, int stride, int pad,
                                        int dilation);

@@ -36,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "convgb_status_string", "convgb_output_dims", "convgb_select_path",
     "convgb_conv2d_fwd_workspace_size", "convgb_conv2d_fwd_path_workspace_size",
     "convgb_im2col_bytes", "conv2d_fwd", "conv2d_fwd_path", "conv2d_fwd_indirect",
-    "convgb_indirection_buffer_bytes",
+    "conv2d_fwd_noalloc", "convgb_indirection_buffer_bytes",
     "build_indirection_buffer", "convgb_im2win_bytes", "im2win_transform",
     "convgb_check_device_errors", "convgb_set_wait_timeout_ns", "convgb_selftest_wait_timeout",
     "convgb_version",
@@ -80,6 +80,8 @@ def load():
     lib.conv2d_fwd_path.restype = I
     lib.conv2d_fwd_indirect.argtypes = [P, P, P] + shape10 + [P, Z, P, I, P]
     lib.conv2d_fwd_indirect.restype = I
+    lib.conv2d_fwd_noalloc.argtypes = [P, P, P] + shape10 + [P, I, P]
+    lib.conv2d_fwd_noalloc.restype = I
     lib.convgb_indirection_buffer_bytes.argtypes = [I] * 7
     lib.convgb_indirection_buffer_bytes.restype = Z
     lib.build_indirection_buffer.argtypes = [I] * 8 + [P, Z, P]
