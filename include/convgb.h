@@ -92,9 +92,14 @@ CONVGB_API convgb_status convgb_output_dims(int H, int W, int KH, int KW, int st
 CONVGB_API int convgb_select_path(int N, int C_in, int H, int W, int C_out, int KH, int KW,
                        int stride, int pad, int dilation);
 
-/* Bytes of workspace conv2d_fwd() needs for this shape on the path it selects
- * (0 for the dense path), or 0 for an invalid shape.  Always smaller than
- * convgb_im2col_bytes() for the shapes this library accepts. */
+/* Bytes of workspace conv2d_fwd() needs for this shape on the path it selects,
+ * or 0 for an invalid shape.  It holds the indirection buffer (gather and stem
+ * paths), the stem path's re-packed weights, and, for layers with too few
+ * output tiles to fill the GPU, fp32 partial sums of a split K loop
+ * (M*C_out*4 bytes, used only when that is under half the im2col size).
+ * 1x1 stride-1 layers need none.  For the benchmark layers the total is a
+ * small fraction of convgb_im2col_bytes(); only tiny images with many output
+ * channels can exceed it. */
 CONVGB_API size_t convgb_conv2d_fwd_workspace_size(int N, int C_in, int H, int W, int C_out, int KH,
                                         int KW, int stride, int pad, int dilation);
 

@@ -103,31 +103,6 @@ long long stem_kpad(const ConvShape& c)
     return ((long long)c.KH * c.KW * stem_cp(c) + 7) / 8 * 8;
 }
 
-// Workspace regions of each path, in order; every region starts 256-byte aligned.
-struct WsLayout {
-    size_t ibuf_off = 0, ibuf_bytes = 0;
-    size_t wpad_off = 0, wpad_bytes = 0;
-    size_t total = 0;
-};
-
-WsLayout workspace_layout(int path, const ConvShape& c)
-{
-    WsLayout L;
-    size_t at = 0;
-    if (path == CONVGB_PATH_GATHER || path == CONVGB_PATH_STEM) {
-        L.ibuf_off = at;
-        L.ibuf_bytes = (size_t)c.H_out * c.W_out * c.KH * c.KW * sizeof(int32_t);
-        at = align_up(at + L.ibuf_bytes, kAlign);
-    }
-    if (path == CONVGB_PATH_STEM) {
-        L.wpad_off = at;
-        L.wpad_bytes = (size_t)c.C_out * stem_kpad(c) * 2;
-        at = align_up(at + L.wpad_bytes, kAlign);
-    }
-    L.total = at;
-    return L;
-}
-
 // ------------------------------------------------------------ driver entry point
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -168,54 +143,182 @@ int pick_bn(int C_out)
     return 256;
 }
 
-struct IgemmArgs {
+// How one convolution maps onto the implicit-GEMM kernel.
+struct GemmPlan {
     int amode = kADense;
+    int bn = 128;
+    int splits = 1;
+    int stages = 0;  // shared-memory ring depth
+    int bres = 0;    // weights resident in shared memory
+    long long M = 0, K = 0;
+    int num_kb = 0, m_tiles = 0, n_tiles = 0;
+};
+
+// K partitions per output tile.  When the output tiles alone leave SMs idle,
+// the K loop is split so more CTAs work at once (partial sums meet in an fp32
+// buffer).  Planned for a nominal 148 SMs so that workspace sizes do not
+// depend on the device; a split must cut the estimated time (waves of work
+// per CTA) by a quarter, keep >= 4 K blocks per CTA, and its fp32 buffer must
+// fit under `partial_cap` bytes.
+int choose_splits(long long tiles, int num_kb, long long partial_bytes, long long partial_cap)
+{
+    constexpr int kNominalSms = 148;
+    if (tiles >= 2 * kNominalSms || partial_bytes >= partial_cap) return 1;
+    auto cost = [&](int sp) {
+        return (double)((tiles * sp + kNominalSms - 1) / kNominalSms) / sp;
+    };
+    int best = 1;
+    double best_cost = cost(1);
+    for (int sp = 2; sp <= 16 && num_kb / sp >= 4; ++sp) {
+        double c = cost(sp);
+        if (c < best_cost - 1e-9) {
+            best = sp;
+            best_cost = c;
+        }
+    }
+    return best_cost <= 0.75 * cost(1) ? best : 1;
+}
+
+GemmPlan plan_gemm(int path, const ConvShape& c)
+{
+    GemmPlan g;
+    // Gather path: TMA gather4 when a 64-column K block stays inside one tap's
+    // channels, 16-byte cp.async otherwise.
+    g.amode = path == CONVGB_PATH_DENSE  ? kADense
+              : path == CONVGB_PATH_STEM ? kANarrow
+              : c.C_in % 64 == 0         ? kATmaGather
+                                         : kAGather;
+    g.M = c.M;
+    g.K = path == CONVGB_PATH_STEM ? stem_kpad(c) : c.K;
+    g.bn = pick_bn(c.C_out);
+    g.num_kb = (int)((g.K + 63) / 64);
+    g.m_tiles = (int)((g.M + 127) / 128);
+    g.n_tiles = (c.C_out + g.bn - 1) / g.bn;
+    const long long im2col = c.M * c.K * 2;
+    const long long partial = c.M * c.C_out * 4;
+    g.splits = choose_splits((long long)g.m_tiles * g.n_tiles, g.num_kb, partial, im2col / 2);
+    // Gathered layers whose whole weight matrix is one column tile: keep it in
+    // shared memory for the CTA's lifetime when that still leaves a 4-deep A ring.
+    if (g.amode != kADense && g.n_tiles == 1 && g.splits == 1 &&
+        igemm_pick_stages(g.bn, 1, g.num_kb) >= 4)
+        g.bres = 1;
+    g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb);
+    return g;
+}
+
+// Workspace regions of each path, in order; every region starts 256-byte aligned.
+struct WsLayout {
+    size_t ibuf_off = 0, ibuf_bytes = 0;
+    size_t wpad_off = 0, wpad_bytes = 0;
+    size_t part_off = 0, part_bytes = 0;
+    size_t total = 0;
+};
+
+WsLayout workspace_layout(int path, const ConvShape& c)
+{
+    WsLayout L;
+    size_t at = 0;
+    if (path == CONVGB_PATH_GATHER || path == CONVGB_PATH_STEM) {
+        L.ibuf_off = at;
+        L.ibuf_bytes = (size_t)c.H_out * c.W_out * c.KH * c.KW * sizeof(int32_t);
+        at = align_up(at + L.ibuf_bytes, kAlign);
+    }
+    if (path == CONVGB_PATH_STEM) {
+        L.wpad_off = at;
+        L.wpad_bytes = (size_t)c.C_out * stem_kpad(c) * 2;
+        at = align_up(at + L.wpad_bytes, kAlign);
+    }
+    if (plan_gemm(path, c).splits > 1) {
+        L.part_off = at;
+        L.part_bytes = (size_t)c.M * c.C_out * sizeof(float);
+        at = align_up(at + L.part_bytes, kAlign);
+    }
+    L.total = at;
+    return L;
+}
+
+struct IgemmArgs {
     const void* a_dense = nullptr;  // dense mode: [M][K] bf16
     const uint16_t* x = nullptr;    // gather modes
     const int32_t* ibuf = nullptr;
     const void* w = nullptr;        // [C_out][K] bf16
     const void* bias = nullptr;
     void* y = nullptr;
+    float* partial = nullptr;       // split-K sums (plan.splits > 1)
     int y_f32 = 0;
-    long long M = 0, K = 0;
     int C_out = 0, C_in = 1, cp = 1, taps = 1, HWo = 1;
     long long k_valid = 0, img_elems = 0;
+    int img_rows = 0;    // H*W
+    long long x_rows = 0;  // N*H*W
 };
 
-convgb_status run_igemm(const IgemmArgs& a, cudaStream_t st)
-{
-    if (a.K % 8 != 0) return CONVGB_ERR_UNSUPPORTED;  // TMA row pitch must be 16-byte aligned
-    const int bn = pick_bn(a.C_out);
+// Tensor maps and kernel parameters, all host-side: nothing is launched here,
+// so every failure is reported before the first launch of a call.
+struct PreparedGemm {
     CUtensorMap ta, tb;
-    memset(&ta, 0, sizeof ta);
-    if (!encode_kmajor(&tb, a.w, a.C_out, a.K, bn)) return CONVGB_ERR_CUDA;
-    if (a.amode == kADense && !encode_kmajor(&ta, a.a_dense, a.M, a.K, 128))
+    IgemmParams p;
+    GemmPlan plan;
+};
+
+convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* out)
+{
+    if (g.K % 8 != 0) return CONVGB_ERR_UNSUPPORTED;  // TMA row pitch must be 16-byte aligned
+    memset(out, 0, sizeof *out);
+    out->plan = g;
+    if (!encode_kmajor(&out->tb, a.w, a.C_out, g.K, g.bn)) return CONVGB_ERR_CUDA;
+    if (g.amode == kADense && !encode_kmajor(&out->ta, a.a_dense, g.M, g.K, 128))
+        return CONVGB_ERR_CUDA;
+    // TMA gather: x as [N*H*W][C_in], one-row boxes of 64 channels.
+    if (g.amode == kATmaGather && !encode_kmajor(&out->ta, a.x, a.x_rows, a.C_in, 1))
         return CONVGB_ERR_CUDA;
     unsigned* err = device_error_word();
     if (!err) return CONVGB_ERR_CUDA;
-    IgemmParams p;
-    memset(&p, 0, sizeof p);
+    IgemmParams& p = out->p;
     p.x = a.x;
     p.ibuf = a.ibuf;
     p.bias = static_cast<const uint16_t*>(a.bias);
     p.y = a.y;
-    p.M = (int)a.M;
-    p.K = (int)a.K;
+    p.M = (int)g.M;
+    p.K = (int)g.K;
     p.C_out = a.C_out;
     p.C_in = a.C_in;
     p.cp = a.cp;
     p.k_valid = (int)a.k_valid;
     p.taps = a.taps;
-    p.cin_div = FastDiv((uint32_t)(a.amode == kANarrow ? a.cp : a.C_in));
+    p.cin_div = FastDiv((uint32_t)(g.amode == kANarrow ? a.cp : a.C_in));
     p.hwo_div = FastDiv((uint32_t)a.HWo);
     p.img_elems = a.img_elems;
-    p.num_kb = (int)((a.K + 63) / 64);
-    p.m_tiles = (int)((a.M + 127) / 128);
-    p.n_tiles = (a.C_out + bn - 1) / bn;
+    p.img_rows = a.img_rows;
+    p.oob_row = (int)a.x_rows;
+    p.num_kb = g.num_kb;
+    p.m_tiles = g.m_tiles;
+    p.n_tiles = g.n_tiles;
+    p.splits = g.splits;
+    p.stages = g.stages;
+    p.bres = g.bres;
+    if (g.stages < 2) return CONVGB_ERR_UNSUPPORTED;
+    p.partial = a.partial;
     p.y_f32 = a.y_f32;
     p.timeout_ns = g_timeout_ns.load();
     p.err = err;
-    return launch_igemm(a.amode, bn, ta, tb, p, st) == cudaSuccess ? CONVGB_OK : CONVGB_ERR_CUDA;
+    if (g.splits > 1 && a.partial == nullptr) return CONVGB_ERR_WORKSPACE;
+    return CONVGB_OK;
+}
+
+// Launches the GEMM (and, for split-K, the zeroing of the partial sums before
+// it and the bias/convert pass after it).
+convgb_status launch_gemm(const PreparedGemm& pg, cudaStream_t st)
+{
+    const IgemmParams& p = pg.p;
+    if (p.splits > 1 &&
+        cudaMemsetAsync(p.partial, 0, (size_t)p.M * p.C_out * sizeof(float), st) != cudaSuccess)
+        return CONVGB_ERR_CUDA;
+    if (launch_igemm(pg.plan.amode, pg.plan.bn, pg.ta, pg.tb, p, st) != cudaSuccess)
+        return CONVGB_ERR_CUDA;
+    if (p.splits > 1 &&
+        launch_finish_split(p.partial, p.bias, p.y, p.M, p.C_out, p.y_f32, st) != cudaSuccess)
+        return CONVGB_ERR_CUDA;
+    return CONVGB_OK;
 }
 
 convgb_status conv_impl(int path, const void* x, const void* w, const void* bias, int N, int C_in,
@@ -239,45 +342,46 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
         return CONVGB_ERR_ALIGNMENT;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
+    const GemmPlan plan = plan_gemm(path, c);
 
     IgemmArgs a;
     a.w = w;
     a.bias = bias;
     a.y = y;
     a.y_f32 = y_dtype == CONVGB_F32 ? 1 : 0;
-    a.M = c.M;
     a.C_out = C_out;
+    a.partial = L.part_bytes ? reinterpret_cast<float*>(wsb + L.part_off) : nullptr;
+    int32_t* ibuf = nullptr;
+    uint16_t* wpad = nullptr;
     if (path == CONVGB_PATH_DENSE) {
         // 1x1 stride-1: A = x as [N*H*W][C_in]; full-spatial: A = x as [N][H*W*C_in].
-        a.amode = kADense;
         a.a_dense = x;
-        a.K = c.K;
-        return run_igemm(a, cs);
+    } else {
+        ibuf = reinterpret_cast<int32_t*>(wsb + L.ibuf_off);
+        a.x = static_cast<const uint16_t*>(x);
+        a.ibuf = ibuf;
+        a.C_in = C_in;
+        a.taps = KH * KW;
+        a.HWo = c.H_out * c.W_out;
+        a.img_elems = (long long)H * W * C_in;
+        a.img_rows = H * W;
+        a.x_rows = (long long)N * H * W;
+        if (path == CONVGB_PATH_STEM) {
+            // Weights re-packed with each tap's channels padded to cp.
+            a.cp = stem_cp(c);
+            a.k_valid = (long long)a.taps * a.cp;
+            wpad = reinterpret_cast<uint16_t*>(wsb + L.wpad_off);
+            a.w = wpad;
+        }
     }
-    int32_t* ibuf = reinterpret_cast<int32_t*>(wsb + L.ibuf_off);
-    if (launch_build_indirection(c, ibuf, cs) != cudaSuccess) return CONVGB_ERR_CUDA;
-    a.x = static_cast<const uint16_t*>(x);
-    a.ibuf = ibuf;
-    a.C_in = C_in;
-    a.taps = KH * KW;
-    a.HWo = c.H_out * c.W_out;
-    a.img_elems = (long long)H * W * C_in;
-    if (path == CONVGB_PATH_GATHER) {
-        a.amode = kAGather;
-        a.K = c.K;
-        return run_igemm(a, cs);
-    }
-    // Stem: weights re-packed with each tap's channels padded to cp.
-    a.amode = kANarrow;
-    a.cp = stem_cp(c);
-    a.k_valid = (long long)a.taps * a.cp;
-    a.K = stem_kpad(c);
-    uint16_t* wpad = reinterpret_cast<uint16_t*>(wsb + L.wpad_off);
-    if (launch_pack_padded_weights(static_cast<const uint16_t*>(w), wpad, C_out, a.taps, C_in,
-                                   a.cp, (int)a.K, cs) != cudaSuccess)
+    PreparedGemm pg;
+    st = prepare_gemm(plan, a, &pg);
+    if (st != CONVGB_OK) return st;
+    if (wpad && launch_pack_padded_weights(static_cast<const uint16_t*>(w), wpad, C_out, a.taps,
+                                           C_in, a.cp, (int)plan.K, cs) != cudaSuccess)
         return CONVGB_ERR_CUDA;
-    a.w = wpad;
-    return run_igemm(a, cs);
+    if (ibuf && launch_build_indirection(c, ibuf, cs) != cudaSuccess) return CONVGB_ERR_CUDA;
+    return launch_gemm(pg, cs);
 }
 
 }  // namespace
@@ -411,22 +515,27 @@ convgb_status conv2d_fwd_indirect(const void* x, const void* w, const void* bias
     if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
         !aligned16(ibuf))
         return CONVGB_ERR_ALIGNMENT;
+    // Reusing a caller's buffer leaves no room for split-K partial sums.
+    GemmPlan plan = plan_gemm(CONVGB_PATH_GATHER, c);
+    plan.splits = 1;
     IgemmArgs a;
-    a.amode = kAGather;
     a.x = static_cast<const uint16_t*>(x);
     a.ibuf = ibuf;
     a.w = w;
     a.bias = bias;
     a.y = y;
     a.y_f32 = y_dtype == CONVGB_F32 ? 1 : 0;
-    a.M = c.M;
-    a.K = c.K;
     a.C_out = C_out;
     a.C_in = C_in;
     a.taps = KH * KW;
     a.HWo = c.H_out * c.W_out;
     a.img_elems = (long long)H * W * C_in;
-    return run_igemm(a, static_cast<cudaStream_t>(stream));
+    a.img_rows = H * W;
+    a.x_rows = (long long)N * H * W;
+    PreparedGemm pg;
+    st = prepare_gemm(plan, a, &pg);
+    if (st != CONVGB_OK) return st;
+    return launch_gemm(pg, static_cast<cudaStream_t>(stream));
 }
 
 size_t convgb_indirection_buffer_bytes(int H, int W, int KH, int KW, int stride, int pad,

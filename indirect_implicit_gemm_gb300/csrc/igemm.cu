@@ -38,20 +38,38 @@ constexpr int kGatherThreads = kGatherWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kRowsPerGatherThread = BM * (BK / 8) / kGatherThreads;  // 8
 
+// Shared-memory plan (all offsets from the start of dynamic shared memory):
+//   [0, kHeaderBytes)   mbarriers, TMEM address slot, abort flag
+//   then, aligned to 1024 bytes for the 128-byte swizzle:
+//   B: `stages` ring buffers of BN x 64 K, or (weights resident) all num_kb
+//      K blocks of the single BN-wide column tile, loaded once per CTA
+//   A: `stages` ring buffers of 128 x 64 K
+// The stage count is chosen on the host from what fits (at most kMaxStages).
+constexpr int kMaxStages = 8;
+constexpr int kHeaderBytes = 512;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int kSmemLimit = 232448;    // opt-in dynamic shared memory per block
+static_assert((3 * kMaxStages + 6) * 8 + 8 <= kHeaderBytes, "header area");
+
 template <int BN>
 struct Cfg {
-    static constexpr int kABytes = BM * BK * 2;
-    static constexpr int kBBytes = BN * BK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
-    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-    static constexpr int kTmemCols = 2 * BN;  // two accumulators
-    static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarBytes;
+    static constexpr int kBBytes = BN * BK * 2;  // one K block of B
+    static constexpr int kTmemCols = 2 * BN;    // two accumulators
     static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
     static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation must be a power of 2");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
-    static_assert((3 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
+};
+
+// Advances a ring position: stage index and the parity of its current fill.
+struct Ring {
+    uint32_t stage = 0, phase = 0;
+    __device__ __forceinline__ void next(uint32_t stages)
+    {
+        if (++stage == stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
 };
 
 // Shared state every role needs for bounded waits.
@@ -162,39 +180,79 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, int m, int co0
     }
 }
 
+// Work unit `tile` -> output tile origin and K-block range.  Units are ordered
+// (m tile, n tile, K split) with the split fastest, then the n tile, so CTAs
+// working at the same time share A rows in L2.
+struct Unit {
+    int m0, n0, kb0, kb1;
+};
+template <int BN>
+__device__ __forceinline__ Unit unit_of(const IgemmParams& p, int tile)
+{
+    const int ks = tile % p.splits;
+    const int mn = tile / p.splits;
+    Unit u;
+    u.m0 = (mn / p.n_tiles) * BM;
+    u.n0 = (mn % p.n_tiles) * BN;
+    u.kb0 = static_cast<int>(static_cast<long long>(ks) * p.num_kb / p.splits);
+    u.kb1 = static_cast<int>(static_cast<long long>(ks + 1) * p.num_kb / p.splits);
+    return u;
+}
+
+// Split-K epilogue: adds 32 fp32 columns of row m into the partial-sum buffer.
+__device__ __forceinline__ void reduce_chunk(const IgemmParams& p, int m, int co0,
+                                             const uint32_t (&r)[32])
+{
+    float* out = p.partial + static_cast<long long>(m) * p.C_out + co0;
+    const int ncols = min(32, p.C_out - co0);
+    if (ncols == 32 && (p.C_out & 3) == 0) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out + 4 * q),
+                         "f"(__uint_as_float(r[4 * q])), "f"(__uint_as_float(r[4 * q + 1])),
+                         "f"(__uint_as_float(r[4 * q + 2])), "f"(__uint_as_float(r[4 * q + 3]))
+                         : "memory");
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < ncols) atomicAdd(out + i, __uint_as_float(r[i]));
+    }
+}
+
 template <int BN, int AMODE>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                  const __grid_constant__ CUtensorMap tmap_b, const IgemmParams p)
 {
     using C = Cfg<BN>;
-    constexpr int S = C::kStages;
     constexpr bool GATHER = AMODE != kADense;
-    // cp.async groups each gather thread keeps in flight: all stages but one
-    // (S would deadlock: the stage it waits to refill could not be released).
-    constexpr int kLag = S - 1;
+    const uint32_t S = static_cast<uint32_t>(p.stages);
     extern __shared__ uint8_t smem_raw[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+    uint64_t* full_a = bars;                  // A stage ready
+    uint64_t* full_b = bars + kMaxStages;     // B stage ready (tx bytes), count 1
+    uint64_t* empty = bars + 2 * kMaxStages;  // MMA done with stage, count 1 (tcgen05.commit)
+    uint64_t* tfull = bars + 3 * kMaxStages;  // accumulator ready, count 1 (tcgen05.commit)
+    uint64_t* tempty = tfull + 2;             // accumulator drained, count kEpiThreads
+    uint64_t* drain = tempty + 2;             // MMA unwinding, count 1
+    uint64_t* bres_full = drain + 1;          // resident weights loaded (tx bytes), count 1
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bres_full + 1);
+    uint32_t* abort_flag = tmem_slot + 1;
     // The 128-byte swizzle is a function of shared-memory address bits, so the
     // stage buffers must start on 1024-byte boundaries of the shared window.
-    uint8_t* smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + S * C::kABytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::kBBytes);
-    uint64_t* full_a = bars;          // gather threads' stage-ready, count kGatherThreads
-    uint64_t* full_b = bars + S;      // TMA stage-ready (tx bytes), count 1
-    uint64_t* empty = bars + 2 * S;   // MMA done with stage, count 1 (tcgen05.commit)
-    uint64_t* tfull = bars + 3 * S;   // accumulator ready, count 1 (tcgen05.commit)
-    uint64_t* tempty = tfull + 2;     // accumulator drained, count kEpiThreads
-    uint64_t* drain = tempty + 2;     // MMA unwinding, count 1
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-    uint32_t* abort_flag = tmem_slot + 1;
+    const uint32_t base = ptx::smem_addr(smem_raw) + kHeaderBytes;
+    uint8_t* data = smem_raw + kHeaderBytes + ((1024u - (base & 1023u)) & 1023u);
+    uint8_t* sB = data;
+    const uint32_t b_blocks = p.bres ? static_cast<uint32_t>(p.num_kb) : S;
+    uint8_t* sA = data + b_blocks * C::kBBytes;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(&full_a[s], kGatherThreads);
+        for (uint32_t s = 0; s < S; ++s) {
+            // TMA gather: one arrive.expect_tx per stage; thread gathers: every thread arrives.
+            ptx::mbar_init(&full_a[s], AMODE == kATmaGather ? 1 : kGatherThreads);
             ptx::mbar_init(&full_b[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
@@ -203,11 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&tempty[i], kEpiThreads);
         }
         ptx::mbar_init(drain, 1);
+        ptx::mbar_init(bres_full, 1);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
     if (warp == kTmaWarp && lane == 0) {
-        if (!GATHER) ptx::prefetch_tensormap(&tmap_a);
+        if (AMODE == kADense || AMODE == kATmaGather) ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == kMmaWarp) {
@@ -220,49 +279,112 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
-    const int total_tiles = p.m_tiles * p.n_tiles;
+    const int total_tiles = p.m_tiles * p.n_tiles * p.splits;
 
     if (warp < kEpiWarps) {
         // ------------------------------------------------------------ epilogue
         uint32_t lt = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
-            const int m0 = (tile / p.n_tiles) * BM;
-            const int n0 = (tile % p.n_tiles) * BN;
+            const Unit u = unit_of<BN>(p, tile);
             const uint32_t acc = lt & 1u, use = lt >> 1;
             // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds.
             const bool ready = wait_bar(&tfull[acc], use & 1u, wc, kRoleEpilogue);
             if (!__all_sync(0xffffffffu, ready)) break;
             ptx::tc_fence_after();
-            const int m = m0 + warp * 32 + lane;
+            const int m = u.m0 + warp * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + ch * 32, r);
                 ptx::tmem_ld_wait();
-                const int co0 = n0 + ch * 32;
-                if (m < p.M && co0 < p.C_out) store_chunk(p, m, co0, r);
+                const int co0 = u.n0 + ch * 32;
+                if (m < p.M && co0 < p.C_out) {
+                    if (p.splits > 1)
+                        reduce_chunk(p, m, co0, r);
+                    else
+                        store_chunk(p, m, co0, r);
+                }
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&tempty[acc]);
         }
     } else if (warp < kEpiWarps + kGatherWarps) {
         // ------------------------------------------------------------ A gather
-        // Thread gt owns 16-byte chunk c (8 consecutive K columns) of rows
-        // rg, rg+16, ..., rg+112 of every A tile: 8 threads cover one 128-byte row.
-        if (GATHER) {
+        if (AMODE == kATmaGather) {
+            // TMA gather4 through the indirection buffer.  The four gather warps
+            // take turns: warp gw fills the stages whose sequence number is gw
+            // mod 4, so each has four stage-times to look its rows up.  Lane l
+            // owns rows 4l..4l+3 of the 128-row tile: it turns each row's
+            // (pixel, tap) entry into a row index of x viewed as [N*H*W][C_in]
+            // and issues one gather4 of those four 128-byte rows.
+            const int gw = warp - kEpiWarps;
+            uint32_t it = 0;
+            Ring ring;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const Unit u = unit_of<BN>(p, tile);
+                int ib4[4];  // first indirection entry of the row's pixel, or -1
+                int nb4[4];  // first row of the pixel's image
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int m = u.m0 + 4 * lane + q;
+                    ib4[q] = -1;
+                    nb4[q] = 0;
+                    if (m < p.M) {
+                        uint32_t n, pix;
+                        p.hwo_div.divmod(static_cast<uint32_t>(m), n, pix);
+                        ib4[q] = static_cast<int>(pix) * p.taps;
+                        nb4[q] = static_cast<int>(n) * p.img_rows;
+                    }
+                }
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it, ring.next(S)) {
+                    if (it % kGatherWarps != static_cast<uint32_t>(gw)) continue;
+                    uint32_t tap, c0;
+                    p.cin_div.divmod(static_cast<uint32_t>(kb * BK), tap, c0);
+                    int row[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int off = ib4[q] >= 0 ? __ldg(p.ibuf + ib4[q] + tap) : -1;
+                        row[q] = off >= 0 ? nb4[q] + static_cast<int>(
+                                                         p.cin_div.div(static_cast<uint32_t>(off)))
+                                          : p.oob_row;
+                    }
+                    const bool ready =
+                        wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleGather);
+                    if (!__all_sync(0xffffffffu, ready)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) ptx::mbar_arrive_expect_tx(&full_a[ring.stage], kABytes);
+                    __syncwarp();
+                    ptx::tma_gather4(sA + ring.stage * kABytes + lane * 4 * 128, &tmap_a,
+                                     &full_a[ring.stage], static_cast<int>(c0), row[0], row[1],
+                                     row[2], row[3]);
+                }
+            }
+            // Wait (bounded) for this warp's last gathers so none lands after exit.
+            if (lane == 0) {
+                const uint32_t first = it > S ? it - S : 0;
+                for (uint32_t i = first; i < it; ++i)
+                    if (i % kGatherWarps == static_cast<uint32_t>(gw))
+                        drain_wait(&full_a[i % S], (i / S) & 1u, 1000000000ull);
+            }
+        } else if (GATHER) {
+            // Thread gt owns 16-byte chunk c (8 consecutive K columns) of rows
+            // rg, rg+16, ..., rg+112 of every A tile: 8 threads cover one 128-byte row.
             const int gt = threadIdx.x - kEpiThreads;  // 0..127
             const int c = gt & 7;
             const int rg = gt >> 3;
-            uint32_t it = 0;
+            Ring ring;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const int m0 = (tile / p.n_tiles) * BM;
+                const Unit u = unit_of<BN>(p, tile);
                 int ib[kRowsPerGatherThread];        // pixel's first ibuf entry, or -1
                 long long xb[kRowsPerGatherThread];  // image base (elements)
 #pragma unroll
                 for (int j = 0; j < kRowsPerGatherThread; ++j) {
-                    const int m = m0 + rg + 16 * j;
+                    const int m = u.m0 + rg + 16 * j;
                     ib[j] = -1;
                     xb[j] = 0;
                     if (m < p.M) {
@@ -273,12 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // Indirection entries of K block `kb` for this thread's rows
-                // (gather mode), fetched one block ahead of their use.
+                // (16-byte gather), fetched one block ahead of their use.
                 int off[kRowsPerGatherThread], nxt[kRowsPerGatherThread];
                 uint32_t nxt_ci = 0;
                 auto load_offsets = [&](int kb_next) {
                     const int kn = kb_next * BK + c * 8;
-                    const bool kval = kb_next < p.num_kb && kn < p.K;
+                    const bool kval = kb_next < u.kb1 && kn < p.K;
                     uint32_t tap = 0;
                     nxt_ci = 0;
                     if (kval) p.cin_div.divmod(static_cast<uint32_t>(kn), tap, nxt_ci);
@@ -286,23 +408,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < kRowsPerGatherThread; ++j)
                         nxt[j] = (kval && ib[j] >= 0) ? __ldg(p.ibuf + ib[j] + tap) : -1;
                 };
-                if (AMODE == kAGather) load_offsets(0);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const uint32_t stage = it % S, round = it / S;
-                    if (!wait_bar(&empty[stage], (round & 1u) ^ 1u, wc, kRoleGather)) {
+                if (AMODE == kAGather) load_offsets(u.kb0);
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
+                    if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleGather)) {
                         ok = false;
                         break;
                     }
                     const int k = kb * BK + c * 8;
-                    const uint32_t dst0 = ptx::smem_addr(sA + stage * C::kABytes);
+                    uint8_t* stage_a = sA + ring.stage * kABytes;
                     if (AMODE == kAGather) {
                         // C_in % 8 == 0: the chunk is 8 channels of one tap's pixel.
                         // The indirection entries of this K block were loaded one
-                        // block ahead; fetch the next block's now, then copy.
+                        // block ahead; fetch the next block's now, then copy.  The
+                        // thread's arrival on full_a fires when its copies land, so
+                        // the thread never waits for them.
                         const uint32_t ci = nxt_ci;
 #pragma unroll
                         for (int j = 0; j < kRowsPerGatherThread; ++j) off[j] = nxt[j];
                         load_offsets(kb + 1);
+                        const uint32_t dst0 = ptx::smem_addr(stage_a);
 #pragma unroll
                         for (int j = 0; j < kRowsPerGatherThread; ++j) {
                             const int r = rg + 16 * j;
@@ -311,13 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint16_t* src = live ? p.x + xb[j] + off[j] + ci : p.x;
                             ptx::cp_async_16(dst, src, live ? 16u : 0u);
                         }
-                        ptx::cp_async_commit();
-                        // Keep kLag groups in flight; the oldest one is complete now.
-                        if (it >= (uint32_t)kLag) {
-                            ptx::cp_async_wait_group<kLag>();
-                            ptx::fence_proxy_async_smem();
-                            ptx::mbar_arrive(&full_a[(it - kLag) % S]);
-                        }
+                        ptx::cp_async_arrive_noinc(&full_a[ring.stage]);
                     } else {
                         // Narrow C_in: K columns are (tap, channel) with channels padded
                         // to cp (4, or a multiple of 8).  cp == 4: the chunk spans taps
@@ -330,7 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < kRowsPerGatherThread; ++j) {
                             const int o0 = (v0 && ib[j] >= 0) ? __ldg(p.ibuf + ib[j] + t0) : -1;
-                            const int o1 = (v1 && ib[j] >= 0) ? __ldg(p.ibuf + ib[j] + t0 + 1) : -1;
+                            const int o1 =
+                                (v1 && ib[j] >= 0) ? __ldg(p.ibuf + ib[j] + t0 + 1) : -1;
                             uint16_t e[8];
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
@@ -344,49 +463,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v.y = (uint32_t)e[2] | ((uint32_t)e[3] << 16);
                             v.z = (uint32_t)e[4] | ((uint32_t)e[5] << 16);
                             v.w = (uint32_t)e[6] | ((uint32_t)e[7] << 16);
-                            *reinterpret_cast<uint4*>(sA + stage * C::kABytes + r * 128 +
-                                                      ((c ^ (r & 7)) << 4)) = v;
+                            *reinterpret_cast<uint4*>(stage_a + r * 128 + ((c ^ (r & 7)) << 4)) = v;
                         }
                         ptx::fence_proxy_async_smem();
-                        ptx::mbar_arrive(&full_a[stage]);
+                        ptx::mbar_arrive(&full_a[ring.stage]);
                     }
                 }
             }
-            if (AMODE == kAGather) {
-                // Release the stages still in flight (also on the abort path, so
-                // that no copy is outstanding when the CTA exits).
-                ptx::cp_async_wait_all();
-                ptx::fence_proxy_async_smem();
-                for (uint32_t i = it > (uint32_t)kLag ? it - kLag : 0; i < it; ++i)
-                    ptx::mbar_arrive(&full_a[i % S]);
-            }
+            // No copy may still be landing when the CTA exits.
+            if (AMODE == kAGather) ptx::cp_async_wait_all();
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
-            uint32_t it = 0, lt = 0;
-            bool ok = true;
+            Ring ring;
+            uint32_t lt = 0;
+            bool ok = !p.bres || wait_bar(bres_full, 0u, wc, kRoleMma);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++lt) {
+                const Unit u = unit_of<BN>(p, tile);
                 const uint32_t acc = lt & 1u, use = lt >> 1;
                 if (!wait_bar(&tempty[acc], (use & 1u) ^ 1u, wc, kRoleMma)) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const uint32_t stage = it % S, round = it / S;
-                    if (GATHER && !wait_bar(&full_a[stage], round & 1u, wc, kRoleMma)) {
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
+                    if (GATHER && !wait_bar(&full_a[ring.stage], ring.phase, wc, kRoleMma)) {
                         ok = false;
                         break;
                     }
-                    if (!wait_bar(&full_b[stage], round & 1u, wc, kRoleMma)) {
+                    if (!p.bres && !wait_bar(&full_b[ring.stage], ring.phase, wc, kRoleMma)) {
                         ok = false;
                         break;
                     }
+                    // Thread-written A stages (cp.async, st.shared) are read by the
+                    // tensor core through the async proxy.
+                    if (AMODE == kAGather || AMODE == kANarrow) ptx::fence_proxy_async_smem();
                     ptx::tc_fence_after();
                     const uint64_t adesc =
-                        ptx::sdesc_k_major_sw128(ptx::smem_addr(sA + stage * C::kABytes));
+                        ptx::sdesc_k_major_sw128(ptx::smem_addr(sA + ring.stage * kABytes));
+                    const uint32_t bblk = p.bres ? static_cast<uint32_t>(kb) : ring.stage;
                     const uint64_t bdesc =
-                        ptx::sdesc_k_major_sw128(ptx::smem_addr(sB + stage * C::kBBytes));
+                        ptx::sdesc_k_major_sw128(ptx::smem_addr(sB + bblk * C::kBBytes));
                     // The last K block may hold fewer than 64 columns: skip the
                     // all-zero 16-column steps.
                     const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
@@ -394,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < BK / 16; ++kk)
                         if (kk < ksteps)
                             ptx::mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                                          (kb | kk) != 0 ? 1u : 0u);
-                    ptx::mma_commit(&empty[stage]);
+                                          (kb != u.kb0 || kk != 0) ? 1u : 0u);
+                    ptx::mma_commit(&empty[ring.stage]);
                 }
                 if (ok) ptx::mma_commit(&tfull[acc]);
             }
@@ -406,29 +523,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            constexpr uint32_t kTx = GATHER ? C::kBBytes : C::kABytes + C::kBBytes;
-            uint32_t it = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const int m0 = (tile / p.n_tiles) * BM;
-                const int n0 = (tile % p.n_tiles) * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const uint32_t stage = it % S, round = it / S;
-                    if (!wait_bar(&empty[stage], (round & 1u) ^ 1u, wc, kRoleTma)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::mbar_arrive_expect_tx(&full_b[stage], kTx);
-                    if (!GATHER)
-                        ptx::tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full_b[stage],
-                                         kb * BK, m0);
-                    ptx::tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full_b[stage], kb * BK,
-                                     n0);
-                }
+            if (p.bres) {
+                // Weights resident: every K block of the one column tile, once.
+                ptx::mbar_arrive_expect_tx(bres_full,
+                                           static_cast<uint32_t>(p.num_kb) * C::kBBytes);
+                for (int kb = 0; kb < p.num_kb; ++kb)
+                    ptx::tma_load_2d(sB + kb * C::kBBytes, &tmap_b, bres_full, kb * BK, 0);
+                drain_wait(bres_full, 0u, 1000000000ull);
             }
-            // Wait (bounded) for the last loads so none lands after the CTA exits.
-            for (uint32_t i = it > (uint32_t)S ? it - S : 0; i < it; ++i)
-                drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
+            if (!p.bres || !GATHER) {
+                const uint32_t kTx = (p.bres ? 0u : static_cast<uint32_t>(C::kBBytes)) +
+                                     (GATHER ? 0u : static_cast<uint32_t>(kABytes));
+                Ring ring;
+                uint32_t issued = 0;
+                bool ok = true;
+                for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                    const Unit u = unit_of<BN>(p, tile);
+                    for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
+                        if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleTma)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::mbar_arrive_expect_tx(&full_b[ring.stage], kTx);
+                        if (!GATHER)
+                            ptx::tma_load_2d(sA + ring.stage * kABytes, &tmap_a, &full_b[ring.stage],
+                                             kb * BK, u.m0);
+                        if (!p.bres)
+                            ptx::tma_load_2d(sB + ring.stage * C::kBBytes, &tmap_b,
+                                             &full_b[ring.stage], kb * BK, u.n0);
+                    }
+                }
+                // Wait (bounded) for the last loads so none lands after the CTA exits.
+                const uint32_t first = issued > S ? issued - S : 0;
+                for (uint32_t i = first; i < issued; ++i)
+                    drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
+            }
         }
     }
 
@@ -459,24 +588,45 @@ __global__ void selftest_timeout_kernel(unsigned long long timeout_ns, unsigned*
     }
 }
 
+// y[m][co] = partial[m][co] + bias[co], rounded to bf16 or stored as fp32.
+__global__ void __launch_bounds__(256) finish_split_kernel(const float* __restrict__ partial,
+                                                           const uint16_t* __restrict__ bias,
+                                                           void* __restrict__ y, long long total,
+                                                           int C_out, int y_f32)
+{
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += stride) {
+        float v = partial[e];
+        if (bias != nullptr) v += bf16_bits_to_float(bias[e % C_out]);
+        if (y_f32) {
+            static_cast<float*>(y)[e] = v;
+        } else {
+            __nv_bfloat16 b = __float2bfloat16_rn(v);
+            static_cast<uint16_t*>(y)[e] = *reinterpret_cast<uint16_t*>(&b);
+        }
+    }
+}
+
 template <int BN, int AMODE>
 cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const IgemmParams& p,
                       cudaStream_t st)
 {
-    using C = Cfg<BN>;
     auto kern = igemm_kernel<BN, AMODE>;
     static int configured_for = -1;  // device for which the smem attribute was set
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
-    const int tiles = p.m_tiles * p.n_tiles;
+    const int smem = igemm_smem_bytes(BN, p.stages, p.bres, p.num_kb);
+    if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
+    const int tiles = p.m_tiles * p.n_tiles * p.splits;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    kern<<<grid, kThreads, C::kSmemBytes, st>>>(ta, tb, p);
+    kern<<<grid, kThreads, smem, st>>>(ta, tb, p);
     return cudaGetLastError();
 }
 
@@ -495,6 +645,19 @@ cudaError_t launch_mode(int bn, const CUtensorMap& ta, const CUtensorMap& tb, co
 
 }  // namespace
 
+int igemm_smem_bytes(int bn, int stages, int bres, int num_kb)
+{
+    const int b_blocks = bres ? num_kb : stages;
+    return kHeaderBytes + 1024 + b_blocks * bn * BK * 2 + stages * kABytes;
+}
+
+int igemm_pick_stages(int bn, int bres, int num_kb)
+{
+    for (int s = kMaxStages; s >= 2; --s)
+        if (igemm_smem_bytes(bn, s, bres, num_kb) <= kSmemLimit) return s;
+    return 0;
+}
+
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtensorMap& tb,
                          const IgemmParams& p, cudaStream_t st)
 {
@@ -502,8 +665,21 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kADense: return launch_mode<kADense>(bn, ta, tb, p, st);
     case kAGather: return launch_mode<kAGather>(bn, ta, tb, p, st);
     case kANarrow: return launch_mode<kANarrow>(bn, ta, tb, p, st);
+    case kATmaGather: return launch_mode<kATmaGather>(bn, ta, tb, p, st);
     default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_finish_split(const float* partial, const uint16_t* bias, void* y, long long M,
+                                int C_out, int y_f32, cudaStream_t st)
+{
+    const long long total = M * C_out;
+    long long blocks = (total + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms()) * 8;
+    if (blocks > cap) blocks = cap;
+    finish_split_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(partial, bias, y, total, C_out,
+                                                                  y_f32);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_selftest_timeout(unsigned long long timeout_ns, unsigned* err, cudaStream_t st)

@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/convgb.h"
+#include "convgb.h"  // include/ is on the include path
 #include "fastdiv.h"
 
 namespace convgb {
@@ -51,8 +51,14 @@ struct IgemmParams {
     FastDiv cin_div;         // divides a K index by C_in (gather) or by cp (narrow)
     FastDiv hwo_div;         // divides a row index by H_out*W_out (gather mode)
     long long img_elems;     // H*W*C_in (gather mode)
+    int img_rows;            // H*W: pixel rows per image (TMA gather mode)
+    int oob_row;             // a row index past the end of x viewed as [N*H*W][C_in]
     int num_kb;              // ceil(K / 64)
     int m_tiles, n_tiles;
+    int splits;              // K partitions per output tile (1: no split)
+    int stages;              // shared-memory ring depth (2..8)
+    int bres;                // 1: all of W's single column tile resident in shared memory
+    float* partial;          // splits > 1: fp32 [M][C_out] sums, zeroed before the launch
     int y_f32;               // 1: fp32 output, 0: bf16
     unsigned long long timeout_ns;
     unsigned* err;           // device error word
@@ -69,9 +75,17 @@ enum AMode : int {
     kADense = 0,   // TMA tiles of a dense [M][K] matrix (1x1 stride-1, full-spatial)
     kAGather = 1,  // cp.async 16-byte pixel chunks through the indirection buffer (C_in % 8 == 0)
     kANarrow = 2,  // scalar loads through the indirection buffer, channels padded to cp (stem)
+    kATmaGather = 3,  // TMA tile::gather4 of pixel rows named by the indirection buffer
+                      // (C_in % 64 == 0)
 };
+// Dynamic shared memory of one implicit-GEMM CTA, and the deepest ring that fits
+// (0 when none does).
+int igemm_smem_bytes(int bn, int stages, int bres, int num_kb);
+int igemm_pick_stages(int bn, int bres, int num_kb);
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& tmap_a,
                          const CUtensorMap& tmap_b, const IgemmParams& p, cudaStream_t st);
+cudaError_t launch_finish_split(const float* partial, const uint16_t* bias, void* y, long long M,
+                                int C_out, int y_f32, cudaStream_t st);
 cudaError_t launch_selftest_timeout(unsigned long long timeout_ns, unsigned* err,
                                     cudaStream_t st);
 

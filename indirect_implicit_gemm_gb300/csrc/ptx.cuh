@@ -62,8 +62,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 }
 
 // ---------------------------------------------------------------- fences
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy reads (tcgen05.mma operands) that a barrier makes depend on them.
+// Generic-proxy / async-proxy fence on shared memory: shared-memory writes
+// this thread has made or observed (through a barrier) in the generic proxy
+// become visible to its later async-proxy operations (tcgen05.mma reads).
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -92,12 +93,33 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Four rows of a 2-D tensor, chosen by row index, each `box` columns wide from
+// column c0, into four consecutive shared-memory rows at `dst` (tile::gather4;
+// the tensor map's box is one row high).  Rows outside the tensor read as zero.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int r0, int r1, int r2, int r3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(r0), "r"(r1),
+        "r"(r2), "r"(r3)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global->shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                  "r"(src_bytes)
+                 : "memory");
+}
+// Arrives on `bar` (without raising its expected count) once every cp.async
+// this thread issued so far has landed in shared memory.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit()

@@ -99,7 +99,18 @@ def test_path_selection(lib, cfg, path):
 
 def test_dense_path_needs_no_workspace(lib):
     assert lib.workspace_size(32, 256, 56, 56, 64, 1, 1, 1, 0, 1) == 0
-    assert lib.workspace_size(128, 512, 7, 7, 4096, 7, 7, 1, 0, 1) == 0
+    assert lib.workspace_size(32, 512, 7, 7, 2048, 1, 1, 1, 0, 1) == 0
+
+
+def test_split_k_only_for_underfilled_layers(lib):
+    # full-spatial 7x7 -> 4096 at N=128: 16 output tiles, K split, fp32 sums [128][4096]
+    assert lib.workspace_size(128, 512, 7, 7, 4096, 7, 7, 1, 0, 1) == 128 * 4096 * 4
+    # 512 channels at 7x7, N=128: 98 tiles, split; ibuf (49*9*4 -> 1792 B) + sums
+    assert lib.workspace_size(128, 512, 7, 7, 512, 3, 3, 1, 1, 1) == 1792 + 6272 * 512 * 4
+    # plenty of tiles: no split
+    assert lib.workspace_size(32, 64, 56, 56, 128, 3, 3, 1, 1, 1) == 56 * 56 * 9 * 4
+    # a split whose sums would not fit under half of im2col is not taken
+    assert lib.workspace_size(5, 16, 5, 6, 130, 5, 6, 1, 0, 1) == 0
     # asking for the gather path on a 1x1 layer costs only the indirection buffer
     assert lib.workspace_size(32, 256, 56, 56, 64, 1, 1, 1, 0, 1, path=lib.PATH_GATHER) == \
         56 * 56 * 4

@@ -70,6 +70,13 @@ SMALL = [
     S("dense_1x1", N=3, C_in=64, H=11, W=13, C_out=96, KH=1, KW=1, pad=0, seed=20),
     S("dense_1x1_ktail", N=2, C_in=72, H=9, W=9, C_out=40, KH=1, KW=1, pad=0, seed=21),
     S("dense_fullspatial", N=5, C_in=16, H=5, W=6, C_out=130, KH=5, KW=6, pad=0, seed=22),
+    S("dense_fullspatial_splitk", N=8, C_in=64, H=7, W=7, C_out=200, KH=7, KW=7, pad=0, seed=28),
+    S("gather_splitk_cout30", N=2, C_in=256, H=7, W=7, C_out=30, seed=29),
+    S("gather_splitk_cout64", N=2, C_in=256, H=7, W=7, C_out=64, seed=30),
+    S("tmagather_c128_s2_d2", N=2, C_in=128, H=17, W=15, C_out=96, stride=2, pad=2, dilation=2,
+      seed=31),
+    S("tmagather_c192_ragged", N=3, C_in=192, H=9, W=11, C_out=72, seed=32),
+    S("tmagather_c64_5x3", N=2, C_in=64, H=12, W=13, C_out=256, KH=5, KW=3, pad=2, seed=33),
     S("stem_c3_7x7_s2", N=2, C_in=3, H=30, W=26, C_out=64, KH=7, KW=7, stride=2, pad=3, seed=23),
     S("stem_c1", N=2, C_in=1, H=12, W=12, C_out=16, seed=24),
     S("stem_c5", N=1, C_in=5, H=10, W=11, C_out=40, seed=25),
