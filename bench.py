@@ -96,7 +96,7 @@ def shape_numbers(g, c: workloads.ConvShape):
                                             c.dilation),
                 im2win_bytes=g.im2win_bytes(c.N, c.C_in, c.H, c.W, c.KH, c.KW, c.stride, c.pad,
                                             c.dilation),
-                path={1: "gather", 2: "dense", 3: "stem"}.get(
+                path={1: "gather", 2: "dense", 3: "stem", 4: "window"}.get(
                     g.select_path(c.N, c.C_in, c.H, c.W, c.C_out, c.KH, c.KW, c.stride, c.pad,
                                   c.dilation), "?"))
 
@@ -246,7 +246,7 @@ class Layer:
                                    y=self.ys[i % self.sets])
 
     def launches_per_step(self):
-        return {"gather": 2, "dense": 1, "stem": 3}[self.num["path"]]
+        return {"gather": 2, "dense": 1, "stem": 3, "window": 1}[self.num["path"]]
 
 
 def time_layer(layer, steps, warmup, stream):
@@ -450,8 +450,12 @@ def main():
     ms_step = reduce_max(ms_total / args.steps, pg, dev)
     value = world * num["flops"] / (ms_step * 1e-3) / 1e12
 
-    # the dominant kernel alone (implicit GEMM), for the roofline
+    # the dominant kernel alone (implicit GEMM), for the roofline: timed on its
+    # own on the gather path (whose step also builds the indirection buffer);
+    # on single-launch paths the step is that kernel
     k_ms = time_gemm_kernel(layer, max(args.steps, 50), 5, stream)
+    if k_ms is None and layer.launches_per_step() == 1:
+        k_ms = time_layer(layer, max(args.steps, 50), 5, stream)
     t_roof, bound = roofline_time_s(num, peaks)
     roof = None
     if k_ms is not None:
@@ -465,7 +469,8 @@ def main():
             unit = "GB/s"
         roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": None,
-                "kernel": "igemm_kernel (gather, tcgen05)", "kernel_us": k_ms * 1e3,
+                "kernel": "igemm_kernel (%s path, tcgen05)" % num["path"],
+                "kernel_us": k_ms * 1e3,
                 "peak_source": "%s (MEASURED_PEAKS.json %s)" % (
                     peak_src, "bf16_tflops burst" if bound == "tensor" else "hbm_gbs"),
                 "roofline_us": t_roof * 1e6,

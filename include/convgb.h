@@ -76,7 +76,13 @@ typedef enum convgb_path {
     CONVGB_PATH_GATHER = 1,   /* implicit GEMM, A gathered through the indirection buffer */
     CONVGB_PATH_DENSE = 2,    /* plain GEMM: 1x1 stride-1 unpadded, or a kernel covering the
                                  whole unpadded image (a dense layer); no workspace */
-    CONVGB_PATH_STEM = 3      /* tiny C_in (not a multiple of 8): channels padded to 8 */
+    CONVGB_PATH_STEM = 3,     /* C_in not a multiple of 8: each tap's channels padded to 4
+                                 (C_in <= 4) or to a multiple of 8, scalar gather */
+    CONVGB_PATH_WINDOW = 4    /* stride 1, C_in % 64 == 0, W_out + (KW-1)*d <= 128 and
+                                 (KW-1)*d <= 8: tiles of whole output rows; each input row
+                                 is staged in shared memory once per (kh, 64-channel block)
+                                 by TMA and read by all KW taps ("Im2win", Abstract: the
+                                 window order and its continuous accesses, on chip) */
 } convgb_path;
 
 /* Short English text for a status code; never NULL. */
@@ -118,12 +124,14 @@ CONVGB_API size_t convgb_im2col_bytes(int N, int C_in, int H, int W, int KH, int
  * conv2d_fwd -- forward convolution, y = conv(x, w) + bias.
  *
  * Defined by the formula at the top of this file.  Picks a path with
- * convgb_select_path(): the indirection-buffer implicit GEMM in general, a
- * plain GEMM for 1x1 stride-1 unpadded layers ("The Indirect Convolution
- * Algorithm", Abstract: 1x1 convolutions are directly a GEMM) and for kernels
- * that cover the whole unpadded image ("Unifying Convolutions and GEMM",
- * section 4: such a convolution is a dense layer), and a channel-padding stem
- * path when C_in is not a multiple of 8.
+ * convgb_select_path(): a plain GEMM for 1x1 stride-1 unpadded layers ("The
+ * Indirect Convolution Algorithm", Abstract: 1x1 convolutions are directly a
+ * GEMM) and for kernels that cover the whole unpadded image ("Unifying
+ * Convolutions and GEMM", section 4: such a convolution is a dense layer); a
+ * channel-padding stem path when C_in is not a multiple of 8; the window path
+ * for the stride-1 layers it covers; the indirection-buffer implicit GEMM for
+ * everything else (strided, dilated beyond the window limits, other channel
+ * counts).
  *
  *   x         device, bf16 [N][H][W][C_in]
  *   w         device, bf16 [C_out][KH][KW][C_in]

@@ -76,10 +76,23 @@ bool is_full_spatial(const ConvShape& c)
     return c.KH == c.H && c.KW == c.W && c.p == 0 && c.d == 1;  // H_out = W_out = 1
 }
 
+// Window mode geometry: stride-1 layers whose 64-channel blocks stay inside
+// one tap and whose output rows, padded by the tap spill, fit a 128-row tile.
+bool window_geometry(const ConvShape& c)
+{
+    const int wv = c.W_out + (c.KW - 1) * c.d;
+    return c.s == 1 && c.C_in % 64 == 0 && wv <= 128 && (c.KW - 1) * c.d <= 8;
+}
+
+struct GemmPlan;
+GemmPlan plan_gemm(int path, const ConvShape& c);
+bool window_applies(const ConvShape& c);
+
 // Whether `path` can compute this shape.
 bool path_supports(int path, const ConvShape& c)
 {
     switch (path) {
+    case CONVGB_PATH_WINDOW: return window_applies(c);
     case CONVGB_PATH_GATHER: return c.C_in % 8 == 0;
     case CONVGB_PATH_DENSE: return c.C_in % 8 == 0 && (is_pointwise(c) || is_full_spatial(c));
     case CONVGB_PATH_STEM: return c.C_in % 8 != 0;
@@ -91,6 +104,7 @@ int select_path(const ConvShape& c)
 {
     if (path_supports(CONVGB_PATH_DENSE, c)) return CONVGB_PATH_DENSE;
     if (c.C_in % 8 != 0) return CONVGB_PATH_STEM;
+    if (path_supports(CONVGB_PATH_WINDOW, c)) return CONVGB_PATH_WINDOW;
     return CONVGB_PATH_GATHER;
 }
 
@@ -135,6 +149,23 @@ bool encode_kmajor(CUtensorMap* m, const void* base, long long rows, long long c
     return r == CUDA_SUCCESS;
 }
 
+// x [N][H][W][C_in] as a 4-D tensor, box = 64 channels x `wv` pixels of one
+// row, 128-byte swizzle: one staged input row of the window mode.
+bool encode_window(CUtensorMap* m, const void* x, int N, int H, int W, int C_in, int wv)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)C_in, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
+    cuuint64_t strides[3] = {(cuuint64_t)C_in * 2, (cuuint64_t)W * C_in * 2,
+                             (cuuint64_t)H * W * C_in * 2};
+    cuuint32_t box[4] = {64u, (cuuint32_t)wv, 1u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int pick_bn(int C_out)
 {
     if (C_out <= 32) return 32;
@@ -150,6 +181,10 @@ struct GemmPlan {
     int splits = 1;
     int stages = 0;  // shared-memory ring depth
     int bres = 0;    // weights resident in shared memory
+    int m_step = 128;
+    int a_stage_bytes = 128 * 64 * 2;
+    int b_per_stage = 1;
+    int win_wv = 0, win_rows = 0;  // window mode geometry
     long long M = 0, K = 0;
     int num_kb = 0, m_tiles = 0, n_tiles = 0;
 };
@@ -182,6 +217,38 @@ int choose_splits(long long tiles, int num_kb, long long partial_bytes, long lon
 GemmPlan plan_gemm(int path, const ConvShape& c)
 {
     GemmPlan g;
+    if (path == CONVGB_PATH_WINDOW && window_geometry(c)) {
+        g.amode = kAWindow;
+        g.M = c.M;
+        g.K = c.K;
+        g.win_wv = c.W_out + (c.KW - 1) * c.d;
+        g.win_rows = 128 / g.win_wv;
+        g.m_step = g.win_rows;
+        g.a_stage_bytes = window_stage_rows(c.KW, c.d) * 128;
+        g.num_kb = c.KH * (c.C_in / 64);  // one K block per (kh, 64-channel block)
+        g.m_tiles = (int)(((long long)c.N * c.H_out + g.win_rows - 1) / g.win_rows);
+        g.bn = pick_bn(c.C_out);
+        g.n_tiles = (c.C_out + g.bn - 1) / g.bn;
+        const int all_kb = c.KH * c.KW * (c.C_in / 64);
+        if (g.n_tiles == 1 && igemm_pick_stages(g.bn, 1, all_kb, g.a_stage_bytes, 1) >= 3) {
+            g.bres = 1;
+            g.b_per_stage = 1;
+            g.stages = igemm_pick_stages(g.bn, 1, all_kb, g.a_stage_bytes, 1);
+        } else {
+            // Streamed weights: a slot holds the KW blocks of one (kh, cc); keep
+            // the column tile at 128 so at least two slots fit.
+            if (g.bn > 128) {
+                g.bn = 128;
+                g.n_tiles = (c.C_out + 127) / 128;
+            }
+            g.b_per_stage = c.KW;
+            g.stages = igemm_pick_stages(g.bn, 0, 0, g.a_stage_bytes, c.KW);
+        }
+        const long long im2col = c.M * c.K * 2;
+        const long long partial = c.M * c.C_out * 4;
+        g.splits = choose_splits((long long)g.m_tiles * g.n_tiles, g.num_kb, partial, im2col / 2);
+        return g;  // stages == 0 (nothing fits): see window_applies()
+    }
     // Gather path: TMA gather4 when a 64-column K block stays inside one tap's
     // channels, 16-byte cp.async otherwise.
     g.amode = path == CONVGB_PATH_DENSE  ? kADense
@@ -200,10 +267,17 @@ GemmPlan plan_gemm(int path, const ConvShape& c)
     // Gathered layers whose whole weight matrix is one column tile: keep it in
     // shared memory for the CTA's lifetime when that still leaves a 4-deep A ring.
     if (g.amode != kADense && g.n_tiles == 1 && g.splits == 1 &&
-        igemm_pick_stages(g.bn, 1, g.num_kb) >= 4)
+        igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
         g.bres = 1;
-    g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb);
+    g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb, g.a_stage_bytes, 1);
     return g;
+}
+
+// The window path also needs two ring slots (staged rows plus, unless the
+// weights stay resident, the KW weight blocks of one (kh, cc)) to fit.
+bool window_applies(const ConvShape& c)
+{
+    return window_geometry(c) && plan_gemm(CONVGB_PATH_WINDOW, c).stages >= 2;
 }
 
 // Workspace regions of each path, in order; every region starts 256-byte aligned.
@@ -250,6 +324,7 @@ struct IgemmArgs {
     long long k_valid = 0, img_elems = 0;
     int img_rows = 0;    // H*W
     long long x_rows = 0;  // N*H*W
+    const ConvShape* shape = nullptr;  // window mode geometry
 };
 
 // Tensor maps and kernel parameters, all host-side: nothing is launched here,
@@ -271,6 +346,10 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     // TMA gather: x as [N*H*W][C_in], one-row boxes of 64 channels.
     if (g.amode == kATmaGather && !encode_kmajor(&out->ta, a.x, a.x_rows, a.C_in, 1))
         return CONVGB_ERR_CUDA;
+    if (g.amode == kAWindow) {
+        const ConvShape& c = *a.shape;
+        if (!encode_window(&out->ta, a.x, c.N, c.H, c.W, c.C_in, g.win_wv)) return CONVGB_ERR_CUDA;
+    }
     unsigned* err = device_error_word();
     if (!err) return CONVGB_ERR_CUDA;
     IgemmParams& p = out->p;
@@ -291,11 +370,27 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     p.img_rows = a.img_rows;
     p.oob_row = (int)a.x_rows;
     p.num_kb = g.num_kb;
+    p.kb_total = (int)((g.K + 63) / 64);
     p.m_tiles = g.m_tiles;
     p.n_tiles = g.n_tiles;
     p.splits = g.splits;
     p.stages = g.stages;
     p.bres = g.bres;
+    p.m_step = g.m_step;
+    p.a_stage_bytes = g.a_stage_bytes;
+    p.b_per_stage = g.b_per_stage;
+    if (g.amode == kAWindow) {
+        const ConvShape& c = *a.shape;
+        p.win_wv = g.win_wv;
+        p.win_rows = g.win_rows;
+        p.win_groups = c.N * c.H_out;
+        p.win_wout = c.W_out;
+        p.win_kw = c.KW;
+        p.win_d = c.d;
+        p.win_pad = c.p;
+        p.win_cc = c.C_in / 64;
+        p.ho_div = FastDiv((uint32_t)c.H_out);
+    }
     if (g.stages < 2) return CONVGB_ERR_UNSUPPORTED;
     p.partial = a.partial;
     p.y_f32 = a.y_f32;
@@ -331,7 +426,8 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
     if (!x || !w || !y) return CONVGB_ERR_INVALID_ARG;
     if (y_dtype != CONVGB_BF16 && y_dtype != CONVGB_F32) return CONVGB_ERR_INVALID_ARG;
     if (path == CONVGB_PATH_AUTO) path = select_path(c);
-    if (path != CONVGB_PATH_GATHER && path != CONVGB_PATH_DENSE && path != CONVGB_PATH_STEM)
+    if (path != CONVGB_PATH_GATHER && path != CONVGB_PATH_DENSE && path != CONVGB_PATH_STEM &&
+        path != CONVGB_PATH_WINDOW)
         return CONVGB_ERR_INVALID_ARG;
     if (!path_supports(path, c)) return CONVGB_ERR_UNSUPPORTED;
     WsLayout L = workspace_layout(path, c);
@@ -356,6 +452,10 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
     if (path == CONVGB_PATH_DENSE) {
         // 1x1 stride-1: A = x as [N*H*W][C_in]; full-spatial: A = x as [N][H*W*C_in].
         a.a_dense = x;
+    } else if (path == CONVGB_PATH_WINDOW) {
+        a.x = static_cast<const uint16_t*>(x);
+        a.C_in = C_in;
+        a.shape = &c;
     } else {
         ibuf = reinterpret_cast<int32_t*>(wsb + L.ibuf_off);
         a.x = static_cast<const uint16_t*>(x);
@@ -366,6 +466,7 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
         a.img_elems = (long long)H * W * C_in;
         a.img_rows = H * W;
         a.x_rows = (long long)N * H * W;
+        a.shape = &c;
         if (path == CONVGB_PATH_STEM) {
             // Weights re-packed with each tap's channels padded to cp.
             a.cp = stem_cp(c);

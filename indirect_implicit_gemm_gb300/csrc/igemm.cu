@@ -180,7 +180,8 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, int m, int co0
     }
 }
 
-// Work unit `tile` -> output tile origin and K-block range.  Units are ordered
+// Work unit `tile` -> output tile origin (first GEMM row, or first output row
+// in window mode) and K-block range.  Units are ordered
 // (m tile, n tile, K split) with the split fastest, then the n tile, so CTAs
 // working at the same time share A rows in L2.
 struct Unit {
@@ -192,7 +193,7 @@ __device__ __forceinline__ Unit unit_of(const IgemmParams& p, int tile)
     const int ks = tile % p.splits;
     const int mn = tile / p.splits;
     Unit u;
-    u.m0 = (mn / p.n_tiles) * BM;
+    u.m0 = (mn / p.n_tiles) * p.m_step;
     u.n0 = (mn % p.n_tiles) * BN;
     u.kb0 = static_cast<int>(static_cast<long long>(ks) * p.num_kb / p.splits);
     u.kb1 = static_cast<int>(static_cast<long long>(ks + 1) * p.num_kb / p.splits);
@@ -225,8 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap tmap_b, const IgemmParams p)
 {
     using C = Cfg<BN>;
-    constexpr bool GATHER = AMODE != kADense;
+    // A written by the gather warps (signalled on full_a) or by the TMA warp
+    // together with B (signalled on full_b).
+    constexpr bool GATHER = AMODE == kAGather || AMODE == kANarrow || AMODE == kATmaGather;
+    constexpr bool WINDOW = AMODE == kAWindow;
     const uint32_t S = static_cast<uint32_t>(p.stages);
+    const uint32_t AST = static_cast<uint32_t>(p.a_stage_bytes);
     extern __shared__ uint8_t smem_raw[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
     uint64_t* full_a = bars;                  // A stage ready
@@ -243,7 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = ptx::smem_addr(smem_raw) + kHeaderBytes;
     uint8_t* data = smem_raw + kHeaderBytes + ((1024u - (base & 1023u)) & 1023u);
     uint8_t* sB = data;
-    const uint32_t b_blocks = p.bres ? static_cast<uint32_t>(p.num_kb) : S;
+    const uint32_t b_blocks =
+        p.bres ? static_cast<uint32_t>(p.kb_total) : S * static_cast<uint32_t>(p.b_per_stage);
     uint8_t* sA = data + b_blocks * C::kBBytes;
 
     const int warp = threadIdx.x >> 5;
@@ -266,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_barrier_init();
     }
     if (warp == kTmaWarp && lane == 0) {
-        if (AMODE == kADense || AMODE == kATmaGather) ptx::prefetch_tensormap(&tmap_a);
+        if (AMODE == kADense || AMODE == kATmaGather || WINDOW) ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == kMmaWarp) {
@@ -283,6 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kEpiWarps) {
         // ------------------------------------------------------------ epilogue
+        // This thread's accumulator row r = TMEM lane.  Window mode: row r is
+        // virtual pixel (wrow, wcol) of the tile's output rows; spill columns
+        // (wcol >= W_out) and rows past the tile's output rows are discarded.
+        const int r = warp * 32 + lane;
+        const int wrow = WINDOW ? r / p.win_wv : 0;
+        const int wcol = WINDOW ? r - wrow * p.win_wv : 0;
         uint32_t lt = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
             const Unit u = unit_of<BN>(p, tile);
@@ -291,7 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ready = wait_bar(&tfull[acc], use & 1u, wc, kRoleEpilogue);
             if (!__all_sync(0xffffffffu, ready)) break;
             ptx::tc_fence_after();
-            const int m = u.m0 + warp * 32 + lane;
+            int m = u.m0 + r;
+            if (WINDOW) {
+                const int g = u.m0 + wrow;  // output row n*H_out + ho
+                const bool real = wrow < p.win_rows && wcol < p.win_wout && g < p.win_groups;
+                m = real ? g * p.win_wout + wcol : p.M;
+            }
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
@@ -358,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (lane == 0) ptx::mbar_arrive_expect_tx(&full_a[ring.stage], kABytes);
                     __syncwarp();
-                    ptx::tma_gather4(sA + ring.stage * kABytes + lane * 4 * 128, &tmap_a,
+                    ptx::tma_gather4(sA + ring.stage * AST + lane * 4 * 128, &tmap_a,
                                      &full_a[ring.stage], static_cast<int>(c0), row[0], row[1],
                                      row[2], row[3]);
                 }
@@ -415,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const int k = kb * BK + c * 8;
-                    uint8_t* stage_a = sA + ring.stage * kABytes;
+                    uint8_t* stage_a = sA + ring.stage * AST;
                     if (AMODE == kAGather) {
                         // C_in % 8 == 0: the chunk is 8 channels of one tap's pixel.
                         // The indirection entries of this K block were loaded one
@@ -491,7 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (!p.bres && !wait_bar(&full_b[ring.stage], ring.phase, wc, kRoleMma)) {
+                    if ((!GATHER || !p.bres) &&
+                        !wait_bar(&full_b[ring.stage], ring.phase, wc, kRoleMma)) {
                         ok = false;
                         break;
                     }
@@ -499,19 +517,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // tensor core through the async proxy.
                     if (AMODE == kAGather || AMODE == kANarrow) ptx::fence_proxy_async_smem();
                     ptx::tc_fence_after();
-                    const uint64_t adesc =
-                        ptx::sdesc_k_major_sw128(ptx::smem_addr(sA + ring.stage * kABytes));
-                    const uint32_t bblk = p.bres ? static_cast<uint32_t>(kb) : ring.stage;
-                    const uint64_t bdesc =
-                        ptx::sdesc_k_major_sw128(ptx::smem_addr(sB + bblk * C::kBBytes));
-                    // The last K block may hold fewer than 64 columns: skip the
-                    // all-zero 16-column steps.
-                    const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
+                    const uint32_t a_base = ptx::smem_addr(sA + ring.stage * AST);
+                    if (WINDOW) {
+                        // One staged (kh, cc) block feeds every kw tap: tap kw reads
+                        // the staging rows shifted down by kw*d.
+                        const int kh = kb / p.win_cc, cc = kb - kh * p.win_cc;
+                        for (int kw = 0; kw < p.win_kw; ++kw) {
+                            const uint32_t shift = static_cast<uint32_t>(kw * p.win_d);
+                            const uint64_t adesc = ptx::sdesc_k_major_sw128(a_base + shift * 128u);
+                            const uint32_t bblk =
+                                p.bres ? static_cast<uint32_t>((kh * p.win_kw + kw) * p.win_cc + cc)
+                                       : ring.stage * p.b_per_stage + kw;
+                            const uint64_t bdesc =
+                                ptx::sdesc_k_major_sw128(ptx::smem_addr(sB + bblk * C::kBBytes));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        if (kk < ksteps)
-                            ptx::mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                                          (kb != u.kb0 || kk != 0) ? 1u : 0u);
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                ptx::mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                              (kb != u.kb0 || kw != 0 || kk != 0) ? 1u : 0u);
+                        }
+                    } else {
+                        const uint64_t adesc = ptx::sdesc_k_major_sw128(a_base);
+                        const uint32_t bblk = p.bres ? static_cast<uint32_t>(kb) : ring.stage;
+                        const uint64_t bdesc =
+                            ptx::sdesc_k_major_sw128(ptx::smem_addr(sB + bblk * C::kBBytes));
+                        // The last K block may hold fewer than 64 columns: skip the
+                        // all-zero 16-column steps.
+                        const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            if (kk < ksteps)
+                                ptx::mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                              (kb != u.kb0 || kk != 0) ? 1u : 0u);
+                    }
                     ptx::mma_commit(&empty[ring.stage]);
                 }
                 if (ok) ptx::mma_commit(&tfull[acc]);
@@ -526,12 +563,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.bres) {
                 // Weights resident: every K block of the one column tile, once.
                 ptx::mbar_arrive_expect_tx(bres_full,
-                                           static_cast<uint32_t>(p.num_kb) * C::kBBytes);
-                for (int kb = 0; kb < p.num_kb; ++kb)
+                                           static_cast<uint32_t>(p.kb_total) * C::kBBytes);
+                for (int kb = 0; kb < p.kb_total; ++kb)
                     ptx::tma_load_2d(sB + kb * C::kBBytes, &tmap_b, bres_full, kb * BK, 0);
                 drain_wait(bres_full, 0u, 1000000000ull);
             }
-            if (!p.bres || !GATHER) {
+            if (WINDOW) {
+                // Per (tile, kh, cc): one box of win_wv pixels x 64 channels for each
+                // of the tile's output rows (input row ho - p + kh*d, columns -p ..
+                // -p + win_wv - 1; TMA zero-fills what lies outside the image), plus
+                // the KW weight blocks (kh, 0..KW-1, cc) unless weights are resident.
+                const uint32_t row_bytes = static_cast<uint32_t>(p.win_wv) * 128u;
+                Ring ring;
+                uint32_t issued = 0;
+                bool ok = true;
+                for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                    const Unit u = unit_of<BN>(p, tile);
+                    const int rows = min(p.win_rows, p.win_groups - u.m0);
+                    for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
+                        if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleTma)) {
+                            ok = false;
+                            break;
+                        }
+                        const int kh = kb / p.win_cc, cc = kb - kh * p.win_cc;
+                        const uint32_t tx =
+                            static_cast<uint32_t>(rows) * row_bytes +
+                            (p.bres ? 0u : static_cast<uint32_t>(p.win_kw) * C::kBBytes);
+                        ptx::mbar_arrive_expect_tx(&full_b[ring.stage], tx);
+                        uint8_t* stage_a = sA + ring.stage * AST;
+                        for (int j = 0; j < rows; ++j) {
+                            uint32_t n, ho;
+                            p.ho_div.divmod(static_cast<uint32_t>(u.m0 + j), n, ho);
+                            ptx::tma_load_4d(stage_a + j * row_bytes, &tmap_a, &full_b[ring.stage],
+                                             cc * BK, -p.win_pad,
+                                             static_cast<int>(ho) - p.win_pad + kh * p.win_d,
+                                             static_cast<int>(n));
+                        }
+                        if (!p.bres)
+                            for (int kw = 0; kw < p.win_kw; ++kw)
+                                ptx::tma_load_2d(
+                                    sB + (ring.stage * p.b_per_stage + kw) * C::kBBytes, &tmap_b,
+                                    &full_b[ring.stage], ((kh * p.win_kw + kw) * p.win_cc + cc) * BK,
+                                    u.n0);
+                    }
+                }
+                const uint32_t first = issued > S ? issued - S : 0;
+                for (uint32_t i = first; i < issued; ++i)
+                    drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
+            } else if (!p.bres || !GATHER) {
                 const uint32_t kTx = (p.bres ? 0u : static_cast<uint32_t>(C::kBBytes)) +
                                      (GATHER ? 0u : static_cast<uint32_t>(kABytes));
                 Ring ring;
@@ -546,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         ptx::mbar_arrive_expect_tx(&full_b[ring.stage], kTx);
                         if (!GATHER)
-                            ptx::tma_load_2d(sA + ring.stage * kABytes, &tmap_a, &full_b[ring.stage],
+                            ptx::tma_load_2d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, u.m0);
                         if (!p.bres)
                             ptx::tma_load_2d(sB + ring.stage * C::kBBytes, &tmap_b,
@@ -622,7 +701,8 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const IgemmP
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
-    const int smem = igemm_smem_bytes(BN, p.stages, p.bres, p.num_kb);
+    const int smem = igemm_smem_bytes(BN, p.stages, p.bres, p.kb_total, p.a_stage_bytes,
+                                      p.b_per_stage);
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
     const int tiles = p.m_tiles * p.n_tiles * p.splits;
     const int grid = tiles < num_sms() ? tiles : num_sms();
@@ -645,18 +725,22 @@ cudaError_t launch_mode(int bn, const CUtensorMap& ta, const CUtensorMap& tb, co
 
 }  // namespace
 
-int igemm_smem_bytes(int bn, int stages, int bres, int num_kb)
+int igemm_smem_bytes(int bn, int stages, int bres, int num_kb, int a_stage_bytes,
+                     int b_per_stage)
 {
-    const int b_blocks = bres ? num_kb : stages;
-    return kHeaderBytes + 1024 + b_blocks * bn * BK * 2 + stages * kABytes;
+    const int b_blocks = bres ? num_kb : stages * b_per_stage;
+    return kHeaderBytes + 1024 + b_blocks * bn * BK * 2 + stages * a_stage_bytes;
 }
 
-int igemm_pick_stages(int bn, int bres, int num_kb)
+int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per_stage)
 {
     for (int s = kMaxStages; s >= 2; --s)
-        if (igemm_smem_bytes(bn, s, bres, num_kb) <= kSmemLimit) return s;
+        if (igemm_smem_bytes(bn, s, bres, num_kb, a_stage_bytes, b_per_stage) <= kSmemLimit)
+            return s;
     return 0;
 }
+
+int window_stage_rows(int kw, int d) { return (BM + (kw - 1) * d + 7) / 8 * 8; }
 
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtensorMap& tb,
                          const IgemmParams& p, cudaStream_t st)
@@ -666,6 +750,7 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kAGather: return launch_mode<kAGather>(bn, ta, tb, p, st);
     case kANarrow: return launch_mode<kANarrow>(bn, ta, tb, p, st);
     case kATmaGather: return launch_mode<kATmaGather>(bn, ta, tb, p, st);
+    case kAWindow: return launch_mode<kAWindow>(bn, ta, tb, p, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -53,10 +53,18 @@ struct IgemmParams {
     long long img_elems;     // H*W*C_in (gather mode)
     int img_rows;            // H*W: pixel rows per image (TMA gather mode)
     int oob_row;             // a row index past the end of x viewed as [N*H*W][C_in]
-    int num_kb;              // ceil(K / 64)
+    int num_kb;              // K blocks per output tile (window mode: KH * C_in/64 stagings)
+    int kb_total;            // 64-column blocks of W_row: ceil(K / 64)
     int m_tiles, n_tiles;
+    int m_step;              // tile origin step: 128 GEMM rows, or win_rows output rows
     int splits;              // K partitions per output tile (1: no split)
     int stages;              // shared-memory ring depth (2..8)
+    int a_stage_bytes;       // bytes of one A ring slot
+    int b_per_stage;         // B K-blocks per ring slot (1; KW in window mode)
+    // window mode (stride 1): tile = win_rows output rows of win_wv virtual
+    // pixels (W_out real + (KW-1)*d spill); K block kb = (kh, cc)
+    int win_wv, win_rows, win_groups, win_wout, win_kw, win_d, win_pad, win_cc;
+    FastDiv ho_div;          // divides an output-row index (n*H_out + ho) by H_out
     int bres;                // 1: all of W's single column tile resident in shared memory
     float* partial;          // splits > 1: fp32 [M][C_out] sums, zeroed before the launch
     int y_f32;               // 1: fp32 output, 0: bf16
@@ -77,11 +85,16 @@ enum AMode : int {
     kANarrow = 2,  // scalar loads through the indirection buffer, channels padded to cp (stem)
     kATmaGather = 3,  // TMA tile::gather4 of pixel rows named by the indirection buffer
                       // (C_in % 64 == 0)
+    kAWindow = 4,     // stride 1: whole output rows per tile; each input row is staged once
+                      // per (kh, 64-channel block) and read by all KW taps at shifted starts
 };
 // Dynamic shared memory of one implicit-GEMM CTA, and the deepest ring that fits
 // (0 when none does).
-int igemm_smem_bytes(int bn, int stages, int bres, int num_kb);
-int igemm_pick_stages(int bn, int bres, int num_kb);
+int igemm_smem_bytes(int bn, int stages, int bres, int num_kb, int a_stage_bytes,
+                     int b_per_stage);
+int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per_stage);
+// Rows of an A ring slot in window mode (128 plus the tap spill, rounded to 8).
+int window_stage_rows(int kw, int d);
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& tmap_a,
                          const CUtensorMap& tmap_b, const IgemmParams& p, cudaStream_t st);
 cudaError_t launch_finish_split(const float* partial, const uint16_t* bias, void* y, long long M,

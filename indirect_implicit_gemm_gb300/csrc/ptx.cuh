@@ -93,6 +93,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// 4-D tiled bulk tensor load (c0 innermost); out-of-range coordinates, negative
+// ones included, read as zero.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3)
+        : "memory");
+}
+
 // Four rows of a 2-D tensor, chosen by row index, each `box` columns wide from
 // column c0, into four consecutive shared-memory rows at `dst` (tile::gather4;
 // the tensor map's box is one row high).  Rows outside the tensor read as zero.
@@ -213,6 +226,11 @@ __device__ __forceinline__ void tmem_ld_wait()
 // r*128 + ((c ^ (r & 7)) * 16), 8-row groups 1024 bytes apart.  The tile must
 // start on a 1024-byte boundary; stepping K by 16 elements inside the 128-byte
 // row adds 32 bytes to the start address.
+//
+// The swizzle is applied to absolute shared-memory addresses, the same way
+// TMA writes it, so an operand may also start a whole number of 128-byte rows
+// into a tile (the window mode's shifted taps) with the base-offset field left
+// at 0; measured on GB300: a non-zero base offset there reads the wrong rows.
 __device__ __forceinline__ uint64_t sdesc_k_major_sw128(uint32_t saddr)
 {
     uint64_t d = 0;

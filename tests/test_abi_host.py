@@ -86,11 +86,21 @@ def test_sizes_and_workspace_below_im2col(lib, cfg):
     assert ws < im2col, (ws, im2col)
 
 
+def expected_path(c):
+    if c.KH == 1 or "fullspatial" in c.name:
+        return 2  # dense GEMM
+    if c.C_in % 8:
+        return 3  # stem
+    wv = oracle.output_size(c.W, c.KW, c.stride, c.pad, c.dilation) + (c.KW - 1) * c.dilation
+    if c.stride == 1 and c.C_in % 64 == 0 and wv <= 128 and (c.KW - 1) * c.dilation <= 8:
+        return 4  # window
+    return 1  # indirection-buffer gather
+
+
 @pytest.mark.parametrize("cfg,path", [
-    (workloads.TINY, 3), (workloads.RESNET_3X3, 1), (workloads.POINTWISE_S1, 2),
+    (workloads.TINY, 3), (workloads.RESNET_3X3, 4), (workloads.POINTWISE_S1, 2),
     (workloads.POINTWISE_S2, 1), (workloads.STEM_7X7, 3), (workloads.STRIDED_3X3, 1),
-] + [(c, 2 if (c.KH == 1 or "fullspatial" in c.name) else (3 if c.C_in % 8 else 1))
-     for c in workloads.SWEEP], ids=lambda v: getattr(v, "name", str(v)))
+] + [(c, expected_path(c)) for c in workloads.SWEEP], ids=lambda v: getattr(v, "name", str(v)))
 def test_path_selection(lib, cfg, path):
     got = lib.select_path(cfg.N, cfg.C_in, cfg.H, cfg.W, cfg.C_out, cfg.KH, cfg.KW, cfg.stride,
                           cfg.pad, cfg.dilation)
@@ -105,10 +115,15 @@ def test_dense_path_needs_no_workspace(lib):
 def test_split_k_only_for_underfilled_layers(lib):
     # full-spatial 7x7 -> 4096 at N=128: 16 output tiles, K split, fp32 sums [128][4096]
     assert lib.workspace_size(128, 512, 7, 7, 4096, 7, 7, 1, 0, 1) == 128 * 4096 * 4
-    # 512 channels at 7x7, N=128: 98 tiles, split; ibuf (49*9*4 -> 1792 B) + sums
-    assert lib.workspace_size(128, 512, 7, 7, 512, 3, 3, 1, 1, 1) == 1792 + 6272 * 512 * 4
-    # plenty of tiles: no split
-    assert lib.workspace_size(32, 64, 56, 56, 128, 3, 3, 1, 1, 1) == 56 * 56 * 9 * 4
+    # the same 512-channel 7x7 layer on the gather path: 98 tiles, split;
+    # ibuf (49*9*4 -> 1792 B) + sums.  The window path tiles it 256 ways: no split.
+    assert lib.workspace_size(128, 512, 7, 7, 512, 3, 3, 1, 1, 1, path=lib.PATH_GATHER) == \
+        1792 + 6272 * 512 * 4
+    assert lib.workspace_size(128, 512, 7, 7, 512, 3, 3, 1, 1, 1) == 0
+    # plenty of tiles: no split; the gather path needs only its indirection buffer
+    assert lib.workspace_size(32, 64, 56, 56, 128, 3, 3, 1, 1, 1, path=lib.PATH_GATHER) == \
+        56 * 56 * 9 * 4
+    assert lib.workspace_size(32, 64, 56, 56, 128, 3, 3, 1, 1, 1) == 0
     # a split whose sums would not fit under half of im2col is not taken
     assert lib.workspace_size(5, 16, 5, 6, 130, 5, 6, 1, 0, 1) == 0
     # asking for the gather path on a 1x1 layer costs only the indirection buffer
@@ -139,7 +154,7 @@ def call(lib, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(N=0), 1), (dict(C_in=0), 1), (dict(KH=0), 1), (dict(s=0), 1), (dict(p=-1), 1),
     (dict(d=0), 1), (dict(H=2, p=0), 1), (dict(x=0), 1), (dict(w=0), 1), (dict(y=0), 1),
-    (dict(yd=7), 1), (dict(path=9), 1), (dict(path=2), 2), (dict(path=3), 2),
+    (dict(yd=7), 1), (dict(path=9), 1), (dict(path=2), 2), (dict(path=3), 2), (dict(path=4), 2),
     (dict(wsb=16), 3), (dict(ws=0), 1), (dict(x=0x1008), 4), (dict(y=0x3004), 4),
     (dict(b=0x5002), 4), (dict(N=1 << 20, H=1 << 10, W=1 << 10), 2),
 ])

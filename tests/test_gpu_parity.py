@@ -77,6 +77,12 @@ SMALL = [
       seed=31),
     S("tmagather_c192_ragged", N=3, C_in=192, H=9, W=11, C_out=72, seed=32),
     S("tmagather_c64_5x3", N=2, C_in=64, H=12, W=13, C_out=256, KH=5, KW=3, pad=2, seed=33),
+    S("window_c64_d2", N=2, C_in=64, H=20, W=21, C_out=48, pad=2, dilation=2, seed=34),
+    S("window_c128_7x7_many_rows", N=3, C_in=128, H=7, W=7, C_out=64, seed=35),
+    S("window_c64_cout200_streamed", N=2, C_in=64, H=11, W=13, C_out=200, seed=36),
+    S("window_c64_5x5", N=1, C_in=64, H=16, W=18, C_out=32, KH=5, KW=5, pad=2, seed=37),
+    S("window_c64_1x3", N=2, C_in=64, H=6, W=30, C_out=40, KH=1, KW=3, pad=1, seed=38),
+    S("window_c64_wide_row", N=1, C_in=64, H=4, W=126, C_out=64, seed=39),
     S("stem_c3_7x7_s2", N=2, C_in=3, H=30, W=26, C_out=64, KH=7, KW=7, stride=2, pad=3, seed=23),
     S("stem_c1", N=2, C_in=1, H=12, W=12, C_out=16, seed=24),
     S("stem_c5", N=1, C_in=5, H=10, W=11, C_out=40, seed=25),
@@ -95,6 +101,21 @@ def test_conv_small_shapes_match_oracle(gpu_lib, shape, out_dtype):
 @pytest.mark.parametrize("shape", SMALL[:3] + SMALL[9:13], ids=lambda s: s.name)
 def test_conv_without_bias(gpu_lib, shape):
     got, ref, mag = run_full(gpu_lib, shape, with_bias=False)
+    check(got, ref, mag, shape.name)
+
+
+# Shapes the window path takes (its geometry limits, and at most 6 weight
+# blocks per ring slot when the weights are streamed).
+WINDOW_ABLE = [sh for sh in SMALL if sh.stride == 1 and sh.C_in % 64 == 0 and
+               (oracle.output_size(sh.W, sh.KW, 1, sh.pad, sh.dilation) +
+                (sh.KW - 1) * sh.dilation) <= 128 and sh.KW <= 6]
+
+
+@pytest.mark.parametrize("shape", WINDOW_ABLE, ids=lambda s: s.name)
+@pytest.mark.parametrize("path", [1, 4], ids=["gather", "window"])
+def test_window_and_gather_paths_match_oracle(gpu_lib, shape, path):
+    """Both A producers on every shape the window path covers, explicitly."""
+    got, ref, mag = run_full(gpu_lib, shape, path=path, out_dtype=torch.float32)
     check(got, ref, mag, shape.name)
 
 
