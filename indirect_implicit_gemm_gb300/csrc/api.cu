@@ -84,6 +84,35 @@ bool window_geometry(const ConvShape& c)
     return c.s == 1 && c.C_in % 64 == 0 && wv <= 128 && (c.KW - 1) * c.d <= 8;
 }
 
+// Narrow-window stem geometry: small C_in, undilated, output rows that fit a
+// 128-row tile, input rows whose byte length keeps bulk copies 16-byte aligned.
+bool narrow_window_geometry(const ConvShape& c)
+{
+    return c.C_in % 8 != 0 && c.C_in < 16 && c.d == 1 && c.W_out <= 128 &&
+           ((long long)c.W * c.C_in * 2) % 16 == 0;
+}
+
+// Staged-row layout of the narrow window (bytes): the row's data starts at a0
+// (16-byte aligned, at least p*C_in*2 in so pixel -p has room), and each row
+// holds every element an A slice of the last output column can read.
+struct NarrowRows {
+    int kwc, kwcp, a0, rb, rows, slot;
+};
+NarrowRows narrow_rows(const ConvShape& c)
+{
+    NarrowRows r;
+    r.kwc = c.KW * c.C_in;
+    r.kwcp = (r.kwc + 7) / 8 * 8;
+    r.a0 = (c.p * c.C_in * 2 + 15) / 16 * 16;
+    const int lead = r.a0 - c.p * c.C_in * 2;  // byte of pixel -p
+    const int data_end = r.a0 + c.W * c.C_in * 2;
+    const int read_end = lead + ((c.W_out - 1) * c.s * c.C_in + r.kwcp) * 2 + 4;
+    r.rb = ((data_end > read_end ? data_end : read_end) + 15) / 16 * 16;
+    r.rows = 128 / c.W_out;  // output rows per tile
+    r.slot = (r.rows * c.KH * r.rb + 127) / 128 * 128;
+    return r;
+}
+
 struct GemmPlan;
 GemmPlan plan_gemm(int path, const ConvShape& c);
 bool window_applies(const ConvShape& c);
@@ -184,7 +213,8 @@ struct GemmPlan {
     int m_step = 128;
     int a_stage_bytes = 128 * 64 * 2;
     int b_per_stage = 1;
-    int win_wv = 0, win_rows = 0;  // window mode geometry
+    int win_wv = 0, win_rows = 0;  // row-tile geometry (window and narrow window)
+    int extra_smem = 0;            // narrow window: staged-row slots
     long long M = 0, K = 0;
     int num_kb = 0, m_tiles = 0, n_tiles = 0;
 };
@@ -251,6 +281,25 @@ GemmPlan plan_gemm(int path, const ConvShape& c)
     }
     // Gather path: TMA gather4 when a 64-column K block stays inside one tap's
     // channels, 16-byte cp.async otherwise.
+    if (path == CONVGB_PATH_STEM && narrow_window_geometry(c)) {
+        // Whole input rows staged per tile; weights resident (one column tile).
+        const NarrowRows nr = narrow_rows(c);
+        GemmPlan n;
+        n.amode = kANarrowWin;
+        n.M = c.M;
+        n.K = (long long)c.KH * nr.kwcp;
+        n.bn = pick_bn(c.C_out);
+        n.num_kb = (int)((n.K + 63) / 64);
+        n.win_wv = c.W_out;
+        n.win_rows = nr.rows;
+        n.m_step = nr.rows;
+        n.m_tiles = (int)(((long long)c.N * c.H_out + nr.rows - 1) / nr.rows);
+        n.n_tiles = (c.C_out + n.bn - 1) / n.bn;
+        n.bres = 1;
+        n.extra_smem = 2 * nr.slot;
+        n.stages = igemm_pick_stages(n.bn, 1, n.num_kb, n.a_stage_bytes, 1, n.extra_smem);
+        if (n.n_tiles == 1 && n.stages >= 2) return n;
+    }
     g.amode = path == CONVGB_PATH_DENSE  ? kADense
               : path == CONVGB_PATH_STEM ? kANarrow
               : c.C_in % 64 == 0         ? kATmaGather
@@ -292,17 +341,18 @@ WsLayout workspace_layout(int path, const ConvShape& c)
 {
     WsLayout L;
     size_t at = 0;
-    if (path == CONVGB_PATH_GATHER || path == CONVGB_PATH_STEM) {
+    const GemmPlan g = plan_gemm(path, c);
+    if (g.amode == kAGather || g.amode == kATmaGather || g.amode == kANarrow) {
         L.ibuf_off = at;
         L.ibuf_bytes = (size_t)c.H_out * c.W_out * c.KH * c.KW * sizeof(int32_t);
         at = align_up(at + L.ibuf_bytes, kAlign);
     }
     if (path == CONVGB_PATH_STEM) {
         L.wpad_off = at;
-        L.wpad_bytes = (size_t)c.C_out * stem_kpad(c) * 2;
+        L.wpad_bytes = (size_t)c.C_out * g.K * 2;
         at = align_up(at + L.wpad_bytes, kAlign);
     }
-    if (plan_gemm(path, c).splits > 1) {
+    if (g.splits > 1) {
         L.part_off = at;
         L.part_bytes = (size_t)c.M * c.C_out * sizeof(float);
         at = align_up(at + L.part_bytes, kAlign);
@@ -325,6 +375,7 @@ struct IgemmArgs {
     int img_rows = 0;    // H*W
     long long x_rows = 0;  // N*H*W
     const ConvShape* shape = nullptr;  // window mode geometry
+    int pack_taps = 0, pack_cin = 0, pack_cp = 0;  // stem weight packing
 };
 
 // Tensor maps and kernel parameters, all host-side: nothing is launched here,
@@ -379,6 +430,26 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     p.m_step = g.m_step;
     p.a_stage_bytes = g.a_stage_bytes;
     p.b_per_stage = g.b_per_stage;
+    if (g.amode == kANarrowWin) {
+        const ConvShape& c = *a.shape;
+        const NarrowRows nr = narrow_rows(c);
+        p.win_wv = g.win_wv;
+        p.win_rows = g.win_rows;
+        p.win_groups = c.N * c.H_out;
+        p.win_wout = c.W_out;
+        p.ho_div = FastDiv((uint32_t)c.H_out);
+        p.nw_H = c.H;
+        p.nw_W = c.W;
+        p.nw_KH = c.KH;
+        p.nw_s = c.s;
+        p.nw_p = c.p;
+        p.nw_cin = c.C_in;
+        p.nw_rb = nr.rb;
+        p.nw_a0 = nr.a0;
+        p.nw_kwc = nr.kwc;
+        p.nw_kwcp = nr.kwcp;
+        p.nw_slot_bytes = nr.slot;
+    }
     if (g.amode == kAWindow) {
         const ConvShape& c = *a.shape;
         p.win_wv = g.win_wv;
@@ -457,7 +528,7 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
         a.C_in = C_in;
         a.shape = &c;
     } else {
-        ibuf = reinterpret_cast<int32_t*>(wsb + L.ibuf_off);
+        ibuf = L.ibuf_bytes ? reinterpret_cast<int32_t*>(wsb + L.ibuf_off) : nullptr;
         a.x = static_cast<const uint16_t*>(x);
         a.ibuf = ibuf;
         a.C_in = C_in;
@@ -468,18 +539,31 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
         a.x_rows = (long long)N * H * W;
         a.shape = &c;
         if (path == CONVGB_PATH_STEM) {
-            // Weights re-packed with each tap's channels padded to cp.
-            a.cp = stem_cp(c);
-            a.k_valid = (long long)a.taps * a.cp;
+            // Weights re-packed: narrow window, each kh row's KW*C_in weights
+            // padded to a multiple of 8; scalar gather, each tap's channels
+            // padded to cp.
             wpad = reinterpret_cast<uint16_t*>(wsb + L.wpad_off);
             a.w = wpad;
+            if (plan.amode == kANarrowWin) {
+                const NarrowRows nr = narrow_rows(c);
+                a.pack_taps = KH;
+                a.pack_cin = nr.kwc;
+                a.pack_cp = nr.kwcp;
+            } else {
+                a.cp = stem_cp(c);
+                a.k_valid = (long long)a.taps * a.cp;
+                a.pack_taps = a.taps;
+                a.pack_cin = C_in;
+                a.pack_cp = a.cp;
+            }
         }
     }
     PreparedGemm pg;
     st = prepare_gemm(plan, a, &pg);
     if (st != CONVGB_OK) return st;
-    if (wpad && launch_pack_padded_weights(static_cast<const uint16_t*>(w), wpad, C_out, a.taps,
-                                           C_in, a.cp, (int)plan.K, cs) != cudaSuccess)
+    if (wpad && launch_pack_padded_weights(static_cast<const uint16_t*>(w), wpad, C_out,
+                                           a.pack_taps, a.pack_cin, a.pack_cp, (int)plan.K,
+                                           cs) != cudaSuccess)
         return CONVGB_ERR_CUDA;
     if (ibuf && launch_build_indirection(c, ibuf, cs) != cudaSuccess) return CONVGB_ERR_CUDA;
     return launch_gemm(pg, cs);

@@ -49,12 +49,16 @@ constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 512;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kSmemLimit = 232448;    // opt-in dynamic shared memory per block
-static_assert((3 * kMaxStages + 6) * 8 + 8 <= kHeaderBytes, "header area");
+constexpr int kMaxAcc = 4;
+static_assert((3 * kMaxStages + 2 * kMaxAcc + 6) * 8 + 8 <= kHeaderBytes, "header area");
 
 template <int BN>
 struct Cfg {
     static constexpr int kBBytes = BN * BK * 2;  // one K block of B
-    static constexpr int kTmemCols = 2 * BN;    // two accumulators
+    // Accumulators in TMEM (512 columns): up to four, so the MMAs can run up to
+    // three tiles ahead of the epilogue when tiles are short.
+    static constexpr int kAcc = (512 / BN) < kMaxAcc ? (512 / BN) : kMaxAcc;
+    static constexpr int kTmemCols = kAcc * BN;
     static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
     static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation must be a power of 2");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
@@ -228,8 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<BN>;
     // A written by the gather warps (signalled on full_a) or by the TMA warp
     // together with B (signalled on full_b).
-    constexpr bool GATHER = AMODE == kAGather || AMODE == kANarrow || AMODE == kATmaGather;
+    constexpr bool NARROWWIN = AMODE == kANarrowWin;
+    constexpr bool GATHER =
+        AMODE == kAGather || AMODE == kANarrow || AMODE == kATmaGather || NARROWWIN;
     constexpr bool WINDOW = AMODE == kAWindow;
+    constexpr bool ROWTILES = WINDOW || NARROWWIN;  // tiles of whole output rows
     const uint32_t S = static_cast<uint32_t>(p.stages);
     const uint32_t AST = static_cast<uint32_t>(p.a_stage_bytes);
     extern __shared__ uint8_t smem_raw[];
@@ -238,10 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full_b = bars + kMaxStages;     // B stage ready (tx bytes), count 1
     uint64_t* empty = bars + 2 * kMaxStages;  // MMA done with stage, count 1 (tcgen05.commit)
     uint64_t* tfull = bars + 3 * kMaxStages;  // accumulator ready, count 1 (tcgen05.commit)
-    uint64_t* tempty = tfull + 2;             // accumulator drained, count kEpiThreads
-    uint64_t* drain = tempty + 2;             // MMA unwinding, count 1
+    uint64_t* tempty = tfull + kMaxAcc;       // accumulator drained, count kEpiThreads
+    uint64_t* drain = tempty + kMaxAcc;       // MMA unwinding, count 1
     uint64_t* bres_full = drain + 1;          // resident weights loaded (tx bytes), count 1
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bres_full + 1);
+    uint64_t* stg_full = bres_full + 1;       // narrow window: tile's rows staged (tx bytes)
+    uint64_t* stg_empty = stg_full + 2;       // narrow window: staged rows consumed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_empty + 2);
     uint32_t* abort_flag = tmem_slot + 1;
     // The 128-byte swizzle is a function of shared-memory address bits, so the
     // stage buffers must start on 1024-byte boundaries of the shared window.
@@ -251,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_blocks =
         p.bres ? static_cast<uint32_t>(p.kb_total) : S * static_cast<uint32_t>(p.b_per_stage);
     uint8_t* sA = data + b_blocks * C::kBBytes;
+    uint8_t* sStg = sA + S * AST;  // narrow window: two slots of staged input rows
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -262,12 +272,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&full_b[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::kAcc; ++i) {
             ptx::mbar_init(&tfull[i], 1);
             ptx::mbar_init(&tempty[i], kEpiThreads);
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(bres_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&stg_full[i], 1);
+            ptx::mbar_init(&stg_empty[i], kGatherThreads);
+        }
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
@@ -278,6 +292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(tmem_slot, C::kTmemCols);
         ptx::tmem_relinquish();
+    }
+    if (NARROWWIN) {
+        // Staged rows keep their zero borders for the whole kernel: the bulk
+        // copies only ever write row interiors.
+        uint4* z = reinterpret_cast<uint4*>(sStg);
+        const int n16 = 2 * p.nw_slot_bytes / 16;
+        for (int i = threadIdx.x; i < n16; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+        ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -293,38 +315,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         // virtual pixel (wrow, wcol) of the tile's output rows; spill columns
         // (wcol >= W_out) and rows past the tile's output rows are discarded.
         const int r = warp * 32 + lane;
-        const int wrow = WINDOW ? r / p.win_wv : 0;
-        const int wcol = WINDOW ? r - wrow * p.win_wv : 0;
+        const int wrow = ROWTILES ? r / p.win_wv : 0;
+        const int wcol = ROWTILES ? r - wrow * p.win_wv : 0;
         uint32_t lt = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
             const Unit u = unit_of<BN>(p, tile);
-            const uint32_t acc = lt & 1u, use = lt >> 1;
+            const uint32_t acc = lt % C::kAcc, use = lt / C::kAcc;
             // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds.
             const bool ready = wait_bar(&tfull[acc], use & 1u, wc, kRoleEpilogue);
             if (!__all_sync(0xffffffffu, ready)) break;
             ptx::tc_fence_after();
             int m = u.m0 + r;
-            if (WINDOW) {
+            if (ROWTILES) {
                 const int g = u.m0 + wrow;  // output row n*H_out + ho
                 const bool real = wrow < p.win_rows && wcol < p.win_wout && g < p.win_groups;
                 m = real ? g * p.win_wout + wcol : p.M;
             }
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
+            const bool live = m < p.M;
+            // Two 32-column chunks per TMEM round trip; the accumulator is handed
+            // back to the MMA warp as soon as its last chunk is in registers.
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(taddr + ch * 32, r);
+            for (int ch = 0; ch < BN / 32; ch += 2) {
+                uint32_t ra[32], rb[32];
+                ptx::tmem_ld_32x32b_x32(taddr + ch * 32, ra);
+                if (ch + 1 < BN / 32) ptx::tmem_ld_32x32b_x32(taddr + (ch + 1) * 32, rb);
                 ptx::tmem_ld_wait();
+                if (ch + 2 >= BN / 32) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&tempty[acc]);
+                }
                 const int co0 = u.n0 + ch * 32;
-                if (m < p.M && co0 < p.C_out) {
+                if (live && co0 < p.C_out) {
                     if (p.splits > 1)
-                        reduce_chunk(p, m, co0, r);
+                        reduce_chunk(p, m, co0, ra);
                     else
-                        store_chunk(p, m, co0, r);
+                        store_chunk(p, m, co0, ra);
+                }
+                if (live && ch + 1 < BN / 32 && co0 + 32 < p.C_out) {
+                    if (p.splits > 1)
+                        reduce_chunk(p, m, co0 + 32, rb);
+                    else
+                        store_chunk(p, m, co0 + 32, rb);
                 }
             }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&tempty[acc]);
         }
     } else if (warp < kEpiWarps + kGatherWarps) {
         // ------------------------------------------------------------ A gather
@@ -386,6 +420,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (uint32_t i = first; i < it; ++i)
                     if (i % kGatherWarps == static_cast<uint32_t>(gw))
                         drain_wait(&full_a[i % S], (i / S) & 1u, 1000000000ull);
+            }
+        } else if (NARROWWIN) {
+            // Thread t builds A row t: output pixel (tile row j, column wo).  K is
+            // (kh, kw*C_in + c) with each kh slice padded to nw_kwcp, so the slice
+            // of kh is nw_kwc consecutive elements of the staged input row
+            // ho*s - p + kh, starting at pixel wo*s - p.
+            const int t = threadIdx.x - kEpiThreads;  // 0..127
+            const int j = t / p.win_wv, wo = t - j * p.win_wv;
+            const int px_off = wo * p.nw_s * p.nw_cin;  // element offset of the window in its row
+            const int lead = p.nw_a0 / 2 - p.nw_p * p.nw_cin;  // element of pixel -p in a row
+            Ring ring;
+            uint32_t slot = 0, slot_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const Unit u = unit_of<BN>(p, tile);
+                const int rows = min(p.win_rows, p.win_groups - u.m0);
+                const bool row_live = j < rows;
+                int ho = 0;
+                if (row_live) {
+                    uint32_t nn, hh;
+                    p.ho_div.divmod(static_cast<uint32_t>(u.m0 + j), nn, hh);
+                    ho = static_cast<int>(hh);
+                }
+                if (!wait_bar(&stg_full[slot], slot_phase, wc, kRoleGather)) {
+                    ok = false;
+                    break;
+                }
+                const uint16_t* stg = reinterpret_cast<const uint16_t*>(sStg + slot * p.nw_slot_bytes);
+                int kh = (u.kb0 * BK) / p.nw_kwcp;   // slice of the first chunk
+                int o = u.kb0 * BK - kh * p.nw_kwcp;  // offset of the chunk in its slice
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
+                    if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleGather)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* stage_a = sA + ring.stage * AST;
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t w4[4] = {0u, 0u, 0u, 0u};
+                        const int h = ho * p.nw_s - p.nw_p + kh;
+                        if (row_live && kh < p.nw_KH && h >= 0 && h < p.nw_H) {
+                            const int e = (j * p.nw_KH + kh) * (p.nw_rb / 2) + lead + px_off + o;
+                            const uint32_t* wp = reinterpret_cast<const uint32_t*>(stg) + (e >> 1);
+                            uint32_t v[5];
+#pragma unroll
+                            for (int q = 0; q < 5; ++q) v[q] = wp[q];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                w4[q] = (e & 1) ? __funnelshift_r(v[q], v[q + 1], 16) : v[q];
+                            // elements past the slice's KW*C_in belong to the next pixels
+                            const int valid = p.nw_kwc - o;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                if (2 * q >= valid) w4[q] = 0u;
+                                else if (2 * q + 1 >= valid) w4[q] &= 0xFFFFu;
+                            }
+                        }
+                        const int cr = c ^ (t & 7);
+                        *reinterpret_cast<uint4*>(stage_a + t * 128 + cr * 16) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        o += 8;
+                        if (o >= p.nw_kwcp) {
+                            o -= p.nw_kwcp;
+                            ++kh;
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(&full_a[ring.stage]);
+                }
+                ptx::mbar_arrive(&stg_empty[slot]);
+                if (++slot == 2) {
+                    slot = 0;
+                    slot_phase ^= 1u;
+                }
             }
         } else if (GATHER) {
             // Thread gt owns 16-byte chunk c (8 consecutive K columns) of rows
@@ -499,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = !p.bres || wait_bar(bres_full, 0u, wc, kRoleMma);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++lt) {
                 const Unit u = unit_of<BN>(p, tile);
-                const uint32_t acc = lt & 1u, use = lt >> 1;
+                const uint32_t acc = lt % C::kAcc, use = lt / C::kAcc;
                 if (!wait_bar(&tempty[acc], (use & 1u) ^ 1u, wc, kRoleMma)) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -515,7 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // Thread-written A stages (cp.async, st.shared) are read by the
                     // tensor core through the async proxy.
-                    if (AMODE == kAGather || AMODE == kANarrow) ptx::fence_proxy_async_smem();
+                    if (AMODE == kAGather || AMODE == kANarrow || NARROWWIN)
+                        ptx::fence_proxy_async_smem();
                     ptx::tc_fence_after();
                     const uint32_t a_base = ptx::smem_addr(sA + ring.stage * AST);
                     if (WINDOW) {
@@ -566,9 +675,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            static_cast<uint32_t>(p.kb_total) * C::kBBytes);
                 for (int kb = 0; kb < p.kb_total; ++kb)
                     ptx::tma_load_2d(sB + kb * C::kBBytes, &tmap_b, bres_full, kb * BK, 0);
-                drain_wait(bres_full, 0u, 1000000000ull);
+                // (the A loads below are issued at once; the weights' arrival is
+                // awaited by the MMA thread, and here only before exiting)
             }
-            if (WINDOW) {
+            if (NARROWWIN) {
+                // Per tile: every input row its output rows read (KH per output row),
+                // copied whole into the tile's staging slot; rows outside the image
+                // are skipped (the consumer writes zeros for them).
+                const uint32_t row_bytes = static_cast<uint32_t>(p.nw_W * p.nw_cin * 2);
+                uint32_t slot = 0, slot_phase = 0, issued = 0;
+                for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++issued) {
+                    const Unit u = unit_of<BN>(p, tile);
+                    if (!wait_bar(&stg_empty[slot], slot_phase ^ 1u, wc, kRoleTma)) break;
+                    const int rows = min(p.win_rows, p.win_groups - u.m0);
+                    uint32_t copies = 0;
+                    for (int jj = 0; jj < rows; ++jj) {
+                        uint32_t n, ho;
+                        p.ho_div.divmod(static_cast<uint32_t>(u.m0 + jj), n, ho);
+                        for (int kh = 0; kh < p.nw_KH; ++kh) {
+                            const int h = static_cast<int>(ho) * p.nw_s - p.nw_p + kh;
+                            copies += (h >= 0 && h < p.nw_H) ? 1u : 0u;
+                        }
+                    }
+                    ptx::mbar_arrive_expect_tx(&stg_full[slot], copies * row_bytes);
+                    uint8_t* slot_base = sStg + slot * p.nw_slot_bytes;
+                    for (int jj = 0; jj < rows; ++jj) {
+                        uint32_t n, ho;
+                        p.ho_div.divmod(static_cast<uint32_t>(u.m0 + jj), n, ho);
+                        for (int kh = 0; kh < p.nw_KH; ++kh) {
+                            const int h = static_cast<int>(ho) * p.nw_s - p.nw_p + kh;
+                            if (h < 0 || h >= p.nw_H) continue;
+                            const uint16_t* src =
+                                p.x + (static_cast<long long>(n) * p.nw_H + h) * p.nw_W * p.nw_cin;
+                            ptx::bulk_copy_g2s(slot_base + (jj * p.nw_KH + kh) * p.nw_rb + p.nw_a0,
+                                               src, row_bytes, &stg_full[slot]);
+                        }
+                    }
+                    if (++slot == 2) {
+                        slot = 0;
+                        slot_phase ^= 1u;
+                    }
+                }
+                // Wait (bounded) for the last copies so none lands after the CTA exits.
+                for (uint32_t i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+                    drain_wait(&stg_full[i % 2], (i / 2) & 1u, 1000000000ull);
+            } else if (WINDOW) {
                 // Per (tile, kh, cc): one box of win_wv pixels x 64 channels for each
                 // of the tile's output rows (input row ho - p + kh*d, columns -p ..
                 // -p + win_wv - 1; TMA zero-fills what lies outside the image), plus
@@ -640,6 +791,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // The resident weights must have landed before the CTA exits.
+    if (warp == kTmaWarp && lane == 0 && p.bres) drain_wait(bres_full, 0u, 1000000000ull);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -702,7 +855,8 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const IgemmP
         configured_for = dev;
     }
     const int smem = igemm_smem_bytes(BN, p.stages, p.bres, p.kb_total, p.a_stage_bytes,
-                                      p.b_per_stage);
+                                      p.b_per_stage,
+                                      AMODE == kANarrowWin ? 2 * p.nw_slot_bytes : 0);
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
     const int tiles = p.m_tiles * p.n_tiles * p.splits;
     const int grid = tiles < num_sms() ? tiles : num_sms();
@@ -726,16 +880,18 @@ cudaError_t launch_mode(int bn, const CUtensorMap& ta, const CUtensorMap& tb, co
 }  // namespace
 
 int igemm_smem_bytes(int bn, int stages, int bres, int num_kb, int a_stage_bytes,
-                     int b_per_stage)
+                     int b_per_stage, int extra_bytes)
 {
     const int b_blocks = bres ? num_kb : stages * b_per_stage;
-    return kHeaderBytes + 1024 + b_blocks * bn * BK * 2 + stages * a_stage_bytes;
+    return kHeaderBytes + 1024 + b_blocks * bn * BK * 2 + stages * a_stage_bytes + extra_bytes;
 }
 
-int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per_stage)
+int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per_stage,
+                      int extra_bytes)
 {
     for (int s = kMaxStages; s >= 2; --s)
-        if (igemm_smem_bytes(bn, s, bres, num_kb, a_stage_bytes, b_per_stage) <= kSmemLimit)
+        if (igemm_smem_bytes(bn, s, bres, num_kb, a_stage_bytes, b_per_stage, extra_bytes) <=
+            kSmemLimit)
             return s;
     return 0;
 }
@@ -751,6 +907,7 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kANarrow: return launch_mode<kANarrow>(bn, ta, tb, p, st);
     case kATmaGather: return launch_mode<kATmaGather>(bn, ta, tb, p, st);
     case kAWindow: return launch_mode<kAWindow>(bn, ta, tb, p, st);
+    case kANarrowWin: return launch_mode<kANarrowWin>(bn, ta, tb, p, st);
     default: return cudaErrorInvalidValue;
     }
 }

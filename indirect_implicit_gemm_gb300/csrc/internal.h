@@ -65,6 +65,12 @@ struct IgemmParams {
     // pixels (W_out real + (KW-1)*d spill); K block kb = (kh, cc)
     int win_wv, win_rows, win_groups, win_wout, win_kw, win_d, win_pad, win_cc;
     FastDiv ho_div;          // divides an output-row index (n*H_out + ho) by H_out
+    // narrow-window mode: staged input rows
+    int nw_H, nw_W, nw_KH, nw_s, nw_p, nw_cin;
+    int nw_rb;               // bytes per staged row (16-byte multiple)
+    int nw_a0;               // byte offset of the row's data inside its staged row
+    int nw_kwc, nw_kwcp;     // KW*C_in, and that padded to a multiple of 8
+    int nw_slot_bytes;       // bytes of one tile's staged rows (two slots)
     int bres;                // 1: all of W's single column tile resident in shared memory
     float* partial;          // splits > 1: fp32 [M][C_out] sums, zeroed before the launch
     int y_f32;               // 1: fp32 output, 0: bf16
@@ -87,12 +93,16 @@ enum AMode : int {
                       // (C_in % 64 == 0)
     kAWindow = 4,     // stride 1: whole output rows per tile; each input row is staged once
                       // per (kh, 64-channel block) and read by all KW taps at shifted starts
+    kANarrowWin = 5,  // small C_in: whole input rows bulk-copied to shared memory per tile,
+                      // A built from them; K ordered (kh, kw*C_in) with each kh slice
+                      // padded to a multiple of 8
 };
 // Dynamic shared memory of one implicit-GEMM CTA, and the deepest ring that fits
 // (0 when none does).
 int igemm_smem_bytes(int bn, int stages, int bres, int num_kb, int a_stage_bytes,
-                     int b_per_stage);
-int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per_stage);
+                     int b_per_stage, int extra_bytes = 0);
+int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per_stage,
+                      int extra_bytes = 0);
 // Rows of an A ring slot in window mode (128 plus the tap spill, rounded to 8).
 int window_stage_rows(int kw, int d);
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& tmap_a,

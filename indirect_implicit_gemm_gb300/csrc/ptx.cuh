@@ -120,6 +120,18 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Contiguous global->shared bulk copy, completion counted in bytes on `bar`.
+// Both addresses and the size must be multiples of 16 bytes.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global->shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes)
