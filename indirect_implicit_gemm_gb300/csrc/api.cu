@@ -109,12 +109,12 @@ NarrowRows narrow_rows(const ConvShape& c)
     const int read_end = lead + ((c.W_out - 1) * c.s * c.C_in + r.kwcp) * 2 + 4;
     r.rb = ((data_end > read_end ? data_end : read_end) + 15) / 16 * 16;
     r.rows = 128 / c.W_out;  // output rows per tile
-    r.slot = (r.rows * c.KH * r.rb + 127) / 128 * 128;
+    r.slot = (r.rows * c.KH * r.rb + 511) / 512 * 512;  // two slots keep 1024-byte alignment
     return r;
 }
 
 struct GemmPlan;
-GemmPlan plan_gemm(int path, const ConvShape& c);
+GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32 = 0);
 bool window_applies(const ConvShape& c);
 
 // Whether `path` can compute this shape.
@@ -215,6 +215,7 @@ struct GemmPlan {
     int b_per_stage = 1;
     int win_wv = 0, win_rows = 0;  // row-tile geometry (window and narrow window)
     int extra_smem = 0;            // narrow window: staged-row slots
+    int tma_store = 0;             // epilogue through shared memory and TMA stores
     long long M = 0, K = 0;
     int num_kb = 0, m_tiles = 0, n_tiles = 0;
 };
@@ -244,7 +245,30 @@ int choose_splits(long long tiles, int num_kb, long long partial_bytes, long lon
     return best_cost <= 0.75 * cost(1) ? best : 1;
 }
 
-GemmPlan plan_gemm(int path, const ConvShape& c)
+// Turns on the TMA-store epilogue when the output allows it (bf16, rows 16-byte
+// aligned, no split) and the ring still has two stages with its staging tile.
+void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
+{
+    if (y_f32 || c.C_out % 8 != 0 || g.splits != 1 || g.bn < 64 || g.stages < 2) return;
+    const int kb_res = g.bres ? (int)((g.K + 63) / 64) : g.num_kb;
+    const int s = igemm_pick_stages(g.bn, g.bres, kb_res, g.a_stage_bytes, g.b_per_stage,
+                                    g.extra_smem + kEpiStageBytes);
+    if (s < 2) return;
+    g.stages = s;
+    g.tma_store = 1;
+}
+
+GemmPlan plan_gemm_ring(int path, const ConvShape& c);
+
+GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32)
+{
+    GemmPlan g = plan_gemm_ring(path, c);
+    plan_epilogue(g, c, y_f32);
+    return g;
+}
+
+// Operand producers, tiles, splits and the shared-memory ring.
+GemmPlan plan_gemm_ring(int path, const ConvShape& c)
 {
     GemmPlan g;
     if (path == CONVGB_PATH_WINDOW && window_geometry(c)) {
@@ -381,7 +405,7 @@ struct IgemmArgs {
 // Tensor maps and kernel parameters, all host-side: nothing is launched here,
 // so every failure is reported before the first launch of a call.
 struct PreparedGemm {
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ty;
     IgemmParams p;
     GemmPlan plan;
 };
@@ -400,6 +424,12 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     if (g.amode == kAWindow) {
         const ConvShape& c = *a.shape;
         if (!encode_window(&out->ta, a.x, c.N, c.H, c.W, c.C_in, g.win_wv)) return CONVGB_ERR_CUDA;
+    }
+    // TMA-store epilogue: y as [M][C_out], boxes of 64 channels x (one output row
+    // for row tiles, 128 rows otherwise).
+    if (g.tma_store) {
+        const int box_rows = (g.amode == kAWindow || g.amode == kANarrowWin) ? a.shape->W_out : 128;
+        if (!encode_kmajor(&out->ty, a.y, g.M, a.C_out, box_rows)) return CONVGB_ERR_CUDA;
     }
     unsigned* err = device_error_word();
     if (!err) return CONVGB_ERR_CUDA;
@@ -425,6 +455,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     p.m_tiles = g.m_tiles;
     p.n_tiles = g.n_tiles;
     p.splits = g.splits;
+    p.tma_store = g.tma_store;
     p.stages = g.stages;
     p.bres = g.bres;
     p.m_step = g.m_step;
@@ -479,7 +510,7 @@ convgb_status launch_gemm(const PreparedGemm& pg, cudaStream_t st)
     if (p.splits > 1 &&
         cudaMemsetAsync(p.partial, 0, (size_t)p.M * p.C_out * sizeof(float), st) != cudaSuccess)
         return CONVGB_ERR_CUDA;
-    if (launch_igemm(pg.plan.amode, pg.plan.bn, pg.ta, pg.tb, p, st) != cudaSuccess)
+    if (launch_igemm(pg.plan.amode, pg.plan.bn, pg.ta, pg.tb, pg.ty, p, st) != cudaSuccess)
         return CONVGB_ERR_CUDA;
     if (p.splits > 1 &&
         launch_finish_split(p.partial, p.bias, p.y, p.M, p.C_out, p.y_f32, st) != cudaSuccess)
@@ -509,7 +540,7 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
         return CONVGB_ERR_ALIGNMENT;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
-    const GemmPlan plan = plan_gemm(path, c);
+    const GemmPlan plan = plan_gemm(path, c, y_dtype == CONVGB_F32 ? 1 : 0);
 
     IgemmArgs a;
     a.w = w;
@@ -701,8 +732,9 @@ convgb_status conv2d_fwd_indirect(const void* x, const void* w, const void* bias
         !aligned16(ibuf))
         return CONVGB_ERR_ALIGNMENT;
     // Reusing a caller's buffer leaves no room for split-K partial sums.
-    GemmPlan plan = plan_gemm(CONVGB_PATH_GATHER, c);
+    GemmPlan plan = plan_gemm_ring(CONVGB_PATH_GATHER, c);
     plan.splits = 1;
+    plan_epilogue(plan, c, y_dtype == CONVGB_F32 ? 1 : 0);
     IgemmArgs a;
     a.x = static_cast<const uint16_t*>(x);
     a.ibuf = ibuf;

@@ -50,7 +50,7 @@ constexpr int kHeaderBytes = 512;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kSmemLimit = 232448;    // opt-in dynamic shared memory per block
 constexpr int kMaxAcc = 4;
-static_assert((3 * kMaxStages + 2 * kMaxAcc + 6) * 8 + 8 <= kHeaderBytes, "header area");
+static_assert((3 * kMaxStages + 2 * kMaxAcc + 6) * 8 + 8 + 16 <= kHeaderBytes, "header area");
 
 template <int BN>
 struct Cfg {
@@ -227,7 +227,8 @@ __device__ __forceinline__ void reduce_chunk(const IgemmParams& p, int m, int co
 template <int BN, int AMODE>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                 const __grid_constant__ CUtensorMap tmap_b, const IgemmParams p)
+                 const __grid_constant__ CUtensorMap tmap_b,
+                 const __grid_constant__ CUtensorMap tmap_y, const IgemmParams p)
 {
     using C = Cfg<BN>;
     // A written by the gather warps (signalled on full_a) or by the TMA warp
@@ -261,6 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.bres ? static_cast<uint32_t>(p.kb_total) : S * static_cast<uint32_t>(p.b_per_stage);
     uint8_t* sA = data + b_blocks * C::kBBytes;
     uint8_t* sStg = sA + S * AST;  // narrow window: two slots of staged input rows
+    // TMA-store epilogue: a 128 x 64 bf16 staging tile (128-byte swizzle) and the
+    // current column tile's bias in fp32.
+    uint8_t* sEpi = sStg + (NARROWWIN ? 2 * p.nw_slot_bytes : 0);
+    float* sBias = reinterpret_cast<float*>(sEpi + 16384);
+    uint32_t* sVote = reinterpret_cast<uint32_t*>(abort_flag + 1);  // 4 epilogue-warp votes
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -318,12 +324,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wrow = ROWTILES ? r / p.win_wv : 0;
         const int wcol = ROWTILES ? r - wrow * p.win_wv : 0;
         uint32_t lt = 0;
+        int bias_n0 = -1;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
             const Unit u = unit_of<BN>(p, tile);
             const uint32_t acc = lt % C::kAcc, use = lt / C::kAcc;
-            // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds.
-            const bool ready = wait_bar(&tfull[acc], use & 1u, wc, kRoleEpilogue);
-            if (!__all_sync(0xffffffffu, ready)) break;
+            // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds,
+            // and with the TMA store all four warps do (they share named barriers).
+            bool ready = __all_sync(0xffffffffu, wait_bar(&tfull[acc], use & 1u, wc, kRoleEpilogue));
+            if (p.tma_store) {
+                if (lane == 0) sVote[warp] = ready ? 1u : 0u;
+                ptx::named_barrier_sync(1, kEpiThreads);
+                ready = sVote[0] && sVote[1] && sVote[2] && sVote[3];
+                ptx::named_barrier_sync(1, kEpiThreads);
+            }
+            if (!ready) break;
             ptx::tc_fence_after();
             int m = u.m0 + r;
             if (ROWTILES) {
@@ -333,8 +347,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
             const bool live = m < p.M;
-            // Two 32-column chunks per TMEM round trip; the accumulator is handed
-            // back to the MMA warp as soon as its last chunk is in registers.
+            if (p.tma_store) {
+                if (u.n0 != bias_n0) {  // new column tile: stage its bias
+                    ptx::named_barrier_sync(1, kEpiThreads);
+                    for (int i = r; i < BN; i += kEpiThreads)
+                        sBias[i] = (p.bias != nullptr && u.n0 + i < p.C_out)
+                                       ? bf16_bits_to_float(p.bias[u.n0 + i])
+                                       : 0.f;
+                    ptx::named_barrier_sync(1, kEpiThreads);
+                    bias_n0 = u.n0;
+                }
+#pragma unroll 1
+                for (int c64 = 0; c64 < BN / 64; ++c64) {
+                    uint32_t ra[32], rb[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
+                    ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
+                    ptx::tmem_ld_wait();
+                    if (c64 + 1 == BN / 64) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(&tempty[acc]);
+                    }
+                    // The staging tile is free once the previous store has read it.
+                    if (r == 0) ptx::bulk_wait_read_all();
+                    ptx::named_barrier_sync(1, kEpiThreads);
+                    const float* bs = sBias + c64 * 64;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint32_t* src = q < 4 ? ra + 8 * q : rb + 8 * (q - 4);
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(src[0]) + bs[8 * q + 0],
+                                          __uint_as_float(src[1]) + bs[8 * q + 1]);
+                        v.y = pack_bf16x2(__uint_as_float(src[2]) + bs[8 * q + 2],
+                                          __uint_as_float(src[3]) + bs[8 * q + 3]);
+                        v.z = pack_bf16x2(__uint_as_float(src[4]) + bs[8 * q + 4],
+                                          __uint_as_float(src[5]) + bs[8 * q + 5]);
+                        v.w = pack_bf16x2(__uint_as_float(src[6]) + bs[8 * q + 6],
+                                          __uint_as_float(src[7]) + bs[8 * q + 7]);
+                        *reinterpret_cast<uint4*>(sEpi + r * 128 + ((q ^ (r & 7)) << 4)) = v;
+                    }
+                    ptx::fence_proxy_async_smem();
+                    ptx::named_barrier_sync(1, kEpiThreads);
+                    if (r == 0) {
+                        const int c0 = u.n0 + c64 * 64;
+                        if (ROWTILES) {
+                            const int rows = min(p.win_rows, p.win_groups - u.m0);
+                            for (int jj = 0; jj < rows; ++jj)
+                                ptx::tma_store_2d(&tmap_y, sEpi + jj * p.win_wv * 128, c0,
+                                                  (u.m0 + jj) * p.win_wout);
+                        } else {
+                            ptx::tma_store_2d(&tmap_y, sEpi, c0, u.m0);
+                        }
+                        ptx::bulk_commit_group();
+                    }
+                }
+                continue;
+            }
+            // Direct stores: two 32-column chunks per TMEM round trip; the
+            // accumulator is handed back to the MMA warp as soon as its last
+            // chunk is in registers.
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ch += 2) {
                 uint32_t ra[32], rb[32];
@@ -360,6 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        // Every TMA store has finished before the CTA exits.
+        if (p.tma_store && r == 0) ptx::bulk_wait_all();
     } else if (warp < kEpiWarps + kGatherWarps) {
         // ------------------------------------------------------------ A gather
         if (AMODE == kATmaGather) {
@@ -841,8 +913,8 @@ __global__ void __launch_bounds__(256) finish_split_kernel(const float* __restri
 }
 
 template <int BN, int AMODE>
-cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const IgemmParams& p,
-                      cudaStream_t st)
+cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
+                      const IgemmParams& p, cudaStream_t st)
 {
     auto kern = igemm_kernel<BN, AMODE>;
     static int configured_for = -1;  // device for which the smem attribute was set
@@ -856,23 +928,24 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const IgemmP
     }
     const int smem = igemm_smem_bytes(BN, p.stages, p.bres, p.kb_total, p.a_stage_bytes,
                                       p.b_per_stage,
-                                      AMODE == kANarrowWin ? 2 * p.nw_slot_bytes : 0);
+                                      (AMODE == kANarrowWin ? 2 * p.nw_slot_bytes : 0) +
+                                          (p.tma_store ? kEpiStageBytes : 0));
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
     const int tiles = p.m_tiles * p.n_tiles * p.splits;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    kern<<<grid, kThreads, smem, st>>>(ta, tb, p);
+    kern<<<grid, kThreads, smem, st>>>(ta, tb, ty, p);
     return cudaGetLastError();
 }
 
 template <int AMODE>
-cudaError_t launch_mode(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const IgemmParams& p,
-                        cudaStream_t st)
+cudaError_t launch_mode(int bn, const CUtensorMap& ta, const CUtensorMap& tb,
+                        const CUtensorMap& ty, const IgemmParams& p, cudaStream_t st)
 {
     switch (bn) {
-    case 32: return launch_bn<32, AMODE>(ta, tb, p, st);
-    case 64: return launch_bn<64, AMODE>(ta, tb, p, st);
-    case 128: return launch_bn<128, AMODE>(ta, tb, p, st);
-    case 256: return launch_bn<256, AMODE>(ta, tb, p, st);
+    case 32: return launch_bn<32, AMODE>(ta, tb, ty, p, st);
+    case 64: return launch_bn<64, AMODE>(ta, tb, ty, p, st);
+    case 128: return launch_bn<128, AMODE>(ta, tb, ty, p, st);
+    case 256: return launch_bn<256, AMODE>(ta, tb, ty, p, st);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -899,15 +972,15 @@ int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per
 int window_stage_rows(int kw, int d) { return (BM + (kw - 1) * d + 7) / 8 * 8; }
 
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtensorMap& tb,
-                         const IgemmParams& p, cudaStream_t st)
+                         const CUtensorMap& ty, const IgemmParams& p, cudaStream_t st)
 {
     switch (amode) {
-    case kADense: return launch_mode<kADense>(bn, ta, tb, p, st);
-    case kAGather: return launch_mode<kAGather>(bn, ta, tb, p, st);
-    case kANarrow: return launch_mode<kANarrow>(bn, ta, tb, p, st);
-    case kATmaGather: return launch_mode<kATmaGather>(bn, ta, tb, p, st);
-    case kAWindow: return launch_mode<kAWindow>(bn, ta, tb, p, st);
-    case kANarrowWin: return launch_mode<kANarrowWin>(bn, ta, tb, p, st);
+    case kADense: return launch_mode<kADense>(bn, ta, tb, ty, p, st);
+    case kAGather: return launch_mode<kAGather>(bn, ta, tb, ty, p, st);
+    case kANarrow: return launch_mode<kANarrow>(bn, ta, tb, ty, p, st);
+    case kATmaGather: return launch_mode<kATmaGather>(bn, ta, tb, ty, p, st);
+    case kAWindow: return launch_mode<kAWindow>(bn, ta, tb, ty, p, st);
+    case kANarrowWin: return launch_mode<kANarrowWin>(bn, ta, tb, ty, p, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -71,6 +71,8 @@ struct IgemmParams {
     int nw_a0;               // byte offset of the row's data inside its staged row
     int nw_kwc, nw_kwcp;     // KW*C_in, and that padded to a multiple of 8
     int nw_slot_bytes;       // bytes of one tile's staged rows (two slots)
+    int tma_store;           // 1: epilogue stages 64-column chunks in shared memory and
+                             //    stores them with TMA (bf16 y, C_out % 8 == 0, no split)
     int bres;                // 1: all of W's single column tile resident in shared memory
     float* partial;          // splits > 1: fp32 [M][C_out] sums, zeroed before the launch
     int y_f32;               // 1: fp32 output, 0: bf16
@@ -106,7 +108,10 @@ int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per
 // Rows of an A ring slot in window mode (128 plus the tap spill, rounded to 8).
 int window_stage_rows(int kw, int d);
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& tmap_a,
-                         const CUtensorMap& tmap_b, const IgemmParams& p, cudaStream_t st);
+                         const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
+                         const IgemmParams& p, cudaStream_t st);
+// Shared memory the TMA-store epilogue adds (staging tile + bias).
+constexpr int kEpiStageBytes = 16384 + 1024;
 cudaError_t launch_finish_split(const float* partial, const uint16_t* bias, void* y, long long M,
                                 int C_out, int y_f32, cudaStream_t st);
 cudaError_t launch_selftest_timeout(unsigned long long timeout_ns, unsigned* err,
