@@ -215,6 +215,7 @@ struct GemmPlan {
     int b_per_stage = 1;
     int win_wv = 0, win_rows = 0;  // row-tile geometry (window and narrow window)
     int extra_smem = 0;            // narrow window: staged-row slots
+    int nw_slots = 0;
     int tma_store = 0;             // epilogue through shared memory and TMA stores
     long long M = 0, K = 0;
     int num_kb = 0, m_tiles = 0, n_tiles = 0;
@@ -320,7 +321,15 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         n.m_tiles = (int)(((long long)c.N * c.H_out + nr.rows - 1) / nr.rows);
         n.n_tiles = (c.C_out + n.bn - 1) / n.bn;
         n.bres = 1;
-        n.extra_smem = 2 * nr.slot;
+        // Four staged-row slots when they still leave a 4-deep A ring beside the
+        // epilogue's staging tile, else two.
+        for (int slots = 4; slots >= 2; slots -= 2) {
+            n.nw_slots = slots;
+            n.extra_smem = slots * nr.slot;
+            if (igemm_pick_stages(n.bn, 1, n.num_kb, n.a_stage_bytes, 1,
+                                  n.extra_smem + kEpiStageBytes) >= 4)
+                break;
+        }
         n.stages = igemm_pick_stages(n.bn, 1, n.num_kb, n.a_stage_bytes, 1, n.extra_smem);
         if (n.n_tiles == 1 && n.stages >= 2) return n;
     }
@@ -337,9 +346,9 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
     const long long im2col = c.M * c.K * 2;
     const long long partial = c.M * c.C_out * 4;
     g.splits = choose_splits((long long)g.m_tiles * g.n_tiles, g.num_kb, partial, im2col / 2);
-    // Gathered layers whose whole weight matrix is one column tile: keep it in
-    // shared memory for the CTA's lifetime when that still leaves a 4-deep A ring.
-    if (g.amode != kADense && g.n_tiles == 1 && g.splits == 1 &&
+    // Layers whose whole weight matrix is one column tile: keep it in shared
+    // memory for the CTA's lifetime when that still leaves a 4-deep A ring.
+    if (g.n_tiles == 1 && g.splits == 1 &&
         igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
         g.bres = 1;
     g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb, g.a_stage_bytes, 1);
@@ -480,6 +489,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.nw_kwc = nr.kwc;
         p.nw_kwcp = nr.kwcp;
         p.nw_slot_bytes = nr.slot;
+        p.nw_slots = g.nw_slots;
     }
     if (g.amode == kAWindow) {
         const ConvShape& c = *a.shape;
@@ -492,6 +502,9 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.win_pad = c.p;
         p.win_cc = c.C_in / 64;
         p.ho_div = FastDiv((uint32_t)c.H_out);
+        p.x_H = c.H;
+        p.x_W = c.W;
+        p.x_KH = c.KH;
     }
     if (g.stages < 2) return CONVGB_ERR_UNSUPPORTED;
     p.partial = a.partial;

@@ -50,7 +50,9 @@ constexpr int kHeaderBytes = 512;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kSmemLimit = 232448;    // opt-in dynamic shared memory per block
 constexpr int kMaxAcc = 4;
-static_assert((3 * kMaxStages + 2 * kMaxAcc + 6) * 8 + 8 + 16 <= kHeaderBytes, "header area");
+constexpr int kMaxSlots = 4;  // narrow window: staged-row slots
+static_assert((3 * kMaxStages + 2 * kMaxAcc + 2 + 2 * kMaxSlots) * 8 + 8 + 20 <= kHeaderBytes,
+              "header area");
 
 template <int BN>
 struct Cfg {
@@ -250,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* drain = tempty + kMaxAcc;       // MMA unwinding, count 1
     uint64_t* bres_full = drain + 1;          // resident weights loaded (tx bytes), count 1
     uint64_t* stg_full = bres_full + 1;       // narrow window: tile's rows staged (tx bytes)
-    uint64_t* stg_empty = stg_full + 2;       // narrow window: staged rows consumed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_empty + 2);
+    uint64_t* stg_empty = stg_full + kMaxSlots;  // narrow window: staged rows consumed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_empty + kMaxSlots);
     uint32_t* abort_flag = tmem_slot + 1;
     // The 128-byte swizzle is a function of shared-memory address bits, so the
     // stage buffers must start on 1024-byte boundaries of the shared window.
@@ -261,12 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_blocks =
         p.bres ? static_cast<uint32_t>(p.kb_total) : S * static_cast<uint32_t>(p.b_per_stage);
     uint8_t* sA = data + b_blocks * C::kBBytes;
-    uint8_t* sStg = sA + S * AST;  // narrow window: two slots of staged input rows
+    uint8_t* sStg = sA + S * AST;  // narrow window: nw_slots slots of staged input rows
+    const uint32_t NS = NARROWWIN ? static_cast<uint32_t>(p.nw_slots) : 1u;
     // TMA-store epilogue: a 128 x 64 bf16 staging tile (128-byte swizzle) and the
     // current column tile's bias in fp32.
-    uint8_t* sEpi = sStg + (NARROWWIN ? 2 * p.nw_slot_bytes : 0);
+    uint8_t* sEpi = sStg + (NARROWWIN ? NS * p.nw_slot_bytes : 0);
     float* sBias = reinterpret_cast<float*>(sEpi + 16384);
     uint32_t* sVote = reinterpret_cast<uint32_t*>(abort_flag + 1);  // 4 epilogue-warp votes
+    volatile uint32_t* sTilesDone = sVote + 4;  // tiles the epilogue has finished (window prefetch)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -284,10 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(bres_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kMaxSlots; ++i) {
             ptx::mbar_init(&stg_full[i], 1);
             ptx::mbar_init(&stg_empty[i], kGatherThreads);
         }
+        *sTilesDone = 0u;
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
@@ -303,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Staged rows keep their zero borders for the whole kernel: the bulk
         // copies only ever write row interiors.
         uint4* z = reinterpret_cast<uint4*>(sStg);
-        const int n16 = 2 * p.nw_slot_bytes / 16;
+        const int n16 = static_cast<int>(NS) * p.nw_slot_bytes / 16;
         for (int i = threadIdx.x; i < n16; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
         ptx::fence_proxy_async_smem();
     }
@@ -400,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::bulk_commit_group();
                     }
                 }
+                if (r == 0) *sTilesDone = lt + 1;
                 continue;
             }
             // Direct stores: two 32-column chunks per TMEM round trip; the
@@ -429,12 +435,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                         store_chunk(p, m, co0 + 32, rb);
                 }
             }
+            if (r == 0) *sTilesDone = lt + 1;
         }
         // Every TMA store has finished before the CTA exits.
         if (p.tma_store && r == 0) ptx::bulk_wait_all();
     } else if (warp < kEpiWarps + kGatherWarps) {
         // ------------------------------------------------------------ A gather
-        if (AMODE == kATmaGather) {
+        if (WINDOW && warp == kEpiWarps) {
+            // The gather warps have nothing to gather in window mode; the first
+            // of them pulls the input rows of the next tiles into L2 with plain
+            // prefetches (the TMA engine stays free for the loads themselves),
+            // about three tiles ahead of the epilogue.
+            const long long row_elems = static_cast<long long>(p.x_W) * p.C_in;
+            const int lines = static_cast<int>((row_elems * 2 + 127) / 128);
+            auto prefetch_tile = [&](int t) {
+                const Unit v = unit_of<BN>(p, t);
+                const int rows = min(p.win_rows, p.win_groups - v.m0);
+                for (int jj = 0; jj < rows; ++jj) {
+                    uint32_t n, ho;
+                    p.ho_div.divmod(static_cast<uint32_t>(v.m0 + jj), n, ho);
+                    for (int kh = 0; kh < p.x_KH; ++kh) {
+                        // (undilated) rows the previous output row of this tile reached
+                        if (jj > 0 && kh < p.x_KH - 1 && p.win_d == 1) continue;
+                        const int h = static_cast<int>(ho) - p.win_pad + kh * p.win_d;
+                        if (h < 0 || h >= p.x_H) continue;
+                        const uint16_t* row =
+                            p.x + (static_cast<long long>(n) * p.x_H + h) * row_elems;
+                        for (int l = lane; l < lines; l += 32)
+                            ptx::prefetch_l2_line(reinterpret_cast<const uint8_t*>(row) + l * 128);
+                    }
+                }
+            };
+            // Pacing is advisory: a bounded spin on the epilogue's tile counter,
+            // then prefetch anyway.
+            volatile uint32_t* aborted = abort_flag;
+            uint32_t lt = 0;
+            for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
+                for (uint32_t spin = 0; spin < (1u << 22) && lt > *sTilesDone + 3u && !*aborted;
+                     ++spin) {
+                }
+                if (*aborted) break;
+                prefetch_tile(tile);
+            }
+        } else if (AMODE == kATmaGather) {
             // TMA gather4 through the indirection buffer.  The four gather warps
             // take turns: warp gw fills the stages whose sequence number is gw
             // mod 4, so each has four stage-times to look its rows up.  Lane l
@@ -528,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint8_t* stage_a = sA + ring.stage * AST;
-#pragma unroll 1
+#pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         uint32_t w4[4] = {0u, 0u, 0u, 0u};
                         const int h = ho * p.nw_s - p.nw_p + kh;
@@ -562,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive(&full_a[ring.stage]);
                 }
                 ptx::mbar_arrive(&stg_empty[slot]);
-                if (++slot == 2) {
+                if (++slot == NS) {
                     slot = 0;
                     slot_phase ^= 1u;
                 }
@@ -783,14 +826,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                src, row_bytes, &stg_full[slot]);
                         }
                     }
-                    if (++slot == 2) {
+                    if (++slot == NS) {
                         slot = 0;
                         slot_phase ^= 1u;
                     }
                 }
                 // Wait (bounded) for the last copies so none lands after the CTA exits.
-                for (uint32_t i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-                    drain_wait(&stg_full[i % 2], (i / 2) & 1u, 1000000000ull);
+                for (uint32_t i = issued > NS ? issued - NS : 0; i < issued; ++i)
+                    drain_wait(&stg_full[i % NS], (i / NS) & 1u, 1000000000ull);
             } else if (WINDOW) {
                 // Per (tile, kh, cc): one box of win_wv pixels x 64 channels for each
                 // of the tile's output rows (input row ho - p + kh*d, columns -p ..
@@ -928,7 +971,7 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
     }
     const int smem = igemm_smem_bytes(BN, p.stages, p.bres, p.kb_total, p.a_stage_bytes,
                                       p.b_per_stage,
-                                      (AMODE == kANarrowWin ? 2 * p.nw_slot_bytes : 0) +
+                                      (AMODE == kANarrowWin ? p.nw_slots * p.nw_slot_bytes : 0) +
                                           (p.tma_store ? kEpiStageBytes : 0));
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
     const int tiles = p.m_tiles * p.n_tiles * p.splits;

@@ -65,12 +65,14 @@ struct IgemmParams {
     // pixels (W_out real + (KW-1)*d spill); K block kb = (kh, cc)
     int win_wv, win_rows, win_groups, win_wout, win_kw, win_d, win_pad, win_cc;
     FastDiv ho_div;          // divides an output-row index (n*H_out + ho) by H_out
+    int x_H, x_W, x_KH;      // window mode: input geometry (L2 prefetch of input rows)
     // narrow-window mode: staged input rows
     int nw_H, nw_W, nw_KH, nw_s, nw_p, nw_cin;
     int nw_rb;               // bytes per staged row (16-byte multiple)
     int nw_a0;               // byte offset of the row's data inside its staged row
     int nw_kwc, nw_kwcp;     // KW*C_in, and that padded to a multiple of 8
-    int nw_slot_bytes;       // bytes of one tile's staged rows (two slots)
+    int nw_slot_bytes;       // bytes of one tile's staged rows
+    int nw_slots;            // staged-row slots (2 or 4)
     int tma_store;           // 1: epilogue stages 64-column chunks in shared memory and
                              //    stores them with TMA (bf16 y, C_out % 8 == 0, no split)
     int bres;                // 1: all of W's single column tile resident in shared memory

@@ -162,6 +162,12 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Hint that the 128-byte line holding `addr` will be read soon (into L2).
+__device__ __forceinline__ void prefetch_l2_line(const void* addr)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // Contiguous global->shared bulk copy, completion counted in bytes on `bar`.
 // Both addresses and the size must be multiples of 16 bytes.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
