@@ -78,11 +78,16 @@ typedef enum convgb_path {
                                  whole unpadded image (a dense layer); no workspace */
     CONVGB_PATH_STEM = 3,     /* C_in not a multiple of 8: each tap's channels padded to 4
                                  (C_in <= 4) or to a multiple of 8, scalar gather */
-    CONVGB_PATH_WINDOW = 4    /* stride 1, C_in % 64 == 0, W_out + (KW-1)*d <= 128 and
+    CONVGB_PATH_WINDOW = 4,   /* stride 1, C_in % 64 == 0, W_out + (KW-1)*d <= 128 and
                                  (KW-1)*d <= 8: tiles of whole output rows; each input row
                                  is staged in shared memory once per (kh, 64-channel block)
                                  by TMA and read by all KW taps ("Im2win", Abstract: the
                                  window order and its continuous accesses, on chip) */
+    CONVGB_PATH_PLANE = 5     /* the window path's shapes: the batch read as one tall image
+                                 of padded rows, tiles of whole padded rows; each input row
+                                 is staged once per (tile, 64-channel block) and read by all
+                                 KH*KW taps; rows and columns of the padding border are
+                                 computed and discarded.  No workspace. */
 } convgb_path;
 
 /* Short English text for a status code; never NULL. */

@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -116,12 +117,14 @@ NarrowRows narrow_rows(const ConvShape& c)
 struct GemmPlan;
 GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32 = 0);
 bool window_applies(const ConvShape& c);
+bool plane_applies(const ConvShape& c);
 
 // Whether `path` can compute this shape.
 bool path_supports(int path, const ConvShape& c)
 {
     switch (path) {
     case CONVGB_PATH_WINDOW: return window_applies(c);
+    case CONVGB_PATH_PLANE: return plane_applies(c);
     case CONVGB_PATH_GATHER: return c.C_in % 8 == 0;
     case CONVGB_PATH_DENSE: return c.C_in % 8 == 0 && (is_pointwise(c) || is_full_spatial(c));
     case CONVGB_PATH_STEM: return c.C_in % 8 != 0;
@@ -217,6 +220,7 @@ struct GemmPlan {
     int extra_smem = 0;            // narrow window: staged-row slots
     int nw_slots = 0;
     int tma_store = 0;             // epilogue through shared memory and TMA stores
+    int pl_u = 1, pl_nacc = 0, b_stages = 0;  // plane mode: sub-tiles, accumulators, B slots
     long long M = 0, K = 0;
     int num_kb = 0, m_tiles = 0, n_tiles = 0;
 };
@@ -260,13 +264,127 @@ void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
 }
 
 GemmPlan plan_gemm_ring(int path, const ConvShape& c);
+GemmPlan plan_plane(const ConvShape& c, int y_f32);
 
 GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32)
 {
+    if (path == CONVGB_PATH_PLANE) return plan_plane(c, y_f32);
     GemmPlan g = plan_gemm_ring(path, c);
     plan_epilogue(g, c, y_f32);
     return g;
 }
+
+// Plane mode.  With stride 1 the padded images stacked along H form one tall
+// image of N*(H+2p) rows of W+2p pixels; every output pixel (n, ho, wo) is
+// virtual pixel (n*(H+2p) + ho, wo) of it, and tap (kh, kw) of virtual pixel
+// (v, w) reads padded pixel (v + kh*d, w + kw*d).  A tile holds R = 128 / (W+2p)
+// whole virtual rows per sub-tile, so in the row-major staging of its padded
+// rows every tap is the same 128-row window shifted by kh*d*(W+2p) + kw*d rows.
+// Virtual pixels in the padding border (wo >= W_out, ho >= H_out) are computed
+// and discarded.  Candidates differ in sub-tiles per tile (1 or 2, sharing each
+// weight block), the column-tile width and whether the weights stay resident;
+// the one with the least estimated time wins.  The estimate per tile is the
+// larger of its tensor-core time and its L2-to-SM bytes at a per-SM share of
+// L2 bandwidth, times the waves of tiles over the SMs.
+GemmPlan plan_plane(const ConvShape& c, int y_f32)
+{
+    GemmPlan best;
+    best.amode = kAPlane;
+    if (!window_geometry(c)) return best;  // stages == 0: not applicable
+    const int wv = c.W + 2 * c.p;
+    const int hp = c.H + 2 * c.p;
+    const int R = 128 / wv;
+    const long long vrows = (long long)c.N * hp - (long long)(c.KH - 1) * c.d;
+    if ((long long)c.N * hp * wv >= (1LL << 31)) return best;
+    const int cc = c.C_in / 64;
+    const int taps = c.KH * c.KW;
+    const int kb_total = taps * cc;
+    const int limit = smem_limit();
+    const bool epi_ok = !y_f32 && c.C_out % 8 == 0;
+    constexpr double kSmClock = 1.9e9, kL2PerSm = 50e9;
+    constexpr int kNominalSms = 148;
+    double best_cost = 1e30;
+    const int bn_top = pick_bn(c.C_out);
+    for (int bn = bn_top; bn >= 64 || bn == bn_top; bn /= 2) {
+        const int n_tiles = (c.C_out + bn - 1) / bn;
+        for (int u = 1; u <= 2; ++u) {
+            if (u * bn > 256) continue;  // at least two accumulators in tensor memory
+            const int rows = ((u - 1) * R + (c.KH - 1) * c.d) * wv + (c.KW - 1) * c.d + 128;
+            const int ast = (rows * 128 + 1023) / 1024 * 1024;
+            const long long m_tiles = (vrows + u * R - 1) / (u * R);
+            for (int bres = (n_tiles == 1) ? 1 : 0; bres >= 0; --bres) {
+                for (int epi = (epi_ok && bn >= 64) ? 1 : 0; epi >= 0; --epi) {
+                    const int extra = epi ? kEpiStageBytes : 0;
+                    int sa = 0, sb = 0;
+                    if (bres) {
+                        for (int s = 8; s >= 2 && !sa; --s)
+                            if (plane_smem_bytes(bn, s, ast, kb_total, extra) <= limit) sa = s;
+                    } else {
+                        for (int s = 3; s >= 2 && !sa; --s)
+                            for (int b = 8; b >= 3 && !sb; --b)
+                                if (plane_smem_bytes(bn, s, ast, b, extra) <= limit) {
+                                    sa = s;
+                                    sb = b;
+                                }
+                        if (sa == 3 && sb < 6) {  // prefer a deeper weight ring
+                            for (int b = 8; b >= 3; --b)
+                                if (plane_smem_bytes(bn, 2, ast, b, extra) <= limit) {
+                                    if (b > sb) {
+                                        sa = 2;
+                                        sb = b;
+                                    }
+                                    break;
+                                }
+                        }
+                    }
+                    if (sa < 2) continue;
+                    const double mma_cyc = (double)cc * taps * u * 4 * (bn / 2 > 48 ? bn / 2 : 48);
+                    const double l2 = (double)cc * (u * R + (c.KH - 1) * c.d) * wv * 128 +
+                                      (bres ? 0.0 : (double)cc * taps * bn * 128);
+                    const double t_tile = std::max(mma_cyc / kSmClock, l2 / kL2PerSm);
+                    const long long tiles = m_tiles * n_tiles;
+                    const double cost =
+                        (double)((tiles + kNominalSms - 1) / kNominalSms) * t_tile;
+                    if (cost < best_cost * 0.98) {
+                        best_cost = cost;
+                        GemmPlan g;
+                        g.amode = kAPlane;
+                        g.M = c.M;
+                        g.K = c.K;
+                        g.bn = bn;
+                        g.win_wv = wv;
+                        g.win_rows = R;
+                        g.pl_u = u;
+                        g.m_step = u * R;
+                        g.m_tiles = (int)m_tiles;
+                        g.n_tiles = n_tiles;
+                        g.num_kb = cc;
+                        g.a_stage_bytes = ast;
+                        g.bres = bres;
+                        g.stages = sa;
+                        g.b_stages = bres ? 0 : sb;
+                        g.pl_nacc = std::min(4, 512 / (u * bn));
+                        g.tma_store = epi;
+                        best = g;
+                    }
+                    break;  // the epilogue staging tile is used whenever it fits
+                }
+            }
+        }
+        if (bn <= 32) break;
+    }
+    if (best.stages >= 2) {
+        if (c.KH == 3 && c.KW == 3) best.amode = best.pl_u == 2 ? kAPlane3U2 : kAPlane3;
+        const long long im2col = c.M * c.K * 2;
+        const long long partial = c.M * c.C_out * 4;
+        best.splits = choose_splits((long long)best.m_tiles * best.n_tiles, best.num_kb, partial,
+                                    im2col / 2);
+        if (best.splits > 1) best.tma_store = 0;
+    }
+    return best;
+}
+
+bool plane_applies(const ConvShape& c) { return plan_plane(c, 0).stages >= 2; }
 
 // Operand producers, tiles, splits and the shared-memory ring.
 GemmPlan plan_gemm_ring(int path, const ConvShape& c)
@@ -430,14 +548,16 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     // TMA gather: x as [N*H*W][C_in], one-row boxes of 64 channels.
     if (g.amode == kATmaGather && !encode_kmajor(&out->ta, a.x, a.x_rows, a.C_in, 1))
         return CONVGB_ERR_CUDA;
-    if (g.amode == kAWindow) {
+    const bool plane = g.amode == kAPlane || g.amode == kAPlane3 || g.amode == kAPlane3U2;
+    if (g.amode == kAWindow || plane) {
         const ConvShape& c = *a.shape;
         if (!encode_window(&out->ta, a.x, c.N, c.H, c.W, c.C_in, g.win_wv)) return CONVGB_ERR_CUDA;
     }
     // TMA-store epilogue: y as [M][C_out], boxes of 64 channels x (one output row
     // for row tiles, 128 rows otherwise).
     if (g.tma_store) {
-        const int box_rows = (g.amode == kAWindow || g.amode == kANarrowWin) ? a.shape->W_out : 128;
+        const int box_rows =
+            (g.amode == kAWindow || g.amode == kANarrowWin || plane) ? a.shape->W_out : 128;
         if (!encode_kmajor(&out->ty, a.y, g.M, a.C_out, box_rows)) return CONVGB_ERR_CUDA;
     }
     unsigned* err = device_error_word();
@@ -464,6 +584,8 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     p.m_tiles = g.m_tiles;
     p.n_tiles = g.n_tiles;
     p.splits = g.splits;
+    p.split_div = FastDiv((uint32_t)g.splits);
+    p.ntile_div = FastDiv((uint32_t)g.n_tiles);
     p.tma_store = g.tma_store;
     p.stages = g.stages;
     p.bres = g.bres;
@@ -506,6 +628,26 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.x_W = c.W;
         p.x_KH = c.KH;
     }
+    if (plane) {
+        const ConvShape& c = *a.shape;
+        p.win_wv = g.win_wv;
+        p.win_rows = g.win_rows;
+        p.win_wout = c.W_out;
+        p.win_kw = c.KW;
+        p.win_d = c.d;
+        p.win_pad = c.p;
+        p.win_cc = c.C_in / 64;
+        p.x_H = c.H;
+        p.x_W = c.W;
+        p.x_KH = c.KH;
+        p.pl_u = g.pl_u;
+        p.pl_srows = g.pl_u * g.win_rows + (c.KH - 1) * c.d;
+        p.pl_n = c.N;
+        p.pl_hout = c.H_out;
+        p.pl_nacc = g.pl_nacc;
+        p.b_stages = g.b_stages;
+        p.hp_div = FastDiv((uint32_t)(c.H + 2 * c.p));
+    }
     if (g.stages < 2) return CONVGB_ERR_UNSUPPORTED;
     p.partial = a.partial;
     p.y_f32 = a.y_f32;
@@ -542,7 +684,7 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
     if (y_dtype != CONVGB_BF16 && y_dtype != CONVGB_F32) return CONVGB_ERR_INVALID_ARG;
     if (path == CONVGB_PATH_AUTO) path = select_path(c);
     if (path != CONVGB_PATH_GATHER && path != CONVGB_PATH_DENSE && path != CONVGB_PATH_STEM &&
-        path != CONVGB_PATH_WINDOW)
+        path != CONVGB_PATH_WINDOW && path != CONVGB_PATH_PLANE)
         return CONVGB_ERR_INVALID_ARG;
     if (!path_supports(path, c)) return CONVGB_ERR_UNSUPPORTED;
     WsLayout L = workspace_layout(path, c);
@@ -567,7 +709,7 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
     if (path == CONVGB_PATH_DENSE) {
         // 1x1 stride-1: A = x as [N*H*W][C_in]; full-spatial: A = x as [N][H*W*C_in].
         a.a_dense = x;
-    } else if (path == CONVGB_PATH_WINDOW) {
+    } else if (path == CONVGB_PATH_WINDOW || path == CONVGB_PATH_PLANE) {
         a.x = static_cast<const uint16_t*>(x);
         a.C_in = C_in;
         a.shape = &c;

@@ -51,7 +51,7 @@ constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kSmemLimit = 232448;    // opt-in dynamic shared memory per block
 constexpr int kMaxAcc = 4;
 constexpr int kMaxSlots = 4;  // narrow window: staged-row slots
-static_assert((3 * kMaxStages + 2 * kMaxAcc + 2 + 2 * kMaxSlots) * 8 + 8 + 20 <= kHeaderBytes,
+static_assert((4 * kMaxStages + 2 * kMaxAcc + 2 + 2 * kMaxSlots) * 8 + 8 + 20 <= kHeaderBytes,
               "header area");
 
 template <int BN>
@@ -193,16 +193,27 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, int m, int co0
 struct Unit {
     int m0, n0, kb0, kb1;
 };
+// Every role evaluates this once per tile, and on the MMA thread it sits
+// between two tiles' MMA groups, so it uses the host-prepared multiply-shift
+// dividers (a run-time division, and above all a 64-bit one, costs hundreds of
+// cycles there).
 template <int BN>
 __device__ __forceinline__ Unit unit_of(const IgemmParams& p, int tile)
 {
-    const int ks = tile % p.splits;
-    const int mn = tile / p.splits;
+    uint32_t mn = static_cast<uint32_t>(tile), ks = 0;
+    if (p.splits > 1) p.split_div.divmod(static_cast<uint32_t>(tile), mn, ks);
+    uint32_t mt = mn, nt = 0;
+    if (p.n_tiles > 1) p.ntile_div.divmod(mn, mt, nt);
     Unit u;
-    u.m0 = (mn / p.n_tiles) * p.m_step;
-    u.n0 = (mn % p.n_tiles) * BN;
-    u.kb0 = static_cast<int>(static_cast<long long>(ks) * p.num_kb / p.splits);
-    u.kb1 = static_cast<int>(static_cast<long long>(ks + 1) * p.num_kb / p.splits);
+    u.m0 = static_cast<int>(mt) * p.m_step;
+    u.n0 = static_cast<int>(nt) * BN;
+    u.kb0 = 0;
+    u.kb1 = p.num_kb;
+    if (p.splits > 1) {
+        const uint32_t nkb = static_cast<uint32_t>(p.num_kb);
+        u.kb0 = static_cast<int>(p.split_div.div(ks * nkb));
+        u.kb1 = static_cast<int>(p.split_div.div((ks + 1u) * nkb));
+    }
     return u;
 }
 
@@ -239,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool GATHER =
         AMODE == kAGather || AMODE == kANarrow || AMODE == kATmaGather || NARROWWIN;
     constexpr bool WINDOW = AMODE == kAWindow;
+    constexpr bool PLANE = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     constexpr bool ROWTILES = WINDOW || NARROWWIN;  // tiles of whole output rows
     const uint32_t S = static_cast<uint32_t>(p.stages);
     const uint32_t AST = static_cast<uint32_t>(p.a_stage_bytes);
@@ -247,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full_a = bars;                  // A stage ready
     uint64_t* full_b = bars + kMaxStages;     // B stage ready (tx bytes), count 1
     uint64_t* empty = bars + 2 * kMaxStages;  // MMA done with stage, count 1 (tcgen05.commit)
-    uint64_t* tfull = bars + 3 * kMaxStages;  // accumulator ready, count 1 (tcgen05.commit)
+    uint64_t* empty_b = bars + 3 * kMaxStages;  // plane mode: MMA done with B slot, count 1
+    uint64_t* tfull = bars + 4 * kMaxStages;  // accumulator ready, count 1 (tcgen05.commit)
     uint64_t* tempty = tfull + kMaxAcc;       // accumulator drained, count kEpiThreads
     uint64_t* drain = tempty + kMaxAcc;       // MMA unwinding, count 1
     uint64_t* bres_full = drain + 1;          // resident weights loaded (tx bytes), count 1
@@ -260,8 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = ptx::smem_addr(smem_raw) + kHeaderBytes;
     uint8_t* data = smem_raw + kHeaderBytes + ((1024u - (base & 1023u)) & 1023u);
     uint8_t* sB = data;
-    const uint32_t b_blocks =
-        p.bres ? static_cast<uint32_t>(p.kb_total) : S * static_cast<uint32_t>(p.b_per_stage);
+    const uint32_t SB = PLANE ? static_cast<uint32_t>(p.b_stages) : 0u;  // plane: B ring slots
+    const uint32_t b_blocks = p.bres ? static_cast<uint32_t>(p.kb_total)
+                              : PLANE ? SB
+                                      : S * static_cast<uint32_t>(p.b_per_stage);
+    // Accumulators: plane mode keeps pl_u sub-tiles of BN columns per tile.
+    const uint32_t NACC = PLANE ? static_cast<uint32_t>(p.pl_nacc) : static_cast<uint32_t>(C::kAcc);
+    const uint32_t ACCW = PLANE ? static_cast<uint32_t>(p.pl_u * BN) : static_cast<uint32_t>(BN);
+    constexpr uint32_t kTmemAlloc = PLANE ? 512u : static_cast<uint32_t>(C::kTmemCols);
     uint8_t* sA = data + b_blocks * C::kBBytes;
     uint8_t* sStg = sA + S * AST;  // narrow window: nw_slots slots of staged input rows
     const uint32_t NS = NARROWWIN ? static_cast<uint32_t>(p.nw_slots) : 1u;
@@ -278,11 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; ++s) {
             // TMA gather: one arrive.expect_tx per stage; thread gathers: every thread arrives.
-            ptx::mbar_init(&full_a[s], AMODE == kATmaGather ? 1 : kGatherThreads);
+            ptx::mbar_init(&full_a[s], (AMODE == kATmaGather || PLANE) ? 1 : kGatherThreads);
             ptx::mbar_init(&full_b[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        for (int i = 0; i < C::kAcc; ++i) {
+        for (uint32_t s = S; s < SB; ++s) ptx::mbar_init(&full_b[s], 1);
+        for (uint32_t s = 0; s < SB; ++s) ptx::mbar_init(&empty_b[s], 1);
+        for (uint32_t i = 0; i < NACC; ++i) {
             ptx::mbar_init(&tfull[i], 1);
             ptx::mbar_init(&tempty[i], kEpiThreads);
         }
@@ -297,11 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_barrier_init();
     }
     if (warp == kTmaWarp && lane == 0) {
-        if (AMODE == kADense || AMODE == kATmaGather || WINDOW) ptx::prefetch_tensormap(&tmap_a);
+        if (AMODE == kADense || AMODE == kATmaGather || WINDOW || PLANE)
+            ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == kMmaWarp) {
-        ptx::tmem_alloc(tmem_slot, C::kTmemCols);
+        ptx::tmem_alloc(tmem_slot, kTmemAlloc);
         ptx::tmem_relinquish();
     }
     if (NARROWWIN) {
@@ -326,16 +348,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // virtual pixel (wrow, wcol) of the tile's output rows; spill columns
         // (wcol >= W_out) and rows past the tile's output rows are discarded.
         const int r = warp * 32 + lane;
-        const int wrow = ROWTILES ? r / p.win_wv : 0;
-        const int wcol = ROWTILES ? r - wrow * p.win_wv : 0;
+        const int wrow = (ROWTILES || PLANE) ? r / p.win_wv : 0;
+        const int wcol = (ROWTILES || PLANE) ? r - wrow * p.win_wv : 0;
         uint32_t lt = 0;
         int bias_n0 = -1;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
+        Ring ar;  // accumulator index and the parity of its current use
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt, ar.next(NACC)) {
             const Unit u = unit_of<BN>(p, tile);
-            const uint32_t acc = lt % C::kAcc, use = lt / C::kAcc;
+            const uint32_t acc = ar.stage;
             // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds,
             // and with the TMA store all four warps do (they share named barriers).
-            bool ready = __all_sync(0xffffffffu, wait_bar(&tfull[acc], use & 1u, wc, kRoleEpilogue));
+            bool ready = __all_sync(0xffffffffu, wait_bar(&tfull[acc], ar.phase, wc, kRoleEpilogue));
             if (p.tma_store) {
                 if (lane == 0) sVote[warp] = ready ? 1u : 0u;
                 ptx::named_barrier_sync(1, kEpiThreads);
@@ -344,95 +367,125 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ready) break;
             ptx::tc_fence_after();
-            int m = u.m0 + r;
-            if (ROWTILES) {
-                const int g = u.m0 + wrow;  // output row n*H_out + ho
-                const bool real = wrow < p.win_rows && wcol < p.win_wout && g < p.win_groups;
-                m = real ? g * p.win_wout + wcol : p.M;
+            if (p.tma_store && u.n0 != bias_n0) {  // new column tile: stage its bias
+                ptx::named_barrier_sync(1, kEpiThreads);
+                for (int i = r; i < BN; i += kEpiThreads)
+                    sBias[i] = (p.bias != nullptr && u.n0 + i < p.C_out)
+                                   ? bf16_bits_to_float(p.bias[u.n0 + i])
+                                   : 0.f;
+                ptx::named_barrier_sync(1, kEpiThreads);
+                bias_n0 = u.n0;
             }
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
-            const bool live = m < p.M;
-            if (p.tma_store) {
-                if (u.n0 != bias_n0) {  // new column tile: stage its bias
-                    ptx::named_barrier_sync(1, kEpiThreads);
-                    for (int i = r; i < BN; i += kEpiThreads)
-                        sBias[i] = (p.bias != nullptr && u.n0 + i < p.C_out)
-                                       ? bf16_bits_to_float(p.bias[u.n0 + i])
-                                       : 0.f;
-                    ptx::named_barrier_sync(1, kEpiThreads);
-                    bias_n0 = u.n0;
+            const uint32_t tbase =
+                tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * ACCW;
+            const int nsub = PLANE ? p.pl_u : 1;
+            for (int sub = 0; sub < nsub; ++sub) {
+                const bool last_sub = sub + 1 == nsub;
+                int m = u.m0 + r;
+                if (PLANE) {
+                    // virtual row v of the stacked padded batch: image v / (H+2p), row v % (H+2p)
+                    const int v = u.m0 + sub * p.win_rows + wrow;
+                    uint32_t n, hv;
+                    p.hp_div.divmod(static_cast<uint32_t>(v), n, hv);
+                    const bool real = wrow < p.win_rows && wcol < p.win_wout &&
+                                      static_cast<int>(hv) < p.pl_hout &&
+                                      static_cast<int>(n) < p.pl_n;
+                    m = real ? (static_cast<int>(n) * p.pl_hout + static_cast<int>(hv)) * p.win_wout +
+                                   wcol
+                             : p.M;
+                } else if (ROWTILES) {
+                    const int g = u.m0 + wrow;  // output row n*H_out + ho
+                    const bool real = wrow < p.win_rows && wcol < p.win_wout && g < p.win_groups;
+                    m = real ? g * p.win_wout + wcol : p.M;
                 }
+                const uint32_t taddr = tbase + static_cast<uint32_t>(sub * BN);
+                const bool live = m < p.M;
+                if (p.tma_store) {
 #pragma unroll 1
-                for (int c64 = 0; c64 < BN / 64; ++c64) {
+                    for (int c64 = 0; c64 < BN / 64; ++c64) {
+                        uint32_t ra[32], rb[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
+                        ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
+                        ptx::tmem_ld_wait();
+                        if (last_sub && c64 + 1 == BN / 64) {
+                            ptx::tc_fence_before();
+                            ptx::mbar_arrive(&tempty[acc]);
+                        }
+                        // The staging tile is free once the previous store has read it.
+                        if (r == 0) ptx::bulk_wait_read_all();
+                        ptx::named_barrier_sync(1, kEpiThreads);
+                        const float* bs = sBias + c64 * 64;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const uint32_t* src = q < 4 ? ra + 8 * q : rb + 8 * (q - 4);
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(src[0]) + bs[8 * q + 0],
+                                              __uint_as_float(src[1]) + bs[8 * q + 1]);
+                            v.y = pack_bf16x2(__uint_as_float(src[2]) + bs[8 * q + 2],
+                                              __uint_as_float(src[3]) + bs[8 * q + 3]);
+                            v.z = pack_bf16x2(__uint_as_float(src[4]) + bs[8 * q + 4],
+                                              __uint_as_float(src[5]) + bs[8 * q + 5]);
+                            v.w = pack_bf16x2(__uint_as_float(src[6]) + bs[8 * q + 6],
+                                              __uint_as_float(src[7]) + bs[8 * q + 7]);
+                            *reinterpret_cast<uint4*>(sEpi + r * 128 + ((q ^ (r & 7)) << 4)) = v;
+                        }
+                        ptx::fence_proxy_async_smem();
+                        ptx::named_barrier_sync(1, kEpiThreads);
+                        if (r == 0) {
+                            const int c0 = u.n0 + c64 * 64;
+                            if (PLANE) {
+                                // one box per real output row of this sub-tile
+                                for (int jj = 0; jj < p.win_rows; ++jj) {
+                                    uint32_t n, hv;
+                                    p.hp_div.divmod(
+                                        static_cast<uint32_t>(u.m0 + sub * p.win_rows + jj), n, hv);
+                                    if (static_cast<int>(n) >= p.pl_n ||
+                                        static_cast<int>(hv) >= p.pl_hout)
+                                        continue;
+                                    ptx::tma_store_2d(
+                                        &tmap_y, sEpi + jj * p.win_wv * 128, c0,
+                                        (static_cast<int>(n) * p.pl_hout + static_cast<int>(hv)) *
+                                            p.win_wout);
+                                }
+                            } else if (ROWTILES) {
+                                const int rows = min(p.win_rows, p.win_groups - u.m0);
+                                for (int jj = 0; jj < rows; ++jj)
+                                    ptx::tma_store_2d(&tmap_y, sEpi + jj * p.win_wv * 128, c0,
+                                                      (u.m0 + jj) * p.win_wout);
+                            } else {
+                                ptx::tma_store_2d(&tmap_y, sEpi, c0, u.m0);
+                            }
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                    continue;
+                }
+                // Direct stores: two 32-column chunks per TMEM round trip; the
+                // accumulator is handed back to the MMA warp as soon as its last
+                // chunk is in registers.
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 32; ch += 2) {
                     uint32_t ra[32], rb[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
-                    ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
+                    ptx::tmem_ld_32x32b_x32(taddr + ch * 32, ra);
+                    if (ch + 1 < BN / 32) ptx::tmem_ld_32x32b_x32(taddr + (ch + 1) * 32, rb);
                     ptx::tmem_ld_wait();
-                    if (c64 + 1 == BN / 64) {
+                    if (last_sub && ch + 2 >= BN / 32) {
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(&tempty[acc]);
                     }
-                    // The staging tile is free once the previous store has read it.
-                    if (r == 0) ptx::bulk_wait_read_all();
-                    ptx::named_barrier_sync(1, kEpiThreads);
-                    const float* bs = sBias + c64 * 64;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint32_t* src = q < 4 ? ra + 8 * q : rb + 8 * (q - 4);
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(src[0]) + bs[8 * q + 0],
-                                          __uint_as_float(src[1]) + bs[8 * q + 1]);
-                        v.y = pack_bf16x2(__uint_as_float(src[2]) + bs[8 * q + 2],
-                                          __uint_as_float(src[3]) + bs[8 * q + 3]);
-                        v.z = pack_bf16x2(__uint_as_float(src[4]) + bs[8 * q + 4],
-                                          __uint_as_float(src[5]) + bs[8 * q + 5]);
-                        v.w = pack_bf16x2(__uint_as_float(src[6]) + bs[8 * q + 6],
-                                          __uint_as_float(src[7]) + bs[8 * q + 7]);
-                        *reinterpret_cast<uint4*>(sEpi + r * 128 + ((q ^ (r & 7)) << 4)) = v;
+                    const int co0 = u.n0 + ch * 32;
+                    if (live && co0 < p.C_out) {
+                        if (p.splits > 1)
+                            reduce_chunk(p, m, co0, ra);
+                        else
+                            store_chunk(p, m, co0, ra);
                     }
-                    ptx::fence_proxy_async_smem();
-                    ptx::named_barrier_sync(1, kEpiThreads);
-                    if (r == 0) {
-                        const int c0 = u.n0 + c64 * 64;
-                        if (ROWTILES) {
-                            const int rows = min(p.win_rows, p.win_groups - u.m0);
-                            for (int jj = 0; jj < rows; ++jj)
-                                ptx::tma_store_2d(&tmap_y, sEpi + jj * p.win_wv * 128, c0,
-                                                  (u.m0 + jj) * p.win_wout);
-                        } else {
-                            ptx::tma_store_2d(&tmap_y, sEpi, c0, u.m0);
-                        }
-                        ptx::bulk_commit_group();
+                    if (live && ch + 1 < BN / 32 && co0 + 32 < p.C_out) {
+                        if (p.splits > 1)
+                            reduce_chunk(p, m, co0 + 32, rb);
+                        else
+                            store_chunk(p, m, co0 + 32, rb);
                     }
-                }
-                if (r == 0) *sTilesDone = lt + 1;
-                continue;
-            }
-            // Direct stores: two 32-column chunks per TMEM round trip; the
-            // accumulator is handed back to the MMA warp as soon as its last
-            // chunk is in registers.
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ch += 2) {
-                uint32_t ra[32], rb[32];
-                ptx::tmem_ld_32x32b_x32(taddr + ch * 32, ra);
-                if (ch + 1 < BN / 32) ptx::tmem_ld_32x32b_x32(taddr + (ch + 1) * 32, rb);
-                ptx::tmem_ld_wait();
-                if (ch + 2 >= BN / 32) {
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(&tempty[acc]);
-                }
-                const int co0 = u.n0 + ch * 32;
-                if (live && co0 < p.C_out) {
-                    if (p.splits > 1)
-                        reduce_chunk(p, m, co0, ra);
-                    else
-                        store_chunk(p, m, co0, ra);
-                }
-                if (live && ch + 1 < BN / 32 && co0 + 32 < p.C_out) {
-                    if (p.splits > 1)
-                        reduce_chunk(p, m, co0 + 32, rb);
-                    else
-                        store_chunk(p, m, co0 + 32, rb);
                 }
             }
             if (r == 0) *sTilesDone = lt + 1;
@@ -441,7 +494,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.tma_store && r == 0) ptx::bulk_wait_all();
     } else if (warp < kEpiWarps + kGatherWarps) {
         // ------------------------------------------------------------ A gather
-        if (WINDOW && warp == kEpiWarps) {
+        if (PLANE && warp == kEpiWarps) {
+            // Plane mode: one lane stages, per (tile, channel block cc), the
+            // pl_srows padded input rows the tile's taps read: virtual row v0 + j
+            // is row (v0 + j) % (H+2p) - p of image (v0 + j) / (H+2p), one box of
+            // win_wv pixels x 64 channels starting at column -p.  TMA zero-fills
+            // the padding rows and columns; rows past the last image are skipped
+            // (they feed only discarded accumulator rows).
+            if (lane == 0) {
+                const uint32_t row_bytes = static_cast<uint32_t>(p.win_wv) * 128u;
+                Ring ring;
+                uint32_t issued = 0;
+                bool ok = true;
+                for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                    const Unit u = unit_of<BN>(p, tile);
+                    for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
+                        if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleGather)) {
+                            ok = false;
+                            break;
+                        }
+                        uint32_t nrows = 0;
+                        for (int j = 0; j < p.pl_srows; ++j)
+                            nrows += static_cast<int>(
+                                         p.hp_div.div(static_cast<uint32_t>(u.m0 + j))) < p.pl_n
+                                         ? 1u
+                                         : 0u;
+                        ptx::mbar_arrive_expect_tx(&full_a[ring.stage], nrows * row_bytes);
+                        uint8_t* stage_a = sA + ring.stage * AST;
+                        for (int j = 0; j < p.pl_srows; ++j) {
+                            uint32_t n, hp;
+                            p.hp_div.divmod(static_cast<uint32_t>(u.m0 + j), n, hp);
+                            if (static_cast<int>(n) >= p.pl_n) continue;
+                            ptx::tma_load_4d(stage_a + j * row_bytes, &tmap_a, &full_a[ring.stage],
+                                             kb * BK, -p.win_pad,
+                                             static_cast<int>(hp) - p.win_pad, static_cast<int>(n));
+                        }
+                    }
+                }
+                // Wait (bounded) for the last loads so none lands after the CTA exits.
+                const uint32_t first = issued > S ? issued - S : 0;
+                for (uint32_t i = first; i < issued; ++i)
+                    drain_wait(&full_a[i % S], (i / S) & 1u, 1000000000ull);
+            }
+        } else if (PLANE && warp == kEpiWarps + 1) {
+            // Pulls the input rows of the CTA's next tiles into L2 with plain
+            // prefetches, at most three tiles ahead of the epilogue (advisory
+            // pacing: a bounded spin, then prefetch anyway).
+            const long long row_elems = static_cast<long long>(p.x_W) * p.C_in;
+            const int lines = static_cast<int>((row_elems * 2 + 127) / 128);
+            volatile uint32_t* aborted = abort_flag;
+            uint32_t lt = 0;
+            for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
+                for (uint32_t spin = 0; spin < (1u << 22) && lt > *sTilesDone + 3u && !*aborted;
+                     ++spin) {
+                }
+                if (*aborted) break;
+                const Unit v = unit_of<BN>(p, tile);
+                if (v.n0 != 0 || v.kb0 != 0) continue;  // one prefetch per row block
+                for (int j = 0; j < p.pl_srows; ++j) {
+                    uint32_t n, hp;
+                    p.hp_div.divmod(static_cast<uint32_t>(v.m0 + j), n, hp);
+                    const int h = static_cast<int>(hp) - p.win_pad;
+                    if (static_cast<int>(n) >= p.pl_n || h < 0 || h >= p.x_H) continue;
+                    const uint8_t* row = reinterpret_cast<const uint8_t*>(
+                        p.x + (static_cast<long long>(n) * p.x_H + h) * row_elems);
+                    for (int l = lane; l < lines; l += 32) ptx::prefetch_l2_line(row + l * 128);
+                }
+            }
+        } else if (WINDOW && warp == kEpiWarps) {
             // The gather warps have nothing to gather in window mode; the first
             // of them pulls the input rows of the next tiles into L2 with plain
             // prefetches (the TMA engine stays free for the loads themselves),
@@ -715,17 +835,148 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
+        if (PLANE && lane == 0) {
+            // Per tile and channel block cc: one staged A slot feeds every tap
+            // (kh, kw) of every sub-tile; tap (kh, kw) of sub-tile u starts
+            // u*win_rows*win_wv + kh*d*win_wv + kw*d rows into the slot.  Streamed
+            // weights arrive one (tap, cc) block per B slot.  Descriptors are
+            // formed by adding 16-byte-unit offsets to the slot bases (the start
+            // address field is the low 14 bits), and nothing on the issue path
+            // waits for arithmetic: with N = 128 an MMA lasts 64 cycles and a
+            // per-tap index computation between MMA groups would idle the tensor
+            // core.  3x3 kernels issue from a compile-time unrolled sequence; other
+            // kernels walk the taps with the next tap's offsets formed before the
+            // current tap's MMAs are issued.
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+            constexpr int CT = AMODE == kAPlane ? 0 : 9;  // compile-time taps (0: runtime)
+            constexpr int CU = AMODE == kAPlane3U2 ? 2 : 1;
+            const uint64_t a_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
+            const uint64_t b_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sB));
+            const uint32_t a_slot_step = AST >> 4;
+            constexpr uint32_t b_blk_step = C::kBBytes >> 4;
+            const uint32_t sub_step = static_cast<uint32_t>(p.win_rows * p.win_wv * 8);
+            const uint32_t row_step = static_cast<uint32_t>(p.win_wv * p.win_d * 8);  // kh + 1
+            const uint32_t col_step = static_cast<uint32_t>(p.win_d * 8);             // kw + 1
+            uint32_t aoff[CT > 0 ? CT : 1], boff[CT > 0 ? CT : 1];
+#pragma unroll
+            for (int t = 0; t < CT; ++t) {
+                aoff[t] = static_cast<uint32_t>(t / 3) * row_step + static_cast<uint32_t>(t % 3) * col_step;
+                boff[t] = static_cast<uint32_t>(t * p.win_cc) * b_blk_step;
+            }
+            Ring ra, rb;
+            uint32_t lt = 0;
+            bool ok = !p.bres || wait_bar(bres_full, 0u, wc, kRoleMma);
+            const int taps = p.x_KH * p.win_kw;
+            Ring ar;
+            for (int tile = blockIdx.x; ok && tile < total_tiles;
+                 tile += gridDim.x, ++lt, ar.next(NACC)) {
+                const Unit u = unit_of<BN>(p, tile);
+                const uint32_t acc = ar.stage;
+                if (!wait_bar(&tempty[acc], ar.phase ^ 1u, wc, kRoleMma)) break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * ACCW;
+                for (int kb = u.kb0; ok && kb < u.kb1; ++kb, ra.next(S)) {
+                    const uint64_t ad = a_desc0 + ra.stage * a_slot_step;
+                    const uint64_t bres_d = b_desc0 + static_cast<uint32_t>(kb) * b_blk_step;
+                    const uint32_t first = kb == u.kb0 ? 0u : 1u;  // accumulate flag of tap 0
+                    if (!wait_bar(&full_a[ra.stage], ra.phase, wc, kRoleMma)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    if (CT > 0) {
+#pragma unroll
+                        for (int t = 0; t < CT; ++t) {
+                            uint64_t bd = bres_d + boff[t];
+                            if (!p.bres) {
+                                if (!wait_bar(&full_b[rb.stage], rb.phase, wc, kRoleMma)) {
+                                    ok = false;
+                                    break;
+                                }
+                                ptx::tc_fence_after();
+                                bd = b_desc0 + rb.stage * b_blk_step;
+                            }
+#pragma unroll
+                            for (int sub = 0; sub < CU; ++sub)
+#pragma unroll
+                                for (int kk = 0; kk < BK / 16; ++kk)
+                                    ptx::mma_bf16(d_tmem + static_cast<uint32_t>(sub * BN),
+                                                  ad + aoff[t] + sub * sub_step + 2 * kk,
+                                                  bd + 2 * kk, idesc,
+                                                  (t != 0 || kk != 0) ? 1u : first);
+                            if (!p.bres) {
+                                ptx::mma_commit(&empty_b[rb.stage]);
+                                rb.next(SB);
+                            }
+                        }
+                    } else {
+                        int kh = 0, kw = 0;
+                        uint32_t a_next = 0;
+                        uint64_t b_next = bres_d;
+                        for (int t = 0; t < taps; ++t) {
+                            const uint32_t a_cur = a_next;
+                            uint64_t bd = b_next;
+                            if (++kw == p.win_kw) {
+                                kw = 0;
+                                ++kh;
+                            }
+                            a_next = static_cast<uint32_t>(kh) * row_step +
+                                     static_cast<uint32_t>(kw) * col_step;
+                            b_next += static_cast<uint64_t>(static_cast<uint32_t>(p.win_cc) *
+                                                            b_blk_step);
+                            if (!p.bres) {
+                                if (!wait_bar(&full_b[rb.stage], rb.phase, wc, kRoleMma)) {
+                                    ok = false;
+                                    break;
+                                }
+                                ptx::tc_fence_after();
+                                bd = b_desc0 + rb.stage * b_blk_step;
+                            }
+                            for (int sub = 0; sub < p.pl_u; ++sub)
+#pragma unroll
+                                for (int kk = 0; kk < BK / 16; ++kk)
+                                    ptx::mma_bf16(d_tmem + static_cast<uint32_t>(sub * BN),
+                                                  ad + a_cur + sub * sub_step + 2 * kk,
+                                                  bd + 2 * kk, idesc,
+                                                  (t != 0 || kk != 0) ? 1u : first);
+                            if (!p.bres) {
+                                ptx::mma_commit(&empty_b[rb.stage]);
+                                rb.next(SB);
+                            }
+                        }
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(&empty[ra.stage]);
+                }
+                if (ok) ptx::mma_commit(&tfull[acc]);
+            }
+            // Make sure no MMA is still reading shared memory or writing TMEM.
+            ptx::mma_commit(drain);
+            drain_wait(drain, 0, 1000000000ull);
+        } else if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+            const uint64_t a_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
+            const uint64_t b_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sB));
+            const uint32_t a_slot_step = AST >> 4;
+            constexpr uint32_t b_blk_step = C::kBBytes >> 4;
+            const uint32_t col_step = static_cast<uint32_t>(p.win_d * 8);  // window: kw + 1
             Ring ring;
             uint32_t lt = 0;
             bool ok = !p.bres || wait_bar(bres_full, 0u, wc, kRoleMma);
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++lt) {
+            Ring ar;
+            for (int tile = blockIdx.x; ok && tile < total_tiles;
+                 tile += gridDim.x, ++lt, ar.next(C::kAcc)) {
                 const Unit u = unit_of<BN>(p, tile);
-                const uint32_t acc = lt % C::kAcc, use = lt / C::kAcc;
-                if (!wait_bar(&tempty[acc], (use & 1u) ^ 1u, wc, kRoleMma)) break;
+                const uint32_t acc = ar.stage;
+                if (!wait_bar(&tempty[acc], ar.phase ^ 1u, wc, kRoleMma)) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
+                // window mode: (kh, cc) of the K block, walked instead of divided
+                int win_kh = 0, win_cc = 0;
+                if (WINDOW) {
+                    win_kh = u.kb0 / p.win_cc;
+                    win_cc = u.kb0 - win_kh * p.win_cc;
+                }
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
                     if (GATHER && !wait_bar(&full_a[ring.stage], ring.phase, wc, kRoleMma)) {
                         ok = false;
@@ -741,36 +992,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (AMODE == kAGather || AMODE == kANarrow || NARROWWIN)
                         ptx::fence_proxy_async_smem();
                     ptx::tc_fence_after();
-                    const uint32_t a_base = ptx::smem_addr(sA + ring.stage * AST);
+                    // Descriptors as slot bases plus 16-byte-unit offsets: no
+                    // division or address arithmetic between MMA groups.
+                    const uint64_t ad = a_desc0 + ring.stage * a_slot_step;
                     if (WINDOW) {
                         // One staged (kh, cc) block feeds every kw tap: tap kw reads
                         // the staging rows shifted down by kw*d.
-                        const int kh = kb / p.win_cc, cc = kb - kh * p.win_cc;
-                        for (int kw = 0; kw < p.win_kw; ++kw) {
-                            const uint32_t shift = static_cast<uint32_t>(kw * p.win_d);
-                            const uint64_t adesc = ptx::sdesc_k_major_sw128(a_base + shift * 128u);
-                            const uint32_t bblk =
-                                p.bres ? static_cast<uint32_t>((kh * p.win_kw + kw) * p.win_cc + cc)
-                                       : ring.stage * p.b_per_stage + kw;
-                            const uint64_t bdesc =
-                                ptx::sdesc_k_major_sw128(ptx::smem_addr(sB + bblk * C::kBBytes));
+                        const uint64_t bd0 =
+                            p.bres ? b_desc0 + static_cast<uint32_t>(win_kh * p.win_kw * p.win_cc +
+                                                                     win_cc) *
+                                                   b_blk_step
+                                   : b_desc0 + ring.stage * p.b_per_stage * b_blk_step;
+                        const uint32_t bstep = p.bres ? p.win_cc * b_blk_step : b_blk_step;
+                        const uint32_t first = kb != u.kb0 ? 1u : 0u;
+                        if (p.win_kw == 3) {
 #pragma unroll
-                            for (int kk = 0; kk < BK / 16; ++kk)
-                                ptx::mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                                              (kb != u.kb0 || kw != 0 || kk != 0) ? 1u : 0u);
+                            for (int kw = 0; kw < 3; ++kw)
+#pragma unroll
+                                for (int kk = 0; kk < BK / 16; ++kk)
+                                    ptx::mma_bf16(d_tmem, ad + kw * col_step + 2 * kk,
+                                                  bd0 + kw * bstep + 2 * kk, idesc,
+                                                  (kw != 0 || kk != 0) ? 1u : first);
+                        } else {
+                            for (int kw = 0; kw < p.win_kw; ++kw)
+#pragma unroll
+                                for (int kk = 0; kk < BK / 16; ++kk)
+                                    ptx::mma_bf16(d_tmem, ad + kw * col_step + 2 * kk,
+                                                  bd0 + kw * bstep + 2 * kk, idesc,
+                                                  (kw != 0 || kk != 0) ? 1u : first);
+                        }
+                        if (++win_cc == p.win_cc) {
+                            win_cc = 0;
+                            ++win_kh;
                         }
                     } else {
-                        const uint64_t adesc = ptx::sdesc_k_major_sw128(a_base);
-                        const uint32_t bblk = p.bres ? static_cast<uint32_t>(kb) : ring.stage;
-                        const uint64_t bdesc =
-                            ptx::sdesc_k_major_sw128(ptx::smem_addr(sB + bblk * C::kBBytes));
+                        const uint64_t bd =
+                            b_desc0 + (p.bres ? static_cast<uint32_t>(kb) : ring.stage) * b_blk_step;
                         // The last K block may hold fewer than 64 columns: skip the
                         // all-zero 16-column steps.
                         const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
                             if (kk < ksteps)
-                                ptx::mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                ptx::mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
                                               (kb != u.kb0 || kk != 0) ? 1u : 0u);
                     }
                     ptx::mma_commit(&empty[ring.stage]);
@@ -834,6 +1098,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Wait (bounded) for the last copies so none lands after the CTA exits.
                 for (uint32_t i = issued > NS ? issued - NS : 0; i < issued; ++i)
                     drain_wait(&stg_full[i % NS], (i / NS) & 1u, 1000000000ull);
+            } else if (PLANE) {
+                // Streamed weights: block (tap, cc) of the tile's column tile per
+                // B slot, in the order the MMA thread consumes them.
+                if (!p.bres) {
+                    const int taps = p.x_KH * p.win_kw;
+                    Ring rb;
+                    uint32_t issued = 0;
+                    bool ok = true;
+                    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                        const Unit u = unit_of<BN>(p, tile);
+                        for (int kb = u.kb0; ok && kb < u.kb1; ++kb)
+                            for (int t = 0; t < taps; ++t, ++issued, rb.next(SB)) {
+                                if (!wait_bar(&empty_b[rb.stage], rb.phase ^ 1u, wc, kRoleTma)) {
+                                    ok = false;
+                                    break;
+                                }
+                                ptx::mbar_arrive_expect_tx(&full_b[rb.stage], C::kBBytes);
+                                ptx::tma_load_2d(sB + rb.stage * C::kBBytes, &tmap_b,
+                                                 &full_b[rb.stage], (t * p.win_cc + kb) * BK, u.n0);
+                            }
+                    }
+                    const uint32_t first = issued > SB ? issued - SB : 0;
+                    for (uint32_t i = first; i < issued; ++i)
+                        drain_wait(&full_b[i % SB], (i / SB) & 1u, 1000000000ull);
+                }
             } else if (WINDOW) {
                 // Per (tile, kh, cc): one box of win_wv pixels x 64 channels for each
                 // of the tile's output rows (input row ho - p + kh*d, columns -p ..
@@ -913,7 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     if (warp == kMmaWarp) {
         __syncwarp();
-        ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+        ptx::tmem_dealloc(tmem_base, kTmemAlloc);
     }
 }
 
@@ -969,11 +1258,24 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
-    const int smem = igemm_smem_bytes(BN, p.stages, p.bres, p.kb_total, p.a_stage_bytes,
-                                      p.b_per_stage,
-                                      (AMODE == kANarrowWin ? p.nw_slots * p.nw_slot_bytes : 0) +
-                                          (p.tma_store ? kEpiStageBytes : 0));
+    const int extra = (AMODE == kANarrowWin ? p.nw_slots * p.nw_slot_bytes : 0) +
+                      (p.tma_store ? kEpiStageBytes : 0);
+    constexpr bool kPlane = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
+    const int smem =
+        kPlane
+            ? plane_smem_bytes(BN, p.stages, p.a_stage_bytes, p.bres ? p.kb_total : p.b_stages,
+                               extra)
+            : igemm_smem_bytes(BN, p.stages, p.bres, p.kb_total, p.a_stage_bytes, p.b_per_stage,
+                               extra);
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
+    if (kPlane &&
+        ((!p.bres && (p.b_stages < 2 || p.b_stages > kMaxStages)) || p.pl_u < 1 || p.pl_u > 2 ||
+         p.pl_nacc < 1 || p.pl_nacc > kMaxAcc || p.pl_nacc * p.pl_u * BN > 512))
+        return cudaErrorInvalidValue;
+    // the unrolled 3x3 variants fix the taps and the sub-tile count at compile time
+    if ((AMODE == kAPlane3 || AMODE == kAPlane3U2) &&
+        (p.x_KH != 3 || p.win_kw != 3 || p.pl_u != (AMODE == kAPlane3U2 ? 2 : 1)))
+        return cudaErrorInvalidValue;
     const int tiles = p.m_tiles * p.n_tiles * p.splits;
     const int grid = tiles < num_sms() ? tiles : num_sms();
     kern<<<grid, kThreads, smem, st>>>(ta, tb, ty, p);
@@ -1014,6 +1316,13 @@ int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per
 
 int window_stage_rows(int kw, int d) { return (BM + (kw - 1) * d + 7) / 8 * 8; }
 
+int plane_smem_bytes(int bn, int a_stages, int a_stage_bytes, int b_blocks, int extra_bytes)
+{
+    return kHeaderBytes + 1024 + b_blocks * bn * BK * 2 + a_stages * a_stage_bytes + extra_bytes;
+}
+
+int smem_limit() { return kSmemLimit; }
+
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtensorMap& tb,
                          const CUtensorMap& ty, const IgemmParams& p, cudaStream_t st)
 {
@@ -1024,6 +1333,9 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kATmaGather: return launch_mode<kATmaGather>(bn, ta, tb, ty, p, st);
     case kAWindow: return launch_mode<kAWindow>(bn, ta, tb, ty, p, st);
     case kANarrowWin: return launch_mode<kANarrowWin>(bn, ta, tb, ty, p, st);
+    case kAPlane: return launch_mode<kAPlane>(bn, ta, tb, ty, p, st);
+    case kAPlane3: return launch_mode<kAPlane3>(bn, ta, tb, ty, p, st);
+    case kAPlane3U2: return launch_mode<kAPlane3U2>(bn, ta, tb, ty, p, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -58,6 +58,8 @@ struct IgemmParams {
     int m_tiles, n_tiles;
     int m_step;              // tile origin step: 128 GEMM rows, or win_rows output rows
     int splits;              // K partitions per output tile (1: no split)
+    FastDiv split_div;       // divides by splits
+    FastDiv ntile_div;       // divides by n_tiles
     int stages;              // shared-memory ring depth (2..8)
     int a_stage_bytes;       // bytes of one A ring slot
     int b_per_stage;         // B K-blocks per ring slot (1; KW in window mode)
@@ -73,6 +75,17 @@ struct IgemmParams {
     int nw_kwc, nw_kwcp;     // KW*C_in, and that padded to a multiple of 8
     int nw_slot_bytes;       // bytes of one tile's staged rows
     int nw_slots;            // staged-row slots (2 or 4)
+    // plane mode (stride 1): the batch is one tall padded image of N*(H+2p)
+    // virtual rows; a tile is pl_u sub-tiles of win_rows virtual output rows,
+    // its A stage for channel block cc holds pl_srows whole padded input rows,
+    // and tap (kh, kw) of sub-tile u reads it from row u*win_rows*win_wv +
+    // kh*d*win_wv + kw*d on
+    int pl_u;                // sub-tiles per tile (1 or 2), each 128 accumulator rows
+    int pl_srows;            // staged input rows per A stage: pl_u*win_rows + (KH-1)*d
+    int pl_n, pl_hout;       // batch and output height
+    int pl_nacc;             // accumulators in tensor memory (each pl_u*BN columns)
+    int b_stages;            // streamed weights: B ring slots of one 64-column block
+    FastDiv hp_div;          // divides a virtual row index by H + 2p
     int tma_store;           // 1: epilogue stages 64-column chunks in shared memory and
                              //    stores them with TMA (bf16 y, C_out % 8 == 0, no split)
     int bres;                // 1: all of W's single column tile resident in shared memory
@@ -100,6 +113,13 @@ enum AMode : int {
     kANarrowWin = 5,  // small C_in: whole input rows bulk-copied to shared memory per tile,
                       // A built from them; K ordered (kh, kw*C_in) with each kh slice
                       // padded to a multiple of 8
+    kAPlane = 6,      // stride 1: tiles of whole padded rows of the stacked batch; each
+                      // input row is staged once per (tile, 64-channel block) and read by
+                      // all KH*KW taps at shifted starts; weights resident or streamed
+                      // one block per ring slot
+    kAPlane3 = 7,     // plane mode for 3x3 kernels, one sub-tile: the MMA issue sequence
+                      // of a staged block is unrolled at compile time
+    kAPlane3U2 = 8,   // plane mode for 3x3 kernels, two sub-tiles per weight block
 };
 // Dynamic shared memory of one implicit-GEMM CTA, and the deepest ring that fits
 // (0 when none does).
@@ -109,6 +129,10 @@ int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per
                       int extra_bytes = 0);
 // Rows of an A ring slot in window mode (128 plus the tap spill, rounded to 8).
 int window_stage_rows(int kw, int d);
+// Dynamic shared memory of a plane-mode CTA: a_stages A slots, b_blocks weight
+// blocks (resident or ring), plus extra bytes.
+int plane_smem_bytes(int bn, int a_stages, int a_stage_bytes, int b_blocks, int extra_bytes);
+int smem_limit();
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& tmap_a,
                          const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
                          const IgemmParams& p, cudaStream_t st);

@@ -32,14 +32,30 @@ def sample_points(shape, Ho, Wo, rng):
     return np.array(pts, dtype=np.int64)
 
 
-@pytest.mark.parametrize("shape", [c for c in workloads.ALL if c.name != workloads.TINY.name],
-                         ids=lambda s: s.name)
+def plane_able(c):
+    return (c.stride == 1 and c.C_in % 64 == 0 and c.W + 2 * c.pad <= 128 and
+            (c.KW - 1) * c.dilation <= 8)
+
+
+FULL = [c for c in workloads.ALL if c.name != workloads.TINY.name]
+
+
+@pytest.mark.parametrize("shape", FULL, ids=lambda s: s.name)
 def test_full_size_config_sampled(gpu_lib, shape):
+    check_sampled(gpu_lib, shape, 0)
+
+
+@pytest.mark.parametrize("shape", [c for c in FULL if plane_able(c)], ids=lambda s: s.name)
+def test_full_size_plane_path_sampled(gpu_lib, shape):
+    check_sampled(gpu_lib, shape, gpu_lib.PATH_PLANE)
+
+
+def check_sampled(gpu_lib, shape, path):
     x, w, b = workloads.make_inputs(shape)
     d = torch.device("cuda:0")
     out_dtype = torch.float32 if shape.out_f32 else torch.bfloat16
-    y = gpu_lib.conv2d_fwd(x.to(d), w.to(d), b.to(d), shape.stride, shape.pad, shape.dilation,
-                           out_dtype=out_dtype)
+    y = gpu_lib.conv2d_fwd_path(path, x.to(d), w.to(d), b.to(d), shape.stride, shape.pad,
+                                shape.dilation, out_dtype=out_dtype)
     st, code = gpu_lib.check_device_errors()
     assert st == 0, "device error word %#x" % code
     assert bool(torch.isfinite(y).all())

@@ -119,6 +119,28 @@ def test_window_and_gather_paths_match_oracle(gpu_lib, shape, path):
     check(got, ref, mag, shape.name)
 
 
+# Plane path: the window path's shapes plus ones that reach its other plan
+# choices: tiles that straddle images, two sub-tiles per weight block with a
+# ragged column tile, split K, an output row of 128 padded pixels, and
+# C_out % 8 != 0 (direct stores instead of the TMA-store epilogue).
+PLANE_EXTRA = [
+    S("plane_u2_c128_cout160", N=64, C_in=128, H=10, W=10, C_out=160, seed=40),
+    S("plane_splitk_c512", N=1, C_in=512, H=5, W=6, C_out=64, seed=41),
+    S("plane_cout30", N=3, C_in=64, H=9, W=10, C_out=30, seed=42),
+    S("plane_c192_cout136", N=2, C_in=192, H=8, W=9, C_out=136, seed=43),
+    S("plane_c64_5x3_d2", N=2, C_in=64, H=12, W=13, C_out=256, KH=5, KW=3, pad=2, dilation=2,
+      seed=44),
+]
+PLANE_ABLE = WINDOW_ABLE + PLANE_EXTRA
+
+
+@pytest.mark.parametrize("shape", PLANE_ABLE, ids=lambda s: s.name)
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_plane_path_matches_oracle(gpu_lib, shape, out_dtype):
+    got, ref, mag = run_full(gpu_lib, shape, path=gpu_lib.PATH_PLANE, out_dtype=out_dtype)
+    check(got, ref, mag, shape.name)
+
+
 def test_tiny_config_full_output(gpu_lib):
     """3 -> 4 channels, 8x8, 3x3, fp32 output: every output element."""
     shape = workloads.TINY
