@@ -101,6 +101,50 @@ def shape_numbers(g, c: workloads.ConvShape):
                                   c.dilation), "?"))
 
 
+KERNEL_SOURCES = ("indirect_implicit_gemm_gb300/csrc/igemm.cu",
+                  "indirect_implicit_gemm_gb300/csrc/api.cu",
+                  "indirect_implicit_gemm_gb300/csrc/internal.h",
+                  "indirect_implicit_gemm_gb300/csrc/ptx.cuh")
+
+
+def kernel_source_hash():
+    """sha256 over the sources that define the implicit-GEMM kernel and its plan."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the GEMM kernel on `workload`, from the committed
+    ncu summary under profiles/, or None when no summary covers this workload
+    or the kernel sources changed since it was taken.  The summary carries
+    lines `workload: <name>`, `source_sha256: <hex>` and
+    `dram_bytes_per_launch: <int>`."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    want = kernel_source_hash()
+    for fn in sorted(os.listdir(d)):
+        if not fn.endswith(".md"):
+            continue
+        kv = {}
+        with open(os.path.join(d, fn)) as f:
+            for line in f:
+                if ":" in line and line.split(":", 1)[0].strip() in (
+                        "workload", "source_sha256", "dram_bytes_per_launch"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip().strip("`")
+        if kv.get("workload") == workload and kv.get("source_sha256") == want:
+            try:
+                return int(kv["dram_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
 def roofline_time_s(num, peaks):
     t_tc = num["flops"] / (peaks["bf16_tflops"] * 1e12)
     t_hbm = num["bytes"] / (peaks["hbm_gbs"] * 1e9)
@@ -468,7 +512,7 @@ def main():
             peak = peaks["hbm_gbs"]
             unit = "GB/s"
         roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": profiled_traffic(c.name),
                 "kernel": "igemm_kernel (%s path, tcgen05)" % num["path"],
                 "kernel_us": k_ms * 1e3,
                 "peak_source": "%s (MEASURED_PEAKS.json %s)" % (
