@@ -219,8 +219,9 @@ struct GemmPlan {
     int win_wv = 0, win_rows = 0;  // row-tile geometry (window and narrow window)
     int extra_smem = 0;            // narrow window: staged-row slots
     int nw_slots = 0;
-    int tma_store = 0;             // epilogue through shared memory and TMA stores
+    int tma_store = 0;             // epilogue through a staging tile and TMA stores
     int pl_u = 1, pl_nacc = 0, b_stages = 0;  // plane mode: sub-tiles, accumulators, B slots
+    int pair = 0;                  // window mode on a CTA pair (each CTA holds bn/2 columns of B)
     long long M = 0, K = 0;
     int num_kb = 0, m_tiles = 0, n_tiles = 0;
 };
@@ -256,8 +257,8 @@ void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
 {
     if (y_f32 || c.C_out % 8 != 0 || g.splits != 1 || g.bn < 64 || g.stages < 2) return;
     const int kb_res = g.bres ? (int)((g.K + 63) / 64) : g.num_kb;
-    const int s = igemm_pick_stages(g.bn, g.bres, kb_res, g.a_stage_bytes, g.b_per_stage,
-                                    g.extra_smem + kEpiStageBytes);
+    const int s = igemm_pick_stages(g.pair ? g.bn / 2 : g.bn, g.bres, kb_res, g.a_stage_bytes,
+                                    g.b_per_stage, g.extra_smem + kEpiStageBytes);
     if (s < 2) return;
     g.stages = s;
     g.tma_store = 1;
@@ -402,21 +403,32 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         g.m_tiles = (int)(((long long)c.N * c.H_out + g.win_rows - 1) / g.win_rows);
         g.bn = pick_bn(c.C_out);
         g.n_tiles = (c.C_out + g.bn - 1) / g.bn;
+        // Two CTAs per MMA (256 rows) for 256-wide column tiles: each holds half
+        // of the weight columns, so each SM reads half of B per MMA and a slot of
+        // streamed weights takes half the shared memory.  (Narrower tiles stay on
+        // one CTA: measured, their time is set by the epilogue, which the pair
+        // does not shorten.)
+        g.pair = (g.bn == 256 && g.m_tiles >= 2) ? 1 : 0;
+        auto bnb = [&] { return g.pair ? g.bn / 2 : g.bn; };
         const int all_kb = c.KH * c.KW * (c.C_in / 64);
-        if (g.n_tiles == 1 && igemm_pick_stages(g.bn, 1, all_kb, g.a_stage_bytes, 1) >= 3) {
+        if (g.n_tiles == 1 && igemm_pick_stages(bnb(), 1, all_kb, g.a_stage_bytes, 1) >= 3) {
             g.bres = 1;
             g.b_per_stage = 1;
-            g.stages = igemm_pick_stages(g.bn, 1, all_kb, g.a_stage_bytes, 1);
+            g.stages = igemm_pick_stages(bnb(), 1, all_kb, g.a_stage_bytes, 1);
         } else {
-            // Streamed weights: a slot holds the KW blocks of one (kh, cc); keep
-            // the column tile at 128 so at least two slots fit.
-            if (g.bn > 128) {
+            // Streamed weights: a slot holds the KW blocks of one (kh, cc).  A
+            // 256-wide column tile only on a pair with three slots beside the
+            // epilogue's staging tile; otherwise 128 so that enough slots fit.
+            if (g.bn > 128 && !(g.pair && igemm_pick_stages(g.bn / 2, 0, 0, g.a_stage_bytes, c.KW,
+                                                            kEpiStageBytes) >= 3)) {
                 g.bn = 128;
                 g.n_tiles = (c.C_out + 127) / 128;
+                g.pair = 0;
             }
             g.b_per_stage = c.KW;
-            g.stages = igemm_pick_stages(g.bn, 0, 0, g.a_stage_bytes, c.KW);
+            g.stages = igemm_pick_stages(bnb(), 0, 0, g.a_stage_bytes, c.KW);
         }
+        if (g.pair) g.amode = kAWindowPair;
         const long long im2col = c.M * c.K * 2;
         const long long partial = c.M * c.C_out * 4;
         g.splits = choose_splits((long long)g.m_tiles * g.n_tiles, g.num_kb, partial, im2col / 2);
@@ -542,22 +554,26 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     if (g.K % 8 != 0) return CONVGB_ERR_UNSUPPORTED;  // TMA row pitch must be 16-byte aligned
     memset(out, 0, sizeof *out);
     out->plan = g;
-    if (!encode_kmajor(&out->tb, a.w, a.C_out, g.K, g.bn)) return CONVGB_ERR_CUDA;
+    if (!encode_kmajor(&out->tb, a.w, a.C_out, g.K, g.pair ? g.bn / 2 : g.bn)) return CONVGB_ERR_CUDA;
     if (g.amode == kADense && !encode_kmajor(&out->ta, a.a_dense, g.M, g.K, 128))
         return CONVGB_ERR_CUDA;
     // TMA gather: x as [N*H*W][C_in], one-row boxes of 64 channels.
     if (g.amode == kATmaGather && !encode_kmajor(&out->ta, a.x, a.x_rows, a.C_in, 1))
         return CONVGB_ERR_CUDA;
     const bool plane = g.amode == kAPlane || g.amode == kAPlane3 || g.amode == kAPlane3U2;
-    if (g.amode == kAWindow || plane) {
+    const bool window = g.amode == kAWindow || g.amode == kAWindowPair;
+    if (window || plane) {
         const ConvShape& c = *a.shape;
         if (!encode_window(&out->ta, a.x, c.N, c.H, c.W, c.C_in, g.win_wv)) return CONVGB_ERR_CUDA;
     }
     // TMA-store epilogue: y as [M][C_out], boxes of 64 channels x (one output row
     // for row tiles, 128 rows otherwise).
     if (g.tma_store) {
-        const int box_rows =
-            (g.amode == kAWindow || g.amode == kANarrowWin || plane) ? a.shape->W_out : 128;
+        // row tiles: the tile's win_rows output rows, consecutive in y; plane
+        // tiles: one output row per box (their rows are not consecutive)
+        const int box_rows = (window || g.amode == kANarrowWin) ? g.win_rows * a.shape->W_out
+                             : plane                             ? a.shape->W_out
+                                                                 : 128;
         if (!encode_kmajor(&out->ty, a.y, g.M, a.C_out, box_rows)) return CONVGB_ERR_CUDA;
     }
     unsigned* err = device_error_word();
@@ -581,7 +597,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     p.oob_row = (int)a.x_rows;
     p.num_kb = g.num_kb;
     p.kb_total = (int)((g.K + 63) / 64);
-    p.m_tiles = g.m_tiles;
+    p.m_tiles = g.pair ? (g.m_tiles + 1) / 2 : g.m_tiles;  // work units: pairs of tiles
     p.n_tiles = g.n_tiles;
     p.splits = g.splits;
     p.split_div = FastDiv((uint32_t)g.splits);
@@ -613,7 +629,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.nw_slot_bytes = nr.slot;
         p.nw_slots = g.nw_slots;
     }
-    if (g.amode == kAWindow) {
+    if (window) {
         const ConvShape& c = *a.shape;
         p.win_wv = g.win_wv;
         p.win_rows = g.win_rows;

@@ -88,13 +88,18 @@ struct WaitCtx {
 // Waits for the phase of `bar` with the given parity.  Returns false (and the
 // caller must unwind) when the wait exceeds the time limit or another role
 // of this CTA has already given up.
+// `cluster`: the phase is completed by arrivals from the peer CTA of a pair,
+// so the wait acquires at cluster scope.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const WaitCtx& w,
-                                         unsigned role)
+                                         unsigned role, bool cluster = false)
 {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto test = [&] {
+        return cluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (test()) return true;
     const unsigned long long t0 = ptx::globaltimer();
     for (uint32_t spins = 1;; ++spins) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (test()) return true;
         if (*w.abort) return false;
         if ((spins & 31u) == 0 && ptx::globaltimer() - t0 > w.timeout_ns) {
             *w.abort = 1u;
@@ -197,15 +202,17 @@ struct Unit {
 // between two tiles' MMA groups, so it uses the host-prepared multiply-shift
 // dividers (a run-time division, and above all a 64-bit one, costs hundreds of
 // cycles there).
-template <int BN>
-__device__ __forceinline__ Unit unit_of(const IgemmParams& p, int tile)
+// Pair mode: unit `tile` is a pair of consecutive output tiles, the CTA of
+// rank r taking tile 2*m + r.
+template <int BN, bool PAIRED = false>
+__device__ __forceinline__ Unit unit_of(const IgemmParams& p, int tile, uint32_t rank = 0)
 {
     uint32_t mn = static_cast<uint32_t>(tile), ks = 0;
     if (p.splits > 1) p.split_div.divmod(static_cast<uint32_t>(tile), mn, ks);
     uint32_t mt = mn, nt = 0;
     if (p.n_tiles > 1) p.ntile_div.divmod(mn, mt, nt);
     Unit u;
-    u.m0 = static_cast<int>(mt) * p.m_step;
+    u.m0 = static_cast<int>(PAIRED ? 2u * mt + rank : mt) * p.m_step;
     u.n0 = static_cast<int>(nt) * BN;
     u.kb0 = 0;
     u.kb1 = p.num_kb;
@@ -237,6 +244,26 @@ __device__ __forceinline__ void reduce_chunk(const IgemmParams& p, int m, int co
     }
 }
 
+// One MMA, and a commit to the barrier at `bar` in every CTA that waits on it:
+// both CTAs of a pair (multicast), or this CTA.
+template <bool PAIRED>
+__device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t acc)
+{
+    if (PAIRED)
+        ptx::mma_bf16_pair(d, a, b, idesc, acc);
+    else
+        ptx::mma_bf16(d, a, b, idesc, acc);
+}
+template <bool PAIRED>
+__device__ __forceinline__ void mma_commit_to(uint64_t* bar, bool both = true)
+{
+    if (PAIRED)
+        ptx::mma_commit_pair(bar, both ? 0x3 : 0x1);
+    else
+        ptx::mma_commit(bar);
+}
+
 template <int BN, int AMODE>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -249,7 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool NARROWWIN = AMODE == kANarrowWin;
     constexpr bool GATHER =
         AMODE == kAGather || AMODE == kANarrow || AMODE == kATmaGather || NARROWWIN;
-    constexpr bool WINDOW = AMODE == kAWindow;
+    constexpr bool PAIR = AMODE == kAWindowPair;  // window mode on a CTA pair
+    constexpr bool WINDOW = AMODE == kAWindow || PAIR;
+    // B block bytes in this CTA's shared memory (a pair splits B's columns)
+    constexpr uint32_t BB = PAIR ? C::kBBytes / 2 : C::kBBytes;
     constexpr bool PLANE = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     constexpr bool ROWTILES = WINDOW || NARROWWIN;  // tiles of whole output rows
     const uint32_t S = static_cast<uint32_t>(p.stages);
@@ -273,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = ptx::smem_addr(smem_raw) + kHeaderBytes;
     uint8_t* data = smem_raw + kHeaderBytes + ((1024u - (base & 1023u)) & 1023u);
     uint8_t* sB = data;
-    const uint32_t SB = PLANE ? static_cast<uint32_t>(p.b_stages) : 0u;  // plane: B ring slots
+    const uint32_t SB = PLANE ? static_cast<uint32_t>(p.b_stages) : 1u;  // plane: B ring slots
     const uint32_t b_blocks = p.bres ? static_cast<uint32_t>(p.kb_total)
                               : PLANE ? SB
                                       : S * static_cast<uint32_t>(p.b_per_stage);
@@ -281,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t NACC = PLANE ? static_cast<uint32_t>(p.pl_nacc) : static_cast<uint32_t>(C::kAcc);
     const uint32_t ACCW = PLANE ? static_cast<uint32_t>(p.pl_u * BN) : static_cast<uint32_t>(BN);
     constexpr uint32_t kTmemAlloc = PLANE ? 512u : static_cast<uint32_t>(C::kTmemCols);
-    uint8_t* sA = data + b_blocks * C::kBBytes;
+    uint8_t* sA = data + b_blocks * BB;
     uint8_t* sStg = sA + S * AST;  // narrow window: nw_slots slots of staged input rows
     const uint32_t NS = NARROWWIN ? static_cast<uint32_t>(p.nw_slots) : 1u;
     // TMA-store epilogue: a 128 x 64 bf16 staging tile (128-byte swizzle) and the
@@ -293,6 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Pair mode: both CTAs walk the same sequence of pair units.
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const int t_first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int t_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; ++s) {
@@ -305,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t s = 0; s < SB; ++s) ptx::mbar_init(&empty_b[s], 1);
         for (uint32_t i = 0; i < NACC; ++i) {
             ptx::mbar_init(&tfull[i], 1);
-            ptx::mbar_init(&tempty[i], kEpiThreads);
+            ptx::mbar_init(&tempty[i], PAIR ? 2 * kEpiThreads : kEpiThreads);
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(bres_full, 1);
@@ -323,8 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == kMmaWarp) {
-        ptx::tmem_alloc(tmem_slot, kTmemAlloc);
-        ptx::tmem_relinquish();
+        if (PAIR) {
+            ptx::tmem_alloc_pair(tmem_slot, kTmemAlloc);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(tmem_slot, kTmemAlloc);
+            ptx::tmem_relinquish();
+        }
     }
     if (NARROWWIN) {
         // Staged rows keep their zero borders for the whole kernel: the bulk
@@ -335,7 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    // a pair's barriers must be initialised before either CTA signals the other's
+    if (PAIR)
+        ptx::cluster_sync();
+    else
+        __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -348,13 +391,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // virtual pixel (wrow, wcol) of the tile's output rows; spill columns
         // (wcol >= W_out) and rows past the tile's output rows are discarded.
         const int r = warp * 32 + lane;
+        // the accumulator is handed back to the MMA thread, which in a pair sits in CTA 0
+        auto release_acc = [&](uint32_t acc) {
+            ptx::tc_fence_before();
+            if (PAIR && rank != 0)
+                ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_addr(&tempty[acc]), 0u));
+            else
+                ptx::mbar_arrive(&tempty[acc]);
+        };
         const int wrow = (ROWTILES || PLANE) ? r / p.win_wv : 0;
         const int wcol = (ROWTILES || PLANE) ? r - wrow * p.win_wv : 0;
         uint32_t lt = 0;
         int bias_n0 = -1;
         Ring ar;  // accumulator index and the parity of its current use
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt, ar.next(NACC)) {
-            const Unit u = unit_of<BN>(p, tile);
+        for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt, ar.next(NACC)) {
+            const Unit u = unit_of<BN, PAIR>(p, tile, rank);
             const uint32_t acc = ar.stage;
             // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds,
             // and with the TMA store all four warps do (they share named barriers).
@@ -407,27 +458,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
                         ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
                         ptx::tmem_ld_wait();
-                        if (last_sub && c64 + 1 == BN / 64) {
-                            ptx::tc_fence_before();
-                            ptx::mbar_arrive(&tempty[acc]);
-                        }
+                        if (last_sub && c64 + 1 == BN / 64) release_acc(acc);
                         // The staging tile is free once the previous store has read it.
                         if (r == 0) ptx::bulk_wait_read_all();
                         ptx::named_barrier_sync(1, kEpiThreads);
-                        const float* bs = sBias + c64 * 64;
+                        const float4* bs = reinterpret_cast<const float4*>(sBias + c64 * 64);
+                        // Row tiles keep only real output pixels, packed: the tile's
+                        // output rows are consecutive rows of y, so one box stores
+                        // the chunk.  Other tiles keep row r at r.
+                        const int srow = ROWTILES ? wrow * p.win_wout + wcol : r;
+                        const bool keep = !ROWTILES || (wcol < p.win_wout && wrow < p.win_rows);
+                        if (keep) {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const uint32_t* src = q < 4 ? ra + 8 * q : rb + 8 * (q - 4);
-                            uint4 v;
-                            v.x = pack_bf16x2(__uint_as_float(src[0]) + bs[8 * q + 0],
-                                              __uint_as_float(src[1]) + bs[8 * q + 1]);
-                            v.y = pack_bf16x2(__uint_as_float(src[2]) + bs[8 * q + 2],
-                                              __uint_as_float(src[3]) + bs[8 * q + 3]);
-                            v.z = pack_bf16x2(__uint_as_float(src[4]) + bs[8 * q + 4],
-                                              __uint_as_float(src[5]) + bs[8 * q + 5]);
-                            v.w = pack_bf16x2(__uint_as_float(src[6]) + bs[8 * q + 6],
-                                              __uint_as_float(src[7]) + bs[8 * q + 7]);
-                            *reinterpret_cast<uint4*>(sEpi + r * 128 + ((q ^ (r & 7)) << 4)) = v;
+                            for (int q = 0; q < 8; ++q) {
+                                const uint32_t* src = q < 4 ? ra + 8 * q : rb + 8 * (q - 4);
+                                const float4 b0 = bs[2 * q], b1 = bs[2 * q + 1];
+                                uint4 v;
+                                v.x = pack_bf16x2(__uint_as_float(src[0]) + b0.x,
+                                                  __uint_as_float(src[1]) + b0.y);
+                                v.y = pack_bf16x2(__uint_as_float(src[2]) + b0.z,
+                                                  __uint_as_float(src[3]) + b0.w);
+                                v.z = pack_bf16x2(__uint_as_float(src[4]) + b1.x,
+                                                  __uint_as_float(src[5]) + b1.y);
+                                v.w = pack_bf16x2(__uint_as_float(src[6]) + b1.z,
+                                                  __uint_as_float(src[7]) + b1.w);
+                                *reinterpret_cast<uint4*>(sEpi + srow * 128 +
+                                                          ((q ^ (srow & 7)) << 4)) = v;
+                            }
                         }
                         ptx::fence_proxy_async_smem();
                         ptx::named_barrier_sync(1, kEpiThreads);
@@ -448,10 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             p.win_wout);
                                 }
                             } else if (ROWTILES) {
-                                const int rows = min(p.win_rows, p.win_groups - u.m0);
-                                for (int jj = 0; jj < rows; ++jj)
-                                    ptx::tma_store_2d(&tmap_y, sEpi + jj * p.win_wv * 128, c0,
-                                                      (u.m0 + jj) * p.win_wout);
+                                // win_rows*W_out rows from the tile's first output pixel;
+                                // rows past the end of y are not written
+                                if (u.m0 < p.win_groups)
+                                    ptx::tma_store_2d(&tmap_y, sEpi, c0, u.m0 * p.win_wout);
                             } else {
                                 ptx::tma_store_2d(&tmap_y, sEpi, c0, u.m0);
                             }
@@ -469,10 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_32x32b_x32(taddr + ch * 32, ra);
                     if (ch + 1 < BN / 32) ptx::tmem_ld_32x32b_x32(taddr + (ch + 1) * 32, rb);
                     ptx::tmem_ld_wait();
-                    if (last_sub && ch + 2 >= BN / 32) {
-                        ptx::tc_fence_before();
-                        ptx::mbar_arrive(&tempty[acc]);
-                    }
+                    if (last_sub && ch + 2 >= BN / 32) release_acc(acc);
                     const int co0 = u.n0 + ch * 32;
                     if (live && co0 < p.C_out) {
                         if (p.splits > 1)
@@ -506,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Ring ring;
                 uint32_t issued = 0;
                 bool ok = true;
-                for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                    const Unit u = unit_of<BN>(p, tile);
+                for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
+                    const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
                         if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleGather)) {
                             ok = false;
@@ -544,12 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lines = static_cast<int>((row_elems * 2 + 127) / 128);
             volatile uint32_t* aborted = abort_flag;
             uint32_t lt = 0;
-            for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
+            for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt) {
                 for (uint32_t spin = 0; spin < (1u << 22) && lt > *sTilesDone + 3u && !*aborted;
                      ++spin) {
                 }
                 if (*aborted) break;
-                const Unit v = unit_of<BN>(p, tile);
+                const Unit v = unit_of<BN, PAIR>(p, tile, rank);
                 if (v.n0 != 0 || v.kb0 != 0) continue;  // one prefetch per row block
                 for (int j = 0; j < p.pl_srows; ++j) {
                     uint32_t n, hp;
@@ -569,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long row_elems = static_cast<long long>(p.x_W) * p.C_in;
             const int lines = static_cast<int>((row_elems * 2 + 127) / 128);
             auto prefetch_tile = [&](int t) {
-                const Unit v = unit_of<BN>(p, t);
+                const Unit v = unit_of<BN, PAIR>(p, t, rank);
                 const int rows = min(p.win_rows, p.win_groups - v.m0);
                 for (int jj = 0; jj < rows; ++jj) {
                     uint32_t n, ho;
@@ -590,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // then prefetch anyway.
             volatile uint32_t* aborted = abort_flag;
             uint32_t lt = 0;
-            for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
+            for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt) {
                 for (uint32_t spin = 0; spin < (1u << 22) && lt > *sTilesDone + 3u && !*aborted;
                      ++spin) {
                 }
@@ -608,8 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             Ring ring;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Unit u = unit_of<BN>(p, tile);
+            for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                 int ib4[4];  // first indirection entry of the row's pixel, or -1
                 int nb4[4];  // first row of the pixel's image
 #pragma unroll
@@ -668,8 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring ring;
             uint32_t slot = 0, slot_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Unit u = unit_of<BN>(p, tile);
+            for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                 const int rows = min(p.win_rows, p.win_groups - u.m0);
                 const bool row_live = j < rows;
                 int ho = 0;
@@ -738,8 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rg = gt >> 3;
             Ring ring;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Unit u = unit_of<BN>(p, tile);
+            for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                 int ib[kRowsPerGatherThread];        // pixel's first ibuf entry, or -1
                 long long xb[kRowsPerGatherThread];  // image base (elements)
 #pragma unroll
@@ -853,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t a_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
             const uint64_t b_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sB));
             const uint32_t a_slot_step = AST >> 4;
-            constexpr uint32_t b_blk_step = C::kBBytes >> 4;
+            constexpr uint32_t b_blk_step = BB >> 4;
             const uint32_t sub_step = static_cast<uint32_t>(p.win_rows * p.win_wv * 8);
             const uint32_t row_step = static_cast<uint32_t>(p.win_wv * p.win_d * 8);  // kh + 1
             const uint32_t col_step = static_cast<uint32_t>(p.win_d * 8);             // kw + 1
@@ -868,9 +922,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = !p.bres || wait_bar(bres_full, 0u, wc, kRoleMma);
             const int taps = p.x_KH * p.win_kw;
             Ring ar;
-            for (int tile = blockIdx.x; ok && tile < total_tiles;
-                 tile += gridDim.x, ++lt, ar.next(NACC)) {
-                const Unit u = unit_of<BN>(p, tile);
+            for (int tile = t_first; ok && tile < total_tiles;
+                 tile += t_step, ++lt, ar.next(NACC)) {
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                 const uint32_t acc = ar.stage;
                 if (!wait_bar(&tempty[acc], ar.phase ^ 1u, wc, kRoleMma)) break;
                 ptx::tc_fence_after();
@@ -953,22 +1007,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Make sure no MMA is still reading shared memory or writing TMEM.
             ptx::mma_commit(drain);
             drain_wait(drain, 0, 1000000000ull);
-        } else if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+        } else if (lane == 0 && rank == 0) {
+            // (in a pair only CTA 0 issues: each MMA covers both CTAs' 128 rows)
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
             const uint64_t a_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
             const uint64_t b_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sB));
             const uint32_t a_slot_step = AST >> 4;
-            constexpr uint32_t b_blk_step = C::kBBytes >> 4;
+            constexpr uint32_t b_blk_step = BB >> 4;
             const uint32_t col_step = static_cast<uint32_t>(p.win_d * 8);  // window: kw + 1
             Ring ring;
             uint32_t lt = 0;
             bool ok = !p.bres || wait_bar(bres_full, 0u, wc, kRoleMma);
             Ring ar;
-            for (int tile = blockIdx.x; ok && tile < total_tiles;
-                 tile += gridDim.x, ++lt, ar.next(C::kAcc)) {
-                const Unit u = unit_of<BN>(p, tile);
+            for (int tile = t_first; ok && tile < total_tiles;
+                 tile += t_step, ++lt, ar.next(C::kAcc)) {
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                 const uint32_t acc = ar.stage;
-                if (!wait_bar(&tempty[acc], ar.phase ^ 1u, wc, kRoleMma)) break;
+                if (!wait_bar(&tempty[acc], ar.phase ^ 1u, wc, kRoleMma, PAIR)) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 // window mode: (kh, cc) of the K block, walked instead of divided
@@ -1010,14 +1065,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int kw = 0; kw < 3; ++kw)
 #pragma unroll
                                 for (int kk = 0; kk < BK / 16; ++kk)
-                                    ptx::mma_bf16(d_tmem, ad + kw * col_step + 2 * kk,
+                                    mma_issue<PAIR>(d_tmem, ad + kw * col_step + 2 * kk,
                                                   bd0 + kw * bstep + 2 * kk, idesc,
                                                   (kw != 0 || kk != 0) ? 1u : first);
                         } else {
                             for (int kw = 0; kw < p.win_kw; ++kw)
 #pragma unroll
                                 for (int kk = 0; kk < BK / 16; ++kk)
-                                    ptx::mma_bf16(d_tmem, ad + kw * col_step + 2 * kk,
+                                    mma_issue<PAIR>(d_tmem, ad + kw * col_step + 2 * kk,
                                                   bd0 + kw * bstep + 2 * kk, idesc,
                                                   (kw != 0 || kk != 0) ? 1u : first);
                         }
@@ -1034,26 +1089,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
                             if (kk < ksteps)
-                                ptx::mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
+                                mma_issue<PAIR>(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
                                               (kb != u.kb0 || kk != 0) ? 1u : 0u);
                     }
-                    ptx::mma_commit(&empty[ring.stage]);
+                    mma_commit_to<PAIR>(&empty[ring.stage]);
                 }
-                if (ok) ptx::mma_commit(&tfull[acc]);
+                if (ok) mma_commit_to<PAIR>(&tfull[acc]);
             }
             // Make sure no MMA is still reading shared memory or writing TMEM.
-            ptx::mma_commit(drain);
+            mma_commit_to<PAIR>(drain, false);
             drain_wait(drain, 0, 1000000000ull);
         }
     } else if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             if (p.bres) {
-                // Weights resident: every K block of the one column tile, once.
-                ptx::mbar_arrive_expect_tx(bres_full,
-                                           static_cast<uint32_t>(p.kb_total) * C::kBBytes);
-                for (int kb = 0; kb < p.kb_total; ++kb)
-                    ptx::tma_load_2d(sB + kb * C::kBBytes, &tmap_b, bres_full, kb * BK, 0);
+                // Weights resident: every K block of the one column tile, once (in
+                // a pair each CTA holds half of the columns; CTA 0's barrier counts
+                // both halves).
+                if (rank == 0)
+                    ptx::mbar_arrive_expect_tx(bres_full, static_cast<uint32_t>(p.kb_total) * BB *
+                                                              (PAIR ? 2u : 1u));
+                const uint32_t bres_bar = PAIR ? ptx::mapa(ptx::smem_addr(bres_full), 0u) : 0u;
+                for (int kb = 0; kb < p.kb_total; ++kb) {
+                    if (PAIR)
+                        ptx::tma_load_2d_pair(sB + kb * BB, &tmap_b, bres_bar, kb * BK,
+                                              static_cast<int>(rank) * (BN / 2));
+                    else
+                        ptx::tma_load_2d(sB + kb * BB, &tmap_b, bres_full, kb * BK, 0);
+                }
                 // (the A loads below are issued at once; the weights' arrival is
                 // awaited by the MMA thread, and here only before exiting)
             }
@@ -1063,8 +1127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // are skipped (the consumer writes zeros for them).
                 const uint32_t row_bytes = static_cast<uint32_t>(p.nw_W * p.nw_cin * 2);
                 uint32_t slot = 0, slot_phase = 0, issued = 0;
-                for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++issued) {
-                    const Unit u = unit_of<BN>(p, tile);
+                for (int tile = t_first; tile < total_tiles; tile += t_step, ++issued) {
+                    const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                     if (!wait_bar(&stg_empty[slot], slot_phase ^ 1u, wc, kRoleTma)) break;
                     const int rows = min(p.win_rows, p.win_groups - u.m0);
                     uint32_t copies = 0;
@@ -1106,16 +1170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     Ring rb;
                     uint32_t issued = 0;
                     bool ok = true;
-                    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                        const Unit u = unit_of<BN>(p, tile);
+                    for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
+                        const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                         for (int kb = u.kb0; ok && kb < u.kb1; ++kb)
                             for (int t = 0; t < taps; ++t, ++issued, rb.next(SB)) {
                                 if (!wait_bar(&empty_b[rb.stage], rb.phase ^ 1u, wc, kRoleTma)) {
                                     ok = false;
                                     break;
                                 }
-                                ptx::mbar_arrive_expect_tx(&full_b[rb.stage], C::kBBytes);
-                                ptx::tma_load_2d(sB + rb.stage * C::kBBytes, &tmap_b,
+                                ptx::mbar_arrive_expect_tx(&full_b[rb.stage], BB);
+                                ptx::tma_load_2d(sB + rb.stage * BB, &tmap_b,
                                                  &full_b[rb.stage], (t * p.win_cc + kb) * BK, u.n0);
                             }
                     }
@@ -1132,47 +1196,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Ring ring;
                 uint32_t issued = 0;
                 bool ok = true;
-                for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                    const Unit u = unit_of<BN>(p, tile);
-                    const int rows = min(p.win_rows, p.win_groups - u.m0);
+                // A pair: each CTA stages its own tile's rows and its half of the
+                // weight columns; all of it completes on CTA 0's barrier, which
+                // CTA 0 arms with both CTAs' byte counts.  The peer cannot wait on
+                // that barrier, so CTA 0's drain below covers the peer's copies too
+                // (neither CTA exits before the final cluster barrier).
+                for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
+                    const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                    const int rows = max(0, min(p.win_rows, p.win_groups - u.m0));
+                    int rows_peer = 0;
+                    if (PAIR) {
+                        const Unit v = unit_of<BN, PAIR>(p, tile, 1u);
+                        rows_peer = max(0, min(p.win_rows, p.win_groups - v.m0));
+                    }
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
                         if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleTma)) {
                             ok = false;
                             break;
                         }
                         const int kh = kb / p.win_cc, cc = kb - kh * p.win_cc;
-                        const uint32_t tx =
-                            static_cast<uint32_t>(rows) * row_bytes +
-                            (p.bres ? 0u : static_cast<uint32_t>(p.win_kw) * C::kBBytes);
-                        ptx::mbar_arrive_expect_tx(&full_b[ring.stage], tx);
+                        const uint32_t full_cl =
+                            PAIR ? ptx::mapa(ptx::smem_addr(&full_b[ring.stage]), 0u) : 0u;
+                        if (rank == 0) {
+                            const uint32_t tx =
+                                static_cast<uint32_t>(rows + rows_peer) * row_bytes +
+                                (p.bres ? 0u
+                                        : static_cast<uint32_t>(p.win_kw) * BB * (PAIR ? 2u : 1u));
+                            ptx::mbar_arrive_expect_tx(&full_b[ring.stage], tx);
+                        }
                         uint8_t* stage_a = sA + ring.stage * AST;
                         for (int j = 0; j < rows; ++j) {
                             uint32_t n, ho;
                             p.ho_div.divmod(static_cast<uint32_t>(u.m0 + j), n, ho);
-                            ptx::tma_load_4d(stage_a + j * row_bytes, &tmap_a, &full_b[ring.stage],
-                                             cc * BK, -p.win_pad,
-                                             static_cast<int>(ho) - p.win_pad + kh * p.win_d,
-                                             static_cast<int>(n));
+                            const int h = static_cast<int>(ho) - p.win_pad + kh * p.win_d;
+                            if (PAIR)
+                                ptx::tma_load_4d_pair(stage_a + j * row_bytes, &tmap_a, full_cl,
+                                                      cc * BK, -p.win_pad, h, static_cast<int>(n));
+                            else
+                                ptx::tma_load_4d(stage_a + j * row_bytes, &tmap_a,
+                                                 &full_b[ring.stage], cc * BK, -p.win_pad, h,
+                                                 static_cast<int>(n));
                         }
                         if (!p.bres)
-                            for (int kw = 0; kw < p.win_kw; ++kw)
-                                ptx::tma_load_2d(
-                                    sB + (ring.stage * p.b_per_stage + kw) * C::kBBytes, &tmap_b,
-                                    &full_b[ring.stage], ((kh * p.win_kw + kw) * p.win_cc + cc) * BK,
-                                    u.n0);
+                            for (int kw = 0; kw < p.win_kw; ++kw) {
+                                uint8_t* dst = sB + (ring.stage * p.b_per_stage + kw) * BB;
+                                const int col = ((kh * p.win_kw + kw) * p.win_cc + cc) * BK;
+                                if (PAIR)
+                                    ptx::tma_load_2d_pair(dst, &tmap_b, full_cl, col,
+                                                          u.n0 + static_cast<int>(rank) * (BN / 2));
+                                else
+                                    ptx::tma_load_2d(dst, &tmap_b, &full_b[ring.stage], col, u.n0);
+                            }
                     }
                 }
                 const uint32_t first = issued > S ? issued - S : 0;
-                for (uint32_t i = first; i < issued; ++i)
-                    drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
+                if (rank == 0)
+                    for (uint32_t i = first; i < issued; ++i)
+                        drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
             } else if (!p.bres || !GATHER) {
-                const uint32_t kTx = (p.bres ? 0u : static_cast<uint32_t>(C::kBBytes)) +
+                const uint32_t kTx = (p.bres ? 0u : static_cast<uint32_t>(BB)) +
                                      (GATHER ? 0u : static_cast<uint32_t>(kABytes));
                 Ring ring;
                 uint32_t issued = 0;
                 bool ok = true;
-                for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                    const Unit u = unit_of<BN>(p, tile);
+                for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
+                    const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
                         if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleTma)) {
                             ok = false;
@@ -1183,7 +1271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::tma_load_2d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, u.m0);
                         if (!p.bres)
-                            ptx::tma_load_2d(sB + ring.stage * C::kBBytes, &tmap_b,
+                            ptx::tma_load_2d(sB + ring.stage * BB, &tmap_b,
                                              &full_b[ring.stage], kb * BK, u.n0);
                     }
                 }
@@ -1195,14 +1283,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // The resident weights must have landed before the CTA exits.
-    if (warp == kTmaWarp && lane == 0 && p.bres) drain_wait(bres_full, 0u, 1000000000ull);
+    // The resident weights must have landed before the CTA exits (a pair's
+    // land on CTA 0's barrier, for both CTAs).
+    if (warp == kTmaWarp && lane == 0 && p.bres && rank == 0)
+        drain_wait(bres_full, 0u, 1000000000ull);
     ptx::tc_fence_before();
-    __syncthreads();
+    // a pair's CTA 0 reads the peer's shared memory and writes its TMEM: neither
+    // CTA leaves before both are done
+    if (PAIR)
+        ptx::cluster_sync();
+    else
+        __syncthreads();
     ptx::tc_fence_after();
     if (warp == kMmaWarp) {
         __syncwarp();
-        ptx::tmem_dealloc(tmem_base, kTmemAlloc);
+        if (PAIR)
+            ptx::tmem_dealloc_pair(tmem_base, kTmemAlloc);
+        else
+            ptx::tmem_dealloc(tmem_base, kTmemAlloc);
     }
 }
 
@@ -1265,8 +1363,8 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         kPlane
             ? plane_smem_bytes(BN, p.stages, p.a_stage_bytes, p.bres ? p.kb_total : p.b_stages,
                                extra)
-            : igemm_smem_bytes(BN, p.stages, p.bres, p.kb_total, p.a_stage_bytes, p.b_per_stage,
-                               extra);
+            : igemm_smem_bytes(AMODE == kAWindowPair ? BN / 2 : BN, p.stages, p.bres, p.kb_total,
+                               p.a_stage_bytes, p.b_per_stage, extra);
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
     if (kPlane &&
         ((!p.bres && (p.b_stages < 2 || p.b_stages > kMaxStages)) || p.pl_u < 1 || p.pl_u > 2 ||
@@ -1276,7 +1374,39 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
     if ((AMODE == kAPlane3 || AMODE == kAPlane3U2) &&
         (p.x_KH != 3 || p.win_kw != 3 || p.pl_u != (AMODE == kAPlane3U2 ? 2 : 1)))
         return cudaErrorInvalidValue;
-    const int tiles = p.m_tiles * p.n_tiles * p.splits;
+    const int tiles = p.m_tiles * p.n_tiles * p.splits;  // pair mode: pair units
+    if (AMODE == kAWindowPair) {
+        if (BN < 64) return cudaErrorInvalidValue;
+        // Clusters of two CTAs, as many as can be resident at once (two SMs each).
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        static int cached_dev = -1, cached_smem = -1, cached_clusters = 0;
+        if (cached_dev != dev || cached_smem != smem) {
+            int nc = 0;
+            cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2));
+            if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess || nc < 1) {
+                (void)cudaGetLastError();
+                nc = num_sms() / 2;
+            }
+            cached_dev = dev;
+            cached_smem = smem;
+            cached_clusters = nc;
+        }
+        const int clusters = tiles < cached_clusters ? tiles : cached_clusters;
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     const int grid = tiles < num_sms() ? tiles : num_sms();
     kern<<<grid, kThreads, smem, st>>>(ta, tb, ty, p);
     return cudaGetLastError();
@@ -1332,6 +1462,7 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kANarrow: return launch_mode<kANarrow>(bn, ta, tb, ty, p, st);
     case kATmaGather: return launch_mode<kATmaGather>(bn, ta, tb, ty, p, st);
     case kAWindow: return launch_mode<kAWindow>(bn, ta, tb, ty, p, st);
+    case kAWindowPair: return launch_mode<kAWindowPair>(bn, ta, tb, ty, p, st);
     case kANarrowWin: return launch_mode<kANarrowWin>(bn, ta, tb, ty, p, st);
     case kAPlane: return launch_mode<kAPlane>(bn, ta, tb, ty, p, st);
     case kAPlane3: return launch_mode<kAPlane3>(bn, ta, tb, ty, p, st);

@@ -120,6 +120,9 @@ enum AMode : int {
     kAPlane3 = 7,     // plane mode for 3x3 kernels, one sub-tile: the MMA issue sequence
                       // of a staged block is unrolled at compile time
     kAPlane3U2 = 8,   // plane mode for 3x3 kernels, two sub-tiles per weight block
+    kAWindowPair = 9, // window mode on a cluster of two CTAs: one tcgen05.mma.cta_group::2
+                      // covers both CTAs' output tiles (256 rows); each CTA holds half of
+                      // the weight columns
 };
 // Dynamic shared memory of one implicit-GEMM CTA, and the deepest ring that fits
 // (0 when none does).
