@@ -15,8 +15,8 @@
 // CTA layout (320 threads, one persistent CTA per SM):
 //   warps 0-3  epilogue: TMEM -> registers -> +bias -> bf16/fp32 -> global
 //   warps 4-7  A gather: cp.async 16-byte chunks through the indirection buffer
-//   warp  8    TMEM allocation and the MMA-issuing thread
-//   warp  9    TMA producer for B (and for A in the dense variant)
+//   warp  8    TMA producer for B (and for A in the dense and window variants)
+//   warp  9    TMEM allocation and the MMA-issuing thread
 // Stages cycle through full/empty mbarrier pairs; every wait is bounded in
 // time and a timeout makes the whole CTA drain and return with an error code.
 #include <cuda_bf16.h>
@@ -31,9 +31,12 @@ constexpr int BM = 128;           // GEMM rows per tile (TMEM lanes)
 constexpr int BK = 64;            // K elements per stage: one 128-byte swizzle row
 constexpr int kEpiWarps = 4;
 constexpr int kGatherWarps = 4;
-constexpr int kMmaWarp = kEpiWarps + kGatherWarps;  // 8
-constexpr int kTmaWarp = kMmaWarp + 1;              // 9
-constexpr int kThreads = (kTmaWarp + 1) * 32;       // 320
+// The MMA thread sits on warp 9 (scheduler 1), away from the window path's
+// L2-prefetch warp 4, which shares scheduler 0 with warp 8 (measured: 3% on
+// the 64->128 3x3 layer).
+constexpr int kTmaWarp = kEpiWarps + kGatherWarps;  // 8
+constexpr int kMmaWarp = kTmaWarp + 1;              // 9
+constexpr int kThreads = (kMmaWarp + 1) * 32;       // 320
 constexpr int kGatherThreads = kGatherWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kRowsPerGatherThread = BM * (BK / 8) / kGatherThreads;  // 8
@@ -160,7 +163,15 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, int m, int co0
     const long long row = static_cast<long long>(m) * p.C_out + co0;
     if (p.y_f32) {
         float* out = static_cast<float*>(p.y) + row;
-        if (ncols == 32 && (p.C_out & 3) == 0) {
+        if (ncols == 32 && (p.C_out & 7) == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                ptx::st_global_v8(out + 8 * q, __float_as_uint(v[8 * q]),
+                                  __float_as_uint(v[8 * q + 1]), __float_as_uint(v[8 * q + 2]),
+                                  __float_as_uint(v[8 * q + 3]), __float_as_uint(v[8 * q + 4]),
+                                  __float_as_uint(v[8 * q + 5]), __float_as_uint(v[8 * q + 6]),
+                                  __float_as_uint(v[8 * q + 7]));
+        } else if (ncols == 32 && (p.C_out & 3) == 0) {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 reinterpret_cast<float4*>(out)[q] =
@@ -172,7 +183,17 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, int m, int co0
         }
     } else {
         uint16_t* out = static_cast<uint16_t*>(p.y) + row;
-        if (ncols == 32 && (p.C_out & 7) == 0) {
+        if (ncols == 32 && (p.C_out & 15) == 0) {
+            // whole 32-byte sectors: two 256-bit stores
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float* w = v + 16 * h;
+                ptx::st_global_v8(out + 16 * h, pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                                  pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]),
+                                  pack_bf16x2(w[8], w[9]), pack_bf16x2(w[10], w[11]),
+                                  pack_bf16x2(w[12], w[13]), pack_bf16x2(w[14], w[15]));
+            }
+        } else if (ncols == 32 && (p.C_out & 7) == 0) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 reinterpret_cast<uint4*>(out)[q] =
@@ -1028,7 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 // window mode: (kh, cc) of the K block, walked instead of divided
                 int win_kh = 0, win_cc = 0;
-                if (WINDOW) {
+                if (WINDOW && u.kb0 != 0) {  // split K only
                     win_kh = u.kb0 / p.win_cc;
                     win_cc = u.kb0 - win_kh * p.win_cc;
                 }
