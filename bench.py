@@ -96,7 +96,7 @@ def shape_numbers(g, c: workloads.ConvShape):
                                             c.dilation),
                 im2win_bytes=g.im2win_bytes(c.N, c.C_in, c.H, c.W, c.KH, c.KW, c.stride, c.pad,
                                             c.dilation),
-                path={1: "gather", 2: "dense", 3: "stem", 4: "window"}.get(
+                path={1: "gather", 2: "dense", 3: "stem", 4: "window", 5: "plane", 6: "im2win"}.get(
                     g.select_path(c.N, c.C_in, c.H, c.W, c.C_out, c.KH, c.KW, c.stride, c.pad,
                                   c.dilation), "?"))
 
@@ -290,7 +290,8 @@ class Layer:
                                    y=self.ys[i % self.sets])
 
     def launches_per_step(self):
-        return {"gather": 2, "dense": 1, "stem": 3, "window": 1}[self.num["path"]]
+        return {"gather": 2, "dense": 1, "stem": 3, "window": 1, "plane": 1,
+                "im2win": 3}[self.num["path"]]
 
 
 def time_layer(layer, steps, warmup, stream):

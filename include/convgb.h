@@ -83,11 +83,17 @@ typedef enum convgb_path {
                                  is staged in shared memory once per (kh, 64-channel block)
                                  by TMA and read by all KW taps ("Im2win", Abstract: the
                                  window order and its continuous accesses, on chip) */
-    CONVGB_PATH_PLANE = 5     /* the window path's shapes: the batch read as one tall image
+    CONVGB_PATH_PLANE = 5,    /* the window path's shapes: the batch read as one tall image
                                  of padded rows, tiles of whole padded rows; each input row
                                  is staged once per (tile, 64-channel block) and read by all
                                  KH*KW taps; rows and columns of the padding border are
                                  computed and discarded.  No workspace. */
+    CONVGB_PATH_IM2WIN = 6    /* C_in < 16, undilated, W_out <= 128: x re-laid out in window
+                                 order ("Im2win", Abstract), each column's (kh, ci) vector
+                                 padded to a multiple of 8; every output pixel's A row is then
+                                 one contiguous run of KW columns, loaded by TMA.  Workspace:
+                                 the re-laid-out input (less than half of im2col, else the
+                                 path does not apply) and the re-packed weights. */
 } convgb_path;
 
 /* Short English text for a status code; never NULL. */

@@ -114,6 +114,36 @@ NarrowRows narrow_rows(const ConvShape& c)
     return r;
 }
 
+// im2win path: each column of the window-order buffer holds the KH*C_in values
+// (kh, ci) of one input column, padded to KC (a multiple of 8) so that rows of
+// the buffer stay 16-byte aligned for TMA; W_used columns per output row.
+struct Im2winGeom {
+    int KC = 0, W_used = 0, R = 0;
+    long long buf_bytes = 0;
+};
+Im2winGeom im2win_geom(const ConvShape& c)
+{
+    Im2winGeom g;
+    g.KC = (c.KH * c.C_in + 7) / 8 * 8;
+    g.W_used = (c.W_out - 1) * c.s + (c.KW - 1) * c.d + 1;
+    g.R = c.W_out <= 128 ? 128 / c.W_out : 0;
+    g.buf_bytes = (long long)c.N * c.H_out * g.W_used * g.KC * 2;
+    return g;
+}
+
+// Small C_in, undilated, output rows that fit a 128-row tile, one output row's
+// block and its input rows within the re-layout kernel's 48 KB of shared
+// memory, and a buffer under half of im2col.
+bool im2win_applies(const ConvShape& c)
+{
+    if (c.C_in >= 16 || c.d != 1 || c.W_out > 128) return false;
+    const Im2winGeom g = im2win_geom(c);
+    // the re-layout kernel's shared memory: one output row's block and its input rows
+    if ((long long)g.W_used * g.KC * 2 + c.KH * c.W * c.C_in * 2 + 16 > 48 * 1024) return false;
+    if (g.buf_bytes / 2 >= (1LL << 31)) return false;
+    return g.buf_bytes < c.M * c.K * 2 / 2;
+}
+
 struct GemmPlan;
 GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32 = 0);
 bool window_applies(const ConvShape& c);
@@ -125,6 +155,7 @@ bool path_supports(int path, const ConvShape& c)
     switch (path) {
     case CONVGB_PATH_WINDOW: return window_applies(c);
     case CONVGB_PATH_PLANE: return plane_applies(c);
+    case CONVGB_PATH_IM2WIN: return im2win_applies(c);
     case CONVGB_PATH_GATHER: return c.C_in % 8 == 0;
     case CONVGB_PATH_DENSE: return c.C_in % 8 == 0 && (is_pointwise(c) || is_full_spatial(c));
     case CONVGB_PATH_STEM: return c.C_in % 8 != 0;
@@ -135,7 +166,7 @@ bool path_supports(int path, const ConvShape& c)
 int select_path(const ConvShape& c)
 {
     if (path_supports(CONVGB_PATH_DENSE, c)) return CONVGB_PATH_DENSE;
-    if (c.C_in % 8 != 0) return CONVGB_PATH_STEM;
+    if (c.C_in % 8 != 0) return im2win_applies(c) ? CONVGB_PATH_IM2WIN : CONVGB_PATH_STEM;
     if (path_supports(CONVGB_PATH_WINDOW, c)) return CONVGB_PATH_WINDOW;
     return CONVGB_PATH_GATHER;
 }
@@ -198,6 +229,25 @@ bool encode_window(CUtensorMap* m, const void* x, int N, int H, int W, int C_in,
     return r == CUDA_SUCCESS;
 }
 
+// The im2win buffer [N*H_out][W_used][KC] as A: row (wo, g) is the K = KW*KC
+// contiguous elements from column wo*s of output row g, so consecutive rows
+// overlap (row pitch s*KC elements).  Box: 64 K x W_out pixels x R output rows,
+// 128-byte swizzle, landing as R*W_out consecutive 128-byte tile rows.
+bool encode_im2win(CUtensorMap* m, const void* win, const ConvShape& c, int KC, int W_used, int R)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)c.KW * KC, (cuuint64_t)c.W_out,
+                          (cuuint64_t)c.N * c.H_out};
+    cuuint64_t strides[2] = {(cuuint64_t)c.s * KC * 2, (cuuint64_t)W_used * KC * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)c.W_out, (cuuint32_t)R};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(win), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int pick_bn(int C_out)
 {
     if (C_out <= 32) return 32;
@@ -220,6 +270,7 @@ struct GemmPlan {
     int extra_smem = 0;            // narrow window: staged-row slots
     int nw_slots = 0;
     int tma_store = 0;             // epilogue through a staging tile and TMA stores
+    int epi_bufs = 1;              // staging tiles of that epilogue
     int pl_u = 1, pl_nacc = 0, b_stages = 0;  // plane mode: sub-tiles, accumulators, B slots
     int pair = 0;                  // window mode on a CTA pair (each CTA holds bn/2 columns of B)
     long long M = 0, K = 0;
@@ -257,11 +308,20 @@ void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
 {
     if (y_f32 || c.C_out % 8 != 0 || g.splits != 1 || g.bn < 64 || g.stages < 2) return;
     const int kb_res = g.bres ? (int)((g.K + 63) / 64) : g.num_kb;
-    const int s = igemm_pick_stages(g.pair ? g.bn / 2 : g.bn, g.bres, kb_res, g.a_stage_bytes,
-                                    g.b_per_stage, g.extra_smem + kEpiStageBytes);
+    const int bnb = g.pair ? g.bn / 2 : g.bn;
+    const int s = igemm_pick_stages(bnb, g.bres, kb_res, g.a_stage_bytes, g.b_per_stage,
+                                    g.extra_smem + kEpiStageBytes);
     if (s < 2) return;
     g.stages = s;
     g.tma_store = 1;
+    g.epi_bufs = 1;
+    // A second staging tile when it costs at most one ring stage and leaves four.
+    const int s2 = igemm_pick_stages(bnb, g.bres, kb_res, g.a_stage_bytes, g.b_per_stage,
+                                     g.extra_smem + kEpiStageBytes + kEpiTileBytes);
+    if (s2 >= 4 && s2 >= s - 1) {
+        g.stages = s2;
+        g.epi_bufs = 2;
+    }
 }
 
 GemmPlan plan_gemm_ring(int path, const ConvShape& c);
@@ -434,6 +494,29 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         g.splits = choose_splits((long long)g.m_tiles * g.n_tiles, g.num_kb, partial, im2col / 2);
         return g;  // stages == 0 (nothing fits): see window_applies()
     }
+    if (path == CONVGB_PATH_IM2WIN) {
+        // A by TMA from the window-order buffer: tiles of R whole output rows,
+        // K ordered (kw, kh, ci) with each kw slice padded to KC.
+        const Im2winGeom ig = im2win_geom(c);
+        g.amode = kAIm2win;
+        g.M = c.M;
+        g.K = (long long)c.KW * ig.KC;
+        g.num_kb = (int)((g.K + 63) / 64);
+        g.win_wv = c.W_out;
+        g.win_rows = ig.R;
+        g.m_step = ig.R;
+        g.m_tiles = (int)(((long long)c.N * c.H_out + ig.R - 1) / ig.R);
+        g.bn = pick_bn(c.C_out);
+        g.n_tiles = (c.C_out + g.bn - 1) / g.bn;
+        const long long im2col = c.M * c.K * 2;
+        const long long partial = c.M * c.C_out * 4;
+        g.splits = choose_splits((long long)g.m_tiles * g.n_tiles, g.num_kb, partial, im2col / 2);
+        if (g.n_tiles == 1 && g.splits == 1 &&
+            igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
+            g.bres = 1;
+        g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb, g.a_stage_bytes, 1);
+        return g;
+    }
     // Gather path: TMA gather4 when a 64-column K block stays inside one tap's
     // channels, 16-byte cp.async otherwise.
     if (path == CONVGB_PATH_STEM && narrow_window_geometry(c)) {
@@ -494,6 +577,7 @@ bool window_applies(const ConvShape& c)
 
 // Workspace regions of each path, in order; every region starts 256-byte aligned.
 struct WsLayout {
+    size_t win_off = 0, win_bytes = 0;  // im2win path: window-order input
     size_t ibuf_off = 0, ibuf_bytes = 0;
     size_t wpad_off = 0, wpad_bytes = 0;
     size_t part_off = 0, part_bytes = 0;
@@ -510,7 +594,12 @@ WsLayout workspace_layout(int path, const ConvShape& c)
         L.ibuf_bytes = (size_t)c.H_out * c.W_out * c.KH * c.KW * sizeof(int32_t);
         at = align_up(at + L.ibuf_bytes, kAlign);
     }
-    if (path == CONVGB_PATH_STEM) {
+    if (path == CONVGB_PATH_IM2WIN) {
+        L.win_off = at;
+        L.win_bytes = (size_t)im2win_geom(c).buf_bytes;
+        at = align_up(at + L.win_bytes, kAlign);
+    }
+    if (path == CONVGB_PATH_STEM || path == CONVGB_PATH_IM2WIN) {
         L.wpad_off = at;
         L.wpad_bytes = (size_t)c.C_out * g.K * 2;
         at = align_up(at + L.wpad_bytes, kAlign);
@@ -557,6 +646,11 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     if (!encode_kmajor(&out->tb, a.w, a.C_out, g.K, g.pair ? g.bn / 2 : g.bn)) return CONVGB_ERR_CUDA;
     if (g.amode == kADense && !encode_kmajor(&out->ta, a.a_dense, g.M, g.K, 128))
         return CONVGB_ERR_CUDA;
+    if (g.amode == kAIm2win) {
+        const Im2winGeom ig = im2win_geom(*a.shape);
+        if (!encode_im2win(&out->ta, a.a_dense, *a.shape, ig.KC, ig.W_used, ig.R))
+            return CONVGB_ERR_CUDA;
+    }
     // TMA gather: x as [N*H*W][C_in], one-row boxes of 64 channels.
     if (g.amode == kATmaGather && !encode_kmajor(&out->ta, a.x, a.x_rows, a.C_in, 1))
         return CONVGB_ERR_CUDA;
@@ -571,7 +665,8 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     if (g.tma_store) {
         // row tiles: the tile's win_rows output rows, consecutive in y; plane
         // tiles: one output row per box (their rows are not consecutive)
-        const int box_rows = (window || g.amode == kANarrowWin) ? g.win_rows * a.shape->W_out
+        const int box_rows = (window || g.amode == kANarrowWin || g.amode == kAIm2win)
+                                 ? g.win_rows * a.shape->W_out
                              : plane                             ? a.shape->W_out
                                                                  : 128;
         if (!encode_kmajor(&out->ty, a.y, g.M, a.C_out, box_rows)) return CONVGB_ERR_CUDA;
@@ -603,6 +698,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     p.split_div = FastDiv((uint32_t)g.splits);
     p.ntile_div = FastDiv((uint32_t)g.n_tiles);
     p.tma_store = g.tma_store;
+    p.epi_bufs = g.epi_bufs;
     p.stages = g.stages;
     p.bres = g.bres;
     p.m_step = g.m_step;
@@ -628,6 +724,13 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.nw_kwcp = nr.kwcp;
         p.nw_slot_bytes = nr.slot;
         p.nw_slots = g.nw_slots;
+    }
+    if (g.amode == kAIm2win) {
+        const ConvShape& c = *a.shape;
+        p.win_wv = c.W_out;
+        p.win_rows = g.win_rows;
+        p.win_groups = c.N * c.H_out;
+        p.win_wout = c.W_out;
     }
     if (window) {
         const ConvShape& c = *a.shape;
@@ -700,7 +803,7 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
     if (y_dtype != CONVGB_BF16 && y_dtype != CONVGB_F32) return CONVGB_ERR_INVALID_ARG;
     if (path == CONVGB_PATH_AUTO) path = select_path(c);
     if (path != CONVGB_PATH_GATHER && path != CONVGB_PATH_DENSE && path != CONVGB_PATH_STEM &&
-        path != CONVGB_PATH_WINDOW && path != CONVGB_PATH_PLANE)
+        path != CONVGB_PATH_WINDOW && path != CONVGB_PATH_PLANE && path != CONVGB_PATH_IM2WIN)
         return CONVGB_ERR_INVALID_ARG;
     if (!path_supports(path, c)) return CONVGB_ERR_UNSUPPORTED;
     WsLayout L = workspace_layout(path, c);
@@ -727,6 +830,13 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
         a.a_dense = x;
     } else if (path == CONVGB_PATH_WINDOW || path == CONVGB_PATH_PLANE) {
         a.x = static_cast<const uint16_t*>(x);
+        a.C_in = C_in;
+        a.shape = &c;
+    } else if (path == CONVGB_PATH_IM2WIN) {
+        // A = the window-order buffer, B = the weights re-packed to its K order
+        a.a_dense = wsb + L.win_off;
+        wpad = reinterpret_cast<uint16_t*>(wsb + L.wpad_off);
+        a.w = wpad;
         a.C_in = C_in;
         a.shape = &c;
     } else {
@@ -763,10 +873,18 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
     PreparedGemm pg;
     st = prepare_gemm(plan, a, &pg);
     if (st != CONVGB_OK) return st;
-    if (wpad && launch_pack_padded_weights(static_cast<const uint16_t*>(w), wpad, C_out,
-                                           a.pack_taps, a.pack_cin, a.pack_cp, (int)plan.K,
-                                           cs) != cudaSuccess)
+    if (path == CONVGB_PATH_IM2WIN) {
+        const int KC = im2win_geom(c).KC;
+        if (launch_pack_im2win_weights(static_cast<const uint16_t*>(w), wpad, C_out, KH, KW, C_in,
+                                       KC, cs) != cudaSuccess ||
+            launch_im2win_padded(c, KC, static_cast<const uint16_t*>(x),
+                                 reinterpret_cast<uint16_t*>(wsb + L.win_off), cs) != cudaSuccess)
+            return CONVGB_ERR_CUDA;
+    } else if (wpad && launch_pack_padded_weights(static_cast<const uint16_t*>(w), wpad, C_out,
+                                                  a.pack_taps, a.pack_cin, a.pack_cp,
+                                                  (int)plan.K, cs) != cudaSuccess) {
         return CONVGB_ERR_CUDA;
+    }
     if (ibuf && launch_build_indirection(c, ibuf, cs) != cudaSuccess) return CONVGB_ERR_CUDA;
     return launch_gemm(pg, cs);
 }

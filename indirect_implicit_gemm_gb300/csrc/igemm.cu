@@ -54,7 +54,7 @@ constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kSmemLimit = 232448;    // opt-in dynamic shared memory per block
 constexpr int kMaxAcc = 4;
 constexpr int kMaxSlots = 4;  // narrow window: staged-row slots
-static_assert((4 * kMaxStages + 2 * kMaxAcc + 2 + 2 * kMaxSlots) * 8 + 8 + 20 <= kHeaderBytes,
+static_assert((4 * kMaxStages + 2 * kMaxAcc + 2 + 2 * kMaxSlots) * 8 + 8 + 36 <= kHeaderBytes,
               "header area");
 
 template <int BN>
@@ -302,7 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // B block bytes in this CTA's shared memory (a pair splits B's columns)
     constexpr uint32_t BB = PAIR ? C::kBBytes / 2 : C::kBBytes;
     constexpr bool PLANE = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
-    constexpr bool ROWTILES = WINDOW || NARROWWIN;  // tiles of whole output rows
+    constexpr bool IM2WIN = AMODE == kAIm2win;
+    constexpr bool ROWTILES = WINDOW || NARROWWIN || IM2WIN;  // tiles of whole output rows
+    // Modes whose gather warps have nothing to gather run the epilogue on eight
+    // warps: each thread converts 32 of a 64-column chunk's columns instead of
+    // all 64 (the epilogue is latency-bound with one warp per scheduler).
+    constexpr bool EPI8 = WINDOW || AMODE == kADense || IM2WIN;
+    constexpr int kEpiN = EPI8 ? 2 * kEpiThreads : kEpiThreads;
     const uint32_t S = static_cast<uint32_t>(p.stages);
     const uint32_t AST = static_cast<uint32_t>(p.a_stage_bytes);
     extern __shared__ uint8_t smem_raw[];
@@ -338,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA-store epilogue: a 128 x 64 bf16 staging tile (128-byte swizzle) and the
     // current column tile's bias in fp32.
     uint8_t* sEpi = sStg + (NARROWWIN ? NS * p.nw_slot_bytes : 0);
-    float* sBias = reinterpret_cast<float*>(sEpi + 16384);
-    uint32_t* sVote = reinterpret_cast<uint32_t*>(abort_flag + 1);  // 4 epilogue-warp votes
-    volatile uint32_t* sTilesDone = sVote + 4;  // tiles the epilogue has finished (window prefetch)
+    float* sBias = reinterpret_cast<float*>(sEpi + p.epi_bufs * kEpiTileBytes);
+    uint32_t* sVote = reinterpret_cast<uint32_t*>(abort_flag + 1);  // up to 8 epilogue-warp votes
+    volatile uint32_t* sTilesDone = sVote + 8;  // tiles the epilogue has finished (plane prefetch)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t s = 0; s < SB; ++s) ptx::mbar_init(&empty_b[s], 1);
         for (uint32_t i = 0; i < NACC; ++i) {
             ptx::mbar_init(&tfull[i], 1);
-            ptx::mbar_init(&tempty[i], PAIR ? 2 * kEpiThreads : kEpiThreads);
+            ptx::mbar_init(&tempty[i], PAIR ? 2 * kEpiN : kEpiN);
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(bres_full, 1);
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_barrier_init();
     }
     if (warp == kTmaWarp && lane == 0) {
-        if (AMODE == kADense || AMODE == kATmaGather || WINDOW || PLANE)
+        if (AMODE == kADense || AMODE == kATmaGather || WINDOW || PLANE || IM2WIN)
             ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
     }
@@ -406,12 +412,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
     const int total_tiles = p.m_tiles * p.n_tiles * p.splits;
 
-    if (warp < kEpiWarps) {
+    if (warp < kEpiWarps || (EPI8 && warp < kEpiWarps + kGatherWarps)) {
         // ------------------------------------------------------------ epilogue
-        // This thread's accumulator row r = TMEM lane.  Window mode: row r is
-        // virtual pixel (wrow, wcol) of the tile's output rows; spill columns
-        // (wcol >= W_out) and rows past the tile's output rows are discarded.
-        const int r = warp * 32 + lane;
+        // This thread's accumulator row r = TMEM lane (a warp reaches the lane
+        // quarter warp % 4).  Window mode: row r is virtual pixel (wrow, wcol) of
+        // the tile's output rows; spill columns (wcol >= W_out) and rows past the
+        // tile's output rows are discarded.  With eight warps, warp w takes the
+        // 32-column half w / 4 of every 64-column chunk.
+        const int quad = warp & 3;
+        const int half = EPI8 ? (warp >> 2) : 0;
+        const int r = quad * 32 + lane;
+        const int et = EPI8 ? static_cast<int>(threadIdx.x) : r;  // index among epilogue threads
         // the accumulator is handed back to the MMA thread, which in a pair sits in CTA 0
         auto release_acc = [&](uint32_t acc) {
             ptx::tc_fence_before();
@@ -423,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wrow = (ROWTILES || PLANE) ? r / p.win_wv : 0;
         const int wcol = (ROWTILES || PLANE) ? r - wrow * p.win_wv : 0;
         uint32_t lt = 0;
+        uint32_t echunk = 0;  // staged chunks so far (double-buffered staging alternates)
         int bias_n0 = -1;
         Ring ar;  // accumulator index and the parity of its current use
         for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt, ar.next(NACC)) {
@@ -433,23 +445,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ready = __all_sync(0xffffffffu, wait_bar(&tfull[acc], ar.phase, wc, kRoleEpilogue));
             if (p.tma_store) {
                 if (lane == 0) sVote[warp] = ready ? 1u : 0u;
-                ptx::named_barrier_sync(1, kEpiThreads);
-                ready = sVote[0] && sVote[1] && sVote[2] && sVote[3];
-                ptx::named_barrier_sync(1, kEpiThreads);
+                ptx::named_barrier_sync(1, kEpiN);
+                ready = sVote[0] && sVote[1] && sVote[2] && sVote[3] &&
+                        (!EPI8 || (sVote[4] && sVote[5] && sVote[6] && sVote[7]));
+                ptx::named_barrier_sync(1, kEpiN);
             }
             if (!ready) break;
             ptx::tc_fence_after();
             if (p.tma_store && u.n0 != bias_n0) {  // new column tile: stage its bias
-                ptx::named_barrier_sync(1, kEpiThreads);
-                for (int i = r; i < BN; i += kEpiThreads)
+                ptx::named_barrier_sync(1, kEpiN);
+                for (int i = et; i < BN; i += kEpiN)
                     sBias[i] = (p.bias != nullptr && u.n0 + i < p.C_out)
                                    ? bf16_bits_to_float(p.bias[u.n0 + i])
                                    : 0.f;
-                ptx::named_barrier_sync(1, kEpiThreads);
+                ptx::named_barrier_sync(1, kEpiN);
                 bias_n0 = u.n0;
             }
             const uint32_t tbase =
-                tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * ACCW;
+                tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACCW;
             const int nsub = PLANE ? p.pl_u : 1;
             for (int sub = 0; sub < nsub; ++sub) {
                 const bool last_sub = sub + 1 == nsub;
@@ -476,13 +489,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                     for (int c64 = 0; c64 < BN / 64; ++c64) {
                         uint32_t ra[32], rb[32];
-                        ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
-                        ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
+                        if (EPI8) {
+                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + half * 32, ra);
+                        } else {
+                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
+                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
+                        }
                         ptx::tmem_ld_wait();
                         if (last_sub && c64 + 1 == BN / 64) release_acc(acc);
-                        // The staging tile is free once the previous store has read it.
-                        if (r == 0) ptx::bulk_wait_read_all();
-                        ptx::named_barrier_sync(1, kEpiThreads);
+                        // The staging tile is free once the store that last used it
+                        // has read it: the previous chunk's, or with two tiles the one
+                        // before.
+                        uint8_t* sE = sEpi + ((p.epi_bufs == 2) ? (echunk & 1u) : 0u) * kEpiTileBytes;
+                        ++echunk;
+                        if (et == 0) {
+                            if (p.epi_bufs == 2)
+                                ptx::bulk_wait_read_1();
+                            else
+                                ptx::bulk_wait_read_all();
+                        }
+                        ptx::named_barrier_sync(1, kEpiN);
                         const float4* bs = reinterpret_cast<const float4*>(sBias + c64 * 64);
                         // Row tiles keep only real output pixels, packed: the tile's
                         // output rows are consecutive rows of y, so one box stores
@@ -491,8 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool keep = !ROWTILES || (wcol < p.win_wout && wrow < p.win_rows);
                         if (keep) {
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const uint32_t* src = q < 4 ? ra + 8 * q : rb + 8 * (q - 4);
+                            for (int qq = 0; qq < (EPI8 ? 4 : 8); ++qq) {
+                                const int q = (EPI8 ? 4 * half : 0) + qq;  // 16-byte piece of the row
+                                const uint32_t* src =
+                                    (EPI8 || qq < 4) ? ra + 8 * qq : rb + 8 * (qq - 4);
                                 const float4 b0 = bs[2 * q], b1 = bs[2 * q + 1];
                                 uint4 v;
                                 v.x = pack_bf16x2(__uint_as_float(src[0]) + b0.x,
@@ -503,13 +531,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   __uint_as_float(src[5]) + b1.y);
                                 v.w = pack_bf16x2(__uint_as_float(src[6]) + b1.z,
                                                   __uint_as_float(src[7]) + b1.w);
-                                *reinterpret_cast<uint4*>(sEpi + srow * 128 +
+                                *reinterpret_cast<uint4*>(sE + srow * 128 +
                                                           ((q ^ (srow & 7)) << 4)) = v;
                             }
                         }
                         ptx::fence_proxy_async_smem();
-                        ptx::named_barrier_sync(1, kEpiThreads);
-                        if (r == 0) {
+                        ptx::named_barrier_sync(1, kEpiN);
+                        if (et == 0) {
                             const int c0 = u.n0 + c64 * 64;
                             if (PLANE) {
                                 // one box per real output row of this sub-tile
@@ -521,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         static_cast<int>(hv) >= p.pl_hout)
                                         continue;
                                     ptx::tma_store_2d(
-                                        &tmap_y, sEpi + jj * p.win_wv * 128, c0,
+                                        &tmap_y, sE + jj * p.win_wv * 128, c0,
                                         (static_cast<int>(n) * p.pl_hout + static_cast<int>(hv)) *
                                             p.win_wout);
                                 }
@@ -529,18 +557,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 // win_rows*W_out rows from the tile's first output pixel;
                                 // rows past the end of y are not written
                                 if (u.m0 < p.win_groups)
-                                    ptx::tma_store_2d(&tmap_y, sEpi, c0, u.m0 * p.win_wout);
+                                    ptx::tma_store_2d(&tmap_y, sE, c0, u.m0 * p.win_wout);
                             } else {
-                                ptx::tma_store_2d(&tmap_y, sEpi, c0, u.m0);
+                                ptx::tma_store_2d(&tmap_y, sE, c0, u.m0);
                             }
                             ptx::bulk_commit_group();
                         }
                     }
                     continue;
                 }
-                // Direct stores: two 32-column chunks per TMEM round trip; the
-                // accumulator is handed back to the MMA warp as soon as its last
-                // chunk is in registers.
+                // Direct stores: two 32-column chunks per TMEM round trip (one per
+                // warp half with eight warps); the accumulator is handed back to
+                // the MMA warp as soon as its last chunk is in registers.
+                if (EPI8) {
+                    bool released = false;
+#pragma unroll 1
+                    for (int ch = half; ch < BN / 32; ch += 2) {
+                        uint32_t ra[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + ch * 32, ra);
+                        ptx::tmem_ld_wait();
+                        if (last_sub && ch + 2 >= BN / 32) {
+                            release_acc(acc);
+                            released = true;
+                        }
+                        const int co0 = u.n0 + ch * 32;
+                        if (live && co0 < p.C_out) {
+                            if (p.splits > 1)
+                                reduce_chunk(p, m, co0, ra);
+                            else
+                                store_chunk(p, m, co0, ra);
+                        }
+                    }
+                    if (last_sub && !released) release_acc(acc);
+                } else {
 #pragma unroll 1
                 for (int ch = 0; ch < BN / 32; ch += 2) {
                     uint32_t ra[32], rb[32];
@@ -562,11 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             store_chunk(p, m, co0 + 32, rb);
                     }
                 }
+                }
             }
-            if (r == 0) *sTilesDone = lt + 1;
+            if (et == 0) *sTilesDone = lt + 1;
         }
         // Every TMA store has finished before the CTA exits.
-        if (p.tma_store && r == 0) ptx::bulk_wait_all();
+        if (p.tma_store && et == 0) ptx::bulk_wait_all();
     } else if (warp < kEpiWarps + kGatherWarps) {
         // ------------------------------------------------------------ A gather
         if (PLANE && warp == kEpiWarps) {
@@ -635,42 +685,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.x + (static_cast<long long>(n) * p.x_H + h) * row_elems);
                     for (int l = lane; l < lines; l += 32) ptx::prefetch_l2_line(row + l * 128);
                 }
-            }
-        } else if (WINDOW && warp == kEpiWarps) {
-            // The gather warps have nothing to gather in window mode; the first
-            // of them pulls the input rows of the next tiles into L2 with plain
-            // prefetches (the TMA engine stays free for the loads themselves),
-            // about three tiles ahead of the epilogue.
-            const long long row_elems = static_cast<long long>(p.x_W) * p.C_in;
-            const int lines = static_cast<int>((row_elems * 2 + 127) / 128);
-            auto prefetch_tile = [&](int t) {
-                const Unit v = unit_of<BN, PAIR>(p, t, rank);
-                const int rows = min(p.win_rows, p.win_groups - v.m0);
-                for (int jj = 0; jj < rows; ++jj) {
-                    uint32_t n, ho;
-                    p.ho_div.divmod(static_cast<uint32_t>(v.m0 + jj), n, ho);
-                    for (int kh = 0; kh < p.x_KH; ++kh) {
-                        // (undilated) rows the previous output row of this tile reached
-                        if (jj > 0 && kh < p.x_KH - 1 && p.win_d == 1) continue;
-                        const int h = static_cast<int>(ho) - p.win_pad + kh * p.win_d;
-                        if (h < 0 || h >= p.x_H) continue;
-                        const uint16_t* row =
-                            p.x + (static_cast<long long>(n) * p.x_H + h) * row_elems;
-                        for (int l = lane; l < lines; l += 32)
-                            ptx::prefetch_l2_line(reinterpret_cast<const uint8_t*>(row) + l * 128);
-                    }
-                }
-            };
-            // Pacing is advisory: a bounded spin on the epilogue's tile counter,
-            // then prefetch anyway.
-            volatile uint32_t* aborted = abort_flag;
-            uint32_t lt = 0;
-            for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt) {
-                for (uint32_t spin = 0; spin < (1u << 22) && lt > *sTilesDone + 3u && !*aborted;
-                     ++spin) {
-                }
-                if (*aborted) break;
-                prefetch_tile(tile);
             }
         } else if (AMODE == kATmaGather) {
             // TMA gather4 through the indirection buffer.  The four gather warps
@@ -1275,8 +1289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (uint32_t i = first; i < issued; ++i)
                         drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
             } else if (!p.bres || !GATHER) {
-                const uint32_t kTx = (p.bres ? 0u : static_cast<uint32_t>(BB)) +
-                                     (GATHER ? 0u : static_cast<uint32_t>(kABytes));
+                // im2win: a box of win_rows output rows x W_out pixels x 64 K
+                const uint32_t a_tx =
+                    GATHER   ? 0u
+                    : IM2WIN ? static_cast<uint32_t>(p.win_rows * p.win_wout) * 128u
+                             : static_cast<uint32_t>(kABytes);
+                const uint32_t kTx = (p.bres ? 0u : static_cast<uint32_t>(BB)) + a_tx;
                 Ring ring;
                 uint32_t issued = 0;
                 bool ok = true;
@@ -1288,7 +1306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         ptx::mbar_arrive_expect_tx(&full_b[ring.stage], kTx);
-                        if (!GATHER)
+                        if (IM2WIN)
+                            ptx::tma_load_3d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
+                                             kb * BK, 0, u.m0);
+                        else if (!GATHER)
                             ptx::tma_load_2d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, u.m0);
                         if (!p.bres)
@@ -1378,7 +1399,7 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         configured_for = dev;
     }
     const int extra = (AMODE == kANarrowWin ? p.nw_slots * p.nw_slot_bytes : 0) +
-                      (p.tma_store ? kEpiStageBytes : 0);
+                      (p.tma_store ? kEpiStageBytes + (p.epi_bufs - 1) * kEpiTileBytes : 0);
     constexpr bool kPlane = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     const int smem =
         kPlane
@@ -1484,6 +1505,7 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kATmaGather: return launch_mode<kATmaGather>(bn, ta, tb, ty, p, st);
     case kAWindow: return launch_mode<kAWindow>(bn, ta, tb, ty, p, st);
     case kAWindowPair: return launch_mode<kAWindowPair>(bn, ta, tb, ty, p, st);
+    case kAIm2win: return launch_mode<kAIm2win>(bn, ta, tb, ty, p, st);
     case kANarrowWin: return launch_mode<kANarrowWin>(bn, ta, tb, ty, p, st);
     case kAPlane: return launch_mode<kAPlane>(bn, ta, tb, ty, p, st);
     case kAPlane3: return launch_mode<kAPlane3>(bn, ta, tb, ty, p, st);

@@ -88,6 +88,8 @@ struct IgemmParams {
     FastDiv hp_div;          // divides a virtual row index by H + 2p
     int tma_store;           // 1: epilogue stages 64-column chunks in shared memory and
                              //    stores them with TMA (bf16 y, C_out % 8 == 0, no split)
+    int epi_bufs;            // TMA-store epilogue: staging tiles (2: chunk k+1 is staged
+                             //    while chunk k's store still reads its tile)
     int bres;                // 1: all of W's single column tile resident in shared memory
     float* partial;          // splits > 1: fp32 [M][C_out] sums, zeroed before the launch
     int y_f32;               // 1: fp32 output, 0: bf16
@@ -100,6 +102,12 @@ cudaError_t launch_build_indirection(const ConvShape& c, int32_t* ibuf, cudaStre
 cudaError_t launch_im2win(const ConvShape& c, const uint16_t* x, uint16_t* win, cudaStream_t st);
 cudaError_t launch_pack_padded_weights(const uint16_t* w, uint16_t* wp, int C_out, int taps,
                                        int C_in, int cp, int k_pad, cudaStream_t st);
+// im2win path: the padded window-order buffer [N*H_out][W_used][KC] and the
+// weights in its K order (kw, kh, ci), [C_out][KW*KC].
+cudaError_t launch_im2win_padded(const ConvShape& c, int KC, const uint16_t* x, uint16_t* win,
+                                 cudaStream_t st);
+cudaError_t launch_pack_im2win_weights(const uint16_t* w, uint16_t* wp, int C_out, int KH, int KW,
+                                       int C_in, int KC, cudaStream_t st);
 
 // How the A operand reaches shared memory.
 enum AMode : int {
@@ -123,6 +131,9 @@ enum AMode : int {
     kAWindowPair = 9, // window mode on a cluster of two CTAs: one tcgen05.mma.cta_group::2
                       // covers both CTAs' output tiles (256 rows); each CTA holds half of
                       // the weight columns
+    kAIm2win = 10,    // A rows read by 3-D TMA boxes from a padded im2win buffer: output
+                      // pixel wo of output row g is the contiguous run of KW columns from
+                      // column wo*s of row g (rows overlap; tiles of whole output rows)
 };
 // Dynamic shared memory of one implicit-GEMM CTA, and the deepest ring that fits
 // (0 when none does).
@@ -139,8 +150,10 @@ int smem_limit();
 cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& tmap_a,
                          const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
                          const IgemmParams& p, cudaStream_t st);
-// Shared memory the TMA-store epilogue adds (staging tile + bias).
-constexpr int kEpiStageBytes = 16384 + 1024;
+// Shared memory the TMA-store epilogue adds: one staging tile (128 x 64 bf16)
+// and the column tile's bias; a second staging tile when double-buffered.
+constexpr int kEpiTileBytes = 16384;
+constexpr int kEpiStageBytes = kEpiTileBytes + 1024;
 cudaError_t launch_finish_split(const float* partial, const uint16_t* bias, void* y, long long M,
                                 int C_out, int y_f32, cudaStream_t st);
 cudaError_t launch_selftest_timeout(unsigned long long timeout_ns, unsigned* err,

@@ -93,6 +93,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// 3-D tiled bulk tensor load (c0 innermost).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // 4-D tiled bulk tensor load (c0 innermost); out-of-range coordinates, negative
 // ones included, read as zero.
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
@@ -139,6 +150,12 @@ __device__ __forceinline__ void bulk_commit_group()
 __device__ __forceinline__ void bulk_wait_read_all()
 {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until the source shared memory of all but the most recent committed
+// bulk store group may be reused.
+__device__ __forceinline__ void bulk_wait_read_1()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Waits until all committed bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_all()

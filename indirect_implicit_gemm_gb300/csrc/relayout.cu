@@ -111,7 +111,112 @@ __global__ void __launch_bounds__(kThreads) pack_padded_weights_kernel(
     }
 }
 
+// Window-order re-layout with each column's (kh, ci) vector padded to KC
+// elements (a multiple of 8), for small C_in.  One CTA per output row
+// g = n*H_out + ho stages that row's KH input rows in shared memory (zeros
+// outside the image), then each thread builds whole columns
+//   win[g][wc][kc] = x[n][ho*s - p + kh][wc - p][ci],  kc = kh*C_in + ci < KH*C_in
+// and 0 for KH*C_in <= kc < KC, wc in [0, W_used), in shared memory (the
+// (kh, ci) walk needs no division), and the CTA copies the row's contiguous
+// W_used*KC block out with coalesced 16-byte stores.
+__global__ void __launch_bounds__(kThreads) im2win_padded_kernel(
+    const uint16_t* __restrict__ x, uint16_t* __restrict__ win, int H, int W, int C_in, int KH,
+    int s, int p, int H_out, int W_used, int KC)
+{
+    extern __shared__ uint4 smem_v[];  // output block [W_used][KC], then rows [KH][W*C_in]
+    const int out_vecs = W_used * KC / 8;
+    uint4* outs = smem_v;
+    uint16_t* rows = reinterpret_cast<uint16_t*>(smem_v + out_vecs);
+    const int g = blockIdx.x;
+    const int n = g / H_out, ho = g - n * H_out;
+    const int rowlen = W * C_in;
+    for (int kh = 0; kh < KH; ++kh) {
+        const int h = ho * s - p + kh;
+        uint16_t* dst = rows + kh * rowlen;
+        if (h < 0 || h >= H) {
+            for (int i = threadIdx.x; i < rowlen; i += blockDim.x) dst[i] = 0;
+            continue;
+        }
+        const uint16_t* src = x + (static_cast<long long>(n) * H + h) * rowlen;
+        if ((rowlen & 7) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+            for (int i = threadIdx.x; i < rowlen / 8; i += blockDim.x)
+                reinterpret_cast<uint4*>(dst)[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+        } else {
+            for (int i = threadIdx.x; i < rowlen; i += blockDim.x) dst[i] = src[i];
+        }
+    }
+    __syncthreads();
+    const int kcv = KC / 8;
+    for (int wc = threadIdx.x; wc < W_used; wc += blockDim.x) {
+        const int w = wc - p;
+        const bool inside = w >= 0 && w < W;
+        uint4* col = outs + wc * kcv;
+        const uint16_t* rp = rows + (inside ? w * C_in : 0);
+        int kh = 0, ci = 0;  // (kh, ci) of the next element, walked
+        for (int vec = 0; vec < kcv; ++vec) {
+            uint32_t a[4];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint32_t v = 0;
+                if (kh < KH) {
+                    if (inside) v = rp[kh * rowlen + ci];
+                    if (++ci == C_in) {
+                        ci = 0;
+                        ++kh;
+                    }
+                }
+                if (q & 1)
+                    a[q >> 1] |= v << 16;
+                else
+                    a[q >> 1] = v;
+            }
+            col[vec] = make_uint4(a[0], a[1], a[2], a[3]);
+        }
+    }
+    __syncthreads();
+    uint4* out = reinterpret_cast<uint4*>(win + static_cast<long long>(g) * W_used * KC);
+    for (int v = threadIdx.x; v < out_vecs; v += blockDim.x) out[v] = outs[v];
+}
+
+// Weights [C_out][KH][KW][C_in] -> [C_out][KW*KC] in the im2win path's K order
+// (kw, kh, ci), each kw slice padded with zeros from KH*C_in to KC.
+__global__ void __launch_bounds__(kThreads) pack_im2win_weights_kernel(
+    const uint16_t* __restrict__ w, uint16_t* __restrict__ wp, int total, FastDiv kpad_div,
+    FastDiv kc_div, int KH, int KW, int C_in)
+{
+    for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < (uint32_t)total;
+         e += gridDim.x * blockDim.x) {
+        uint32_t co, k, kw, kc;
+        kpad_div.divmod(e, co, k);
+        kc_div.divmod(k, kw, kc);
+        const int kh = static_cast<int>(kc) / C_in, ci = static_cast<int>(kc) - kh * C_in;
+        uint16_t v = 0;
+        if (kh < KH)
+            v = w[((static_cast<long long>(co) * KH + kh) * KW + kw) * C_in + ci];
+        wp[e] = v;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_im2win_padded(const ConvShape& c, int KC, const uint16_t* x, uint16_t* win,
+                                 cudaStream_t st)
+{
+    const int W_used = (c.W_out - 1) * c.s + (c.KW - 1) * c.d + 1;
+    const int smem = W_used * KC * 2 + (c.KH * c.W * c.C_in * 2 + 15) / 16 * 16;
+    im2win_padded_kernel<<<c.N * c.H_out, kThreads, smem, st>>>(x, win, c.H, c.W, c.C_in, c.KH,
+                                                                c.s, c.p, c.H_out, W_used, KC);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_im2win_weights(const uint16_t* w, uint16_t* wp, int C_out, int KH, int KW,
+                                       int C_in, int KC, cudaStream_t st)
+{
+    const int total = C_out * KW * KC;
+    pack_im2win_weights_kernel<<<grid_for(total, 4), kThreads, 0, st>>>(
+        w, wp, total, FastDiv(KW * KC), FastDiv(KC), KH, KW, C_in);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_build_indirection(const ConvShape& c, int32_t* ibuf, cudaStream_t st)
 {

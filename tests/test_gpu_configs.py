@@ -50,6 +50,11 @@ def test_full_size_plane_path_sampled(gpu_lib, shape):
     check_sampled(gpu_lib, shape, gpu_lib.PATH_PLANE)
 
 
+@pytest.mark.parametrize("shape", [c for c in FULL if c.C_in % 8 != 0], ids=lambda s: s.name)
+def test_full_size_stem_path_sampled(gpu_lib, shape):
+    check_sampled(gpu_lib, shape, gpu_lib.PATH_STEM)
+
+
 def check_sampled(gpu_lib, shape, path):
     x, w, b = workloads.make_inputs(shape)
     d = torch.device("cuda:0")

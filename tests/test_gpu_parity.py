@@ -141,6 +141,33 @@ def test_plane_path_matches_oracle(gpu_lib, shape, out_dtype):
     check(got, ref, mag, shape.name)
 
 
+# im2win path (small C_in): tiles of one or several output rows, a ragged last
+# tile, streamed weights (C_out > 128), and 11x11 stride 4.
+IM2WIN_SHAPES = [sh for sh in SMALL if sh.name in ("stem_c3_7x7_s2", "stem_c5", "stem_c12")] + [
+    S("im2win_c3_11x11_s4", N=1, C_in=3, H=64, W=64, C_out=64, KH=11, KW=11, stride=4, pad=2,
+      seed=45),
+    S("im2win_c3_5x5_cout200", N=2, C_in=3, H=20, W=20, C_out=200, KH=5, KW=5, pad=2, seed=46),
+    S("im2win_c7_7x7_s2", N=3, C_in=7, H=17, W=23, C_out=48, KH=7, KW=7, stride=2, pad=3,
+      seed=47),
+]
+STEM_SHAPES = [sh for sh in SMALL if sh.C_in % 8 != 0]
+
+
+@pytest.mark.parametrize("shape", IM2WIN_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_im2win_path_matches_oracle(gpu_lib, shape, out_dtype):
+    got, ref, mag = run_full(gpu_lib, shape, path=gpu_lib.PATH_IM2WIN, out_dtype=out_dtype)
+    check(got, ref, mag, shape.name)
+
+
+@pytest.mark.parametrize("shape", STEM_SHAPES, ids=lambda s: s.name)
+def test_stem_path_explicit_matches_oracle(gpu_lib, shape):
+    """The staged-row and scalar stem kernels, which conv2d_fwd no longer picks
+    where the im2win path applies."""
+    got, ref, mag = run_full(gpu_lib, shape, path=gpu_lib.PATH_STEM, out_dtype=torch.float32)
+    check(got, ref, mag, shape.name)
+
+
 def test_tiny_config_full_output(gpu_lib):
     """3 -> 4 channels, 8x8, 3x3, fp32 output: every output element."""
     shape = workloads.TINY
