@@ -72,6 +72,20 @@ bool is_pointwise(const ConvShape& c)
     return c.KH == 1 && c.KW == 1 && c.s == 1 && c.p == 0;
 }
 
+// 1x1 unpadded layers with stride > 1 read only every s-th pixel of every s-th
+// row: a 4-D TMA box with element strides (1, s, s, 1) loads exactly those.  A
+// tile is R whole output rows of one image (R divides H_out), so the box
+// traverses W_out*s pixels and R*s rows, each at most 256.
+int strided_rows(const ConvShape& c)
+{
+    if (!(c.KH == 1 && c.KW == 1 && c.p == 0 && c.s > 1 && c.s <= 8 && c.C_in % 8 == 0))
+        return 0;
+    if (c.W_out > 128 || c.W_out * c.s > 256) return 0;
+    for (int r = 128 / c.W_out; r >= 1; --r)
+        if (c.H_out % r == 0 && r * c.s <= 256) return r;
+    return 0;
+}
+
 bool is_full_spatial(const ConvShape& c)
 {
     return c.KH == c.H && c.KW == c.W && c.p == 0 && c.d == 1;  // H_out = W_out = 1
@@ -157,7 +171,8 @@ bool path_supports(int path, const ConvShape& c)
     case CONVGB_PATH_PLANE: return plane_applies(c);
     case CONVGB_PATH_IM2WIN: return im2win_applies(c);
     case CONVGB_PATH_GATHER: return c.C_in % 8 == 0;
-    case CONVGB_PATH_DENSE: return c.C_in % 8 == 0 && (is_pointwise(c) || is_full_spatial(c));
+    case CONVGB_PATH_DENSE:
+        return c.C_in % 8 == 0 && (is_pointwise(c) || is_full_spatial(c) || strided_rows(c) > 0);
     case CONVGB_PATH_STEM: return c.C_in % 8 != 0;
     default: return false;
     }
@@ -243,6 +258,23 @@ bool encode_im2win(CUtensorMap* m, const void* win, const ConvShape& c, int KC, 
     cuuint32_t box[3] = {64u, (cuuint32_t)c.W_out, (cuuint32_t)R};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(win), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// x [N][H][W][C_in] with element strides (1, s, s, 1): box = 64 channels x
+// W_out pixels x R rows of one image (traversing W_out*s pixels and R*s rows).
+bool encode_strided(CUtensorMap* m, const void* x, const ConvShape& c, int R)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)c.C_in, (cuuint64_t)c.W, (cuuint64_t)c.H, (cuuint64_t)c.N};
+    cuuint64_t strides[3] = {(cuuint64_t)c.C_in * 2, (cuuint64_t)c.W * c.C_in * 2,
+                             (cuuint64_t)c.H * c.W * c.C_in * 2};
+    cuuint32_t box[4] = {64u, (cuuint32_t)(c.W_out * c.s), (cuuint32_t)(R * c.s), 1u};
+    cuuint32_t estr[4] = {1u, (cuuint32_t)c.s, (cuuint32_t)c.s, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -494,6 +526,25 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         g.splits = choose_splits((long long)g.m_tiles * g.n_tiles, g.num_kb, partial, im2col / 2);
         return g;  // stages == 0 (nothing fits): see window_applies()
     }
+    if (path == CONVGB_PATH_DENSE && strided_rows(c) > 0) {
+        // 1x1 stride s: A straight from x by element-strided boxes, tiles of R
+        // whole output rows of one image.
+        const int R = strided_rows(c);
+        g.amode = kAStrided;
+        g.M = c.M;
+        g.K = c.C_in;
+        g.num_kb = (int)((g.K + 63) / 64);
+        g.win_wv = c.W_out;
+        g.win_rows = R;
+        g.m_step = R;
+        g.m_tiles = (int)((long long)c.N * c.H_out / R);
+        g.bn = pick_bn(c.C_out);
+        g.n_tiles = (c.C_out + g.bn - 1) / g.bn;
+        if (g.n_tiles == 1 && igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
+            g.bres = 1;
+        g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb, g.a_stage_bytes, 1);
+        return g;
+    }
     if (path == CONVGB_PATH_IM2WIN) {
         // A by TMA from the window-order buffer: tiles of R whole output rows,
         // K ordered (kw, kh, ci) with each kw slice padded to KC.
@@ -651,6 +702,8 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         if (!encode_im2win(&out->ta, a.a_dense, *a.shape, ig.KC, ig.W_used, ig.R))
             return CONVGB_ERR_CUDA;
     }
+    if (g.amode == kAStrided && !encode_strided(&out->ta, a.a_dense, *a.shape, g.win_rows))
+        return CONVGB_ERR_CUDA;
     // TMA gather: x as [N*H*W][C_in], one-row boxes of 64 channels.
     if (g.amode == kATmaGather && !encode_kmajor(&out->ta, a.x, a.x_rows, a.C_in, 1))
         return CONVGB_ERR_CUDA;
@@ -665,7 +718,8 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     if (g.tma_store) {
         // row tiles: the tile's win_rows output rows, consecutive in y; plane
         // tiles: one output row per box (their rows are not consecutive)
-        const int box_rows = (window || g.amode == kANarrowWin || g.amode == kAIm2win)
+        const int box_rows = (window || g.amode == kANarrowWin || g.amode == kAIm2win ||
+                              g.amode == kAStrided)
                                  ? g.win_rows * a.shape->W_out
                              : plane                             ? a.shape->W_out
                                                                  : 128;
@@ -725,12 +779,14 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.nw_slot_bytes = nr.slot;
         p.nw_slots = g.nw_slots;
     }
-    if (g.amode == kAIm2win) {
+    if (g.amode == kAIm2win || g.amode == kAStrided) {
         const ConvShape& c = *a.shape;
         p.win_wv = c.W_out;
         p.win_rows = g.win_rows;
         p.win_groups = c.N * c.H_out;
         p.win_wout = c.W_out;
+        p.ho_div = FastDiv((uint32_t)c.H_out);
+        p.st_s = c.s;
     }
     if (window) {
         const ConvShape& c = *a.shape;
@@ -826,8 +882,10 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
     int32_t* ibuf = nullptr;
     uint16_t* wpad = nullptr;
     if (path == CONVGB_PATH_DENSE) {
-        // 1x1 stride-1: A = x as [N*H*W][C_in]; full-spatial: A = x as [N][H*W*C_in].
+        // 1x1 stride-1: A = x as [N*H*W][C_in]; full-spatial: A = x as [N][H*W*C_in];
+        // 1x1 stride s: x read by element-strided boxes.
         a.a_dense = x;
+        a.shape = &c;
     } else if (path == CONVGB_PATH_WINDOW || path == CONVGB_PATH_PLANE) {
         a.x = static_cast<const uint16_t*>(x);
         a.C_in = C_in;

@@ -303,11 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t BB = PAIR ? C::kBBytes / 2 : C::kBBytes;
     constexpr bool PLANE = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     constexpr bool IM2WIN = AMODE == kAIm2win;
-    constexpr bool ROWTILES = WINDOW || NARROWWIN || IM2WIN;  // tiles of whole output rows
+    constexpr bool STRIDED = AMODE == kAStrided;
+    constexpr bool ROWTILES = WINDOW || NARROWWIN || IM2WIN || STRIDED;  // whole output rows
     // Modes whose gather warps have nothing to gather run the epilogue on eight
     // warps: each thread converts 32 of a 64-column chunk's columns instead of
     // all 64 (the epilogue is latency-bound with one warp per scheduler).
-    constexpr bool EPI8 = WINDOW || AMODE == kADense || IM2WIN;
+    constexpr bool EPI8 = WINDOW || AMODE == kADense || IM2WIN || STRIDED;
     constexpr int kEpiN = EPI8 ? 2 * kEpiThreads : kEpiThreads;
     const uint32_t S = static_cast<uint32_t>(p.stages);
     const uint32_t AST = static_cast<uint32_t>(p.a_stage_bytes);
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_barrier_init();
     }
     if (warp == kTmaWarp && lane == 0) {
-        if (AMODE == kADense || AMODE == kATmaGather || WINDOW || PLANE || IM2WIN)
+        if (AMODE == kADense || AMODE == kATmaGather || WINDOW || PLANE || IM2WIN || STRIDED)
             ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
     }
@@ -1289,11 +1290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (uint32_t i = first; i < issued; ++i)
                         drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
             } else if (!p.bres || !GATHER) {
-                // im2win: a box of win_rows output rows x W_out pixels x 64 K
+                // im2win, strided 1x1: a box of win_rows output rows x W_out pixels
+                // x 64 K
                 const uint32_t a_tx =
-                    GATHER   ? 0u
-                    : IM2WIN ? static_cast<uint32_t>(p.win_rows * p.win_wout) * 128u
-                             : static_cast<uint32_t>(kABytes);
+                    GATHER                ? 0u
+                    : (IM2WIN || STRIDED) ? static_cast<uint32_t>(p.win_rows * p.win_wout) * 128u
+                                          : static_cast<uint32_t>(kABytes);
                 const uint32_t kTx = (p.bres ? 0u : static_cast<uint32_t>(BB)) + a_tx;
                 Ring ring;
                 uint32_t issued = 0;
@@ -1306,10 +1308,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         ptx::mbar_arrive_expect_tx(&full_b[ring.stage], kTx);
-                        if (IM2WIN)
+                        if (IM2WIN) {
                             ptx::tma_load_3d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, 0, u.m0);
-                        else if (!GATHER)
+                        } else if (STRIDED) {
+                            // input rows ho*s.. of image n, every s-th pixel and row
+                            uint32_t n, ho;
+                            p.ho_div.divmod(static_cast<uint32_t>(u.m0), n, ho);
+                            ptx::tma_load_4d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
+                                             kb * BK, 0, static_cast<int>(ho) * p.st_s,
+                                             static_cast<int>(n));
+                        } else if (!GATHER)
                             ptx::tma_load_2d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, u.m0);
                         if (!p.bres)
@@ -1506,6 +1515,7 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kAWindow: return launch_mode<kAWindow>(bn, ta, tb, ty, p, st);
     case kAWindowPair: return launch_mode<kAWindowPair>(bn, ta, tb, ty, p, st);
     case kAIm2win: return launch_mode<kAIm2win>(bn, ta, tb, ty, p, st);
+    case kAStrided: return launch_mode<kAStrided>(bn, ta, tb, ty, p, st);
     case kANarrowWin: return launch_mode<kANarrowWin>(bn, ta, tb, ty, p, st);
     case kAPlane: return launch_mode<kAPlane>(bn, ta, tb, ty, p, st);
     case kAPlane3: return launch_mode<kAPlane3>(bn, ta, tb, ty, p, st);

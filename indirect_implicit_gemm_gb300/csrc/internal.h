@@ -68,6 +68,7 @@ struct IgemmParams {
     int win_wv, win_rows, win_groups, win_wout, win_kw, win_d, win_pad, win_cc;
     FastDiv ho_div;          // divides an output-row index (n*H_out + ho) by H_out
     int x_H, x_W, x_KH;      // window mode: input geometry (L2 prefetch of input rows)
+    int st_s;                // strided 1x1 mode: the stride
     // narrow-window mode: staged input rows
     int nw_H, nw_W, nw_KH, nw_s, nw_p, nw_cin;
     int nw_rb;               // bytes per staged row (16-byte multiple)
@@ -134,6 +135,9 @@ enum AMode : int {
     kAIm2win = 10,    // A rows read by 3-D TMA boxes from a padded im2win buffer: output
                       // pixel wo of output row g is the contiguous run of KW columns from
                       // column wo*s of row g (rows overlap; tiles of whole output rows)
+    kAStrided = 11,   // 1x1 stride-s unpadded layers: A read from x itself by 4-D TMA boxes
+                      // with element strides (1, s, s, 1), only the pixels the output
+                      // uses; tiles of whole output rows of one image
 };
 // Dynamic shared memory of one implicit-GEMM CTA, and the deepest ring that fits
 // (0 when none does).

@@ -110,7 +110,7 @@ def expected_path(c):
 
 @pytest.mark.parametrize("cfg,path", [
     (workloads.TINY, 3), (workloads.RESNET_3X3, 4), (workloads.POINTWISE_S1, 2),
-    (workloads.POINTWISE_S2, 1), (workloads.STEM_7X7, 6), (workloads.STRIDED_3X3, 1),
+    (workloads.POINTWISE_S2, 2), (workloads.STEM_7X7, 6), (workloads.STRIDED_3X3, 1),
 ] + [(c, expected_path(c)) for c in workloads.SWEEP], ids=lambda v: getattr(v, "name", str(v)))
 def test_path_selection(lib, cfg, path):
     got = lib.select_path(cfg.N, cfg.C_in, cfg.H, cfg.W, cfg.C_out, cfg.KH, cfg.KW, cfg.stride,

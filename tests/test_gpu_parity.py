@@ -88,6 +88,13 @@ SMALL = [
     S("stem_c5", N=1, C_in=5, H=10, W=11, C_out=40, seed=25),
     S("stem_c12", N=1, C_in=12, H=9, W=9, C_out=32, KH=3, KW=3, seed=26),
     S("stem_11x11_s4", N=1, C_in=3, H=47, W=45, C_out=64, KH=11, KW=11, stride=4, pad=2, seed=27),
+    # 1x1 stride > 1: element-strided TMA boxes (K tail, odd widths, stride 3, two column tiles)
+    S("strided_1x1_s2_c72_ragged", N=3, C_in=72, H=10, W=13, C_out=96, KH=1, KW=1, stride=2,
+      pad=0, seed=48),
+    S("strided_1x1_s3_c16", N=2, C_in=16, H=17, W=20, C_out=40, KH=1, KW=1, stride=3, pad=0,
+      seed=49),
+    S("strided_1x1_s2_cout300", N=2, C_in=128, H=12, W=16, C_out=300, KH=1, KW=1, stride=2,
+      pad=0, seed=50),
 ]
 
 
