@@ -592,26 +592,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (last_sub && !released) release_acc(acc);
                 } else {
 #pragma unroll 1
-                for (int ch = 0; ch < BN / 32; ch += 2) {
-                    uint32_t ra[32], rb[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + ch * 32, ra);
-                    if (ch + 1 < BN / 32) ptx::tmem_ld_32x32b_x32(taddr + (ch + 1) * 32, rb);
-                    ptx::tmem_ld_wait();
-                    if (last_sub && ch + 2 >= BN / 32) release_acc(acc);
-                    const int co0 = u.n0 + ch * 32;
-                    if (live && co0 < p.C_out) {
-                        if (p.splits > 1)
-                            reduce_chunk(p, m, co0, ra);
-                        else
-                            store_chunk(p, m, co0, ra);
+                    for (int ch = 0; ch < BN / 32; ch += 2) {
+                        uint32_t ra[32], rb[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + ch * 32, ra);
+                        if (ch + 1 < BN / 32) ptx::tmem_ld_32x32b_x32(taddr + (ch + 1) * 32, rb);
+                        ptx::tmem_ld_wait();
+                        if (last_sub && ch + 2 >= BN / 32) release_acc(acc);
+                        const int co0 = u.n0 + ch * 32;
+                        if (live && co0 < p.C_out) {
+                            if (p.splits > 1)
+                                reduce_chunk(p, m, co0, ra);
+                            else
+                                store_chunk(p, m, co0, ra);
+                        }
+                        if (live && ch + 1 < BN / 32 && co0 + 32 < p.C_out) {
+                            if (p.splits > 1)
+                                reduce_chunk(p, m, co0 + 32, rb);
+                            else
+                                store_chunk(p, m, co0 + 32, rb);
+                        }
                     }
-                    if (live && ch + 1 < BN / 32 && co0 + 32 < p.C_out) {
-                        if (p.splits > 1)
-                            reduce_chunk(p, m, co0 + 32, rb);
-                        else
-                            store_chunk(p, m, co0 + 32, rb);
-                    }
-                }
                 }
             }
             if (et == 0) *sTilesDone = lt + 1;
