@@ -610,12 +610,19 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
     const long long im2col = c.M * c.K * 2;
     const long long partial = c.M * c.C_out * 4;
     g.splits = choose_splits((long long)g.m_tiles * g.n_tiles, g.num_kb, partial, im2col / 2);
+    // TMA gather with 256-wide column tiles: two CTAs per MMA, each streaming
+    // half of the weight columns (as on the window path).
+    if (g.amode == kATmaGather && g.bn == 256 && g.m_tiles >= 2 && g.splits == 1) {
+        g.amode = kATmaGatherPair;
+        g.pair = 1;
+    }
+    const int bnb = g.pair ? g.bn / 2 : g.bn;
     // Layers whose whole weight matrix is one column tile: keep it in shared
     // memory for the CTA's lifetime when that still leaves a 4-deep A ring.
     if (g.n_tiles == 1 && g.splits == 1 &&
-        igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
+        igemm_pick_stages(bnb, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
         g.bres = 1;
-    g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb, g.a_stage_bytes, 1);
+    g.stages = igemm_pick_stages(bnb, g.bres, g.num_kb, g.a_stage_bytes, 1);
     return g;
 }
 
@@ -640,7 +647,8 @@ WsLayout workspace_layout(int path, const ConvShape& c)
     WsLayout L;
     size_t at = 0;
     const GemmPlan g = plan_gemm(path, c);
-    if (g.amode == kAGather || g.amode == kATmaGather || g.amode == kANarrow) {
+    if (g.amode == kAGather || g.amode == kATmaGather || g.amode == kATmaGatherPair ||
+        g.amode == kANarrow) {
         L.ibuf_off = at;
         L.ibuf_bytes = (size_t)c.H_out * c.W_out * c.KH * c.KW * sizeof(int32_t);
         at = align_up(at + L.ibuf_bytes, kAlign);
@@ -705,7 +713,8 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     if (g.amode == kAStrided && !encode_strided(&out->ta, a.a_dense, *a.shape, g.win_rows))
         return CONVGB_ERR_CUDA;
     // TMA gather: x as [N*H*W][C_in], one-row boxes of 64 channels.
-    if (g.amode == kATmaGather && !encode_kmajor(&out->ta, a.x, a.x_rows, a.C_in, 1))
+    if ((g.amode == kATmaGather || g.amode == kATmaGatherPair) &&
+        !encode_kmajor(&out->ta, a.x, a.x_rows, a.C_in, 1))
         return CONVGB_ERR_CUDA;
     const bool plane = g.amode == kAPlane || g.amode == kAPlane3 || g.amode == kAPlane3U2;
     const bool window = g.amode == kAWindow || g.amode == kAWindowPair;
@@ -966,16 +975,16 @@ unsigned* device_error_word()
 
 int num_sms()
 {
-    static int sms[kMaxDevices] = {};
+    static std::atomic<int> sms[kMaxDevices] = {};
     int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return 148;
-    if (sms[dev] == 0) {
-        int v = 0;
+    int v = sms[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
             v = 148;
-        sms[dev] = v;
+        sms[dev].store(v, std::memory_order_relaxed);
     }
-    return sms[dev];
+    return v;
 }
 
 }  // namespace convgb

@@ -21,6 +21,8 @@
 // time and a timeout makes the whole CTA drain and return with an error code.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -295,10 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A written by the gather warps (signalled on full_a) or by the TMA warp
     // together with B (signalled on full_b).
     constexpr bool NARROWWIN = AMODE == kANarrowWin;
-    constexpr bool GATHER =
-        AMODE == kAGather || AMODE == kANarrow || AMODE == kATmaGather || NARROWWIN;
-    constexpr bool PAIR = AMODE == kAWindowPair;  // window mode on a CTA pair
-    constexpr bool WINDOW = AMODE == kAWindow || PAIR;
+    constexpr bool TMAGATHER = AMODE == kATmaGather || AMODE == kATmaGatherPair;
+    constexpr bool GATHER = AMODE == kAGather || AMODE == kANarrow || TMAGATHER || NARROWWIN;
+    constexpr bool PAIR = AMODE == kAWindowPair || AMODE == kATmaGatherPair;  // CTA pair
+    constexpr bool WINDOW = AMODE == kAWindow || AMODE == kAWindowPair;
     // B block bytes in this CTA's shared memory (a pair splits B's columns)
     constexpr uint32_t BB = PAIR ? C::kBBytes / 2 : C::kBBytes;
     constexpr bool PLANE = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; ++s) {
             // TMA gather: one arrive.expect_tx per stage; thread gathers: every thread arrives.
-            ptx::mbar_init(&full_a[s], (AMODE == kATmaGather || PLANE) ? 1 : kGatherThreads);
+            ptx::mbar_init(&full_a[s], (TMAGATHER || PLANE) ? 1 : kGatherThreads);
             ptx::mbar_init(&full_b[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
@@ -380,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_barrier_init();
     }
     if (warp == kTmaWarp && lane == 0) {
-        if (AMODE == kADense || AMODE == kATmaGather || WINDOW || PLANE || IM2WIN || STRIDED)
+        if (AMODE == kADense || TMAGATHER || WINDOW || PLANE || IM2WIN || STRIDED)
             ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
     }
@@ -671,9 +673,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             volatile uint32_t* aborted = abort_flag;
             uint32_t lt = 0;
             for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt) {
-                for (uint32_t spin = 0; spin < (1u << 22) && lt > *sTilesDone + 3u && !*aborted;
-                     ++spin) {
-                }
+                // (backs off between polls so the spin takes no issue slots from the
+                // epilogue warp on the same scheduler)
+                for (uint32_t spin = 0; spin < (1u << 16) && lt > *sTilesDone + 3u && !*aborted;
+                     ++spin)
+                    __nanosleep(256);
                 if (*aborted) break;
                 const Unit v = unit_of<BN, PAIR>(p, tile, rank);
                 if (v.n0 != 0 || v.kb0 != 0) continue;  // one prefetch per row block
@@ -687,13 +691,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int l = lane; l < lines; l += 32) ptx::prefetch_l2_line(row + l * 128);
                 }
             }
-        } else if (AMODE == kATmaGather) {
+        } else if (TMAGATHER) {
             // TMA gather4 through the indirection buffer.  The four gather warps
             // take turns: warp gw fills the stages whose sequence number is gw
             // mod 4, so each has four stage-times to look its rows up.  Lane l
             // owns rows 4l..4l+3 of the 128-row tile: it turns each row's
             // (pixel, tap) entry into a row index of x viewed as [N*H*W][C_in]
-            // and issues one gather4 of those four 128-byte rows.
+            // and issues one gather4 of those four 128-byte rows.  On a pair both
+            // CTAs' gathers complete on CTA 0's barrier, which CTA 0 arms for both
+            // (rows past M gather zeros, so both always deliver a full tile).
             const int gw = warp - kEpiWarps;
             uint32_t it = 0;
             Ring ring;
@@ -732,15 +738,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (lane == 0) ptx::mbar_arrive_expect_tx(&full_a[ring.stage], kABytes);
+                    if (lane == 0 && rank == 0)
+                        ptx::mbar_arrive_expect_tx(&full_a[ring.stage],
+                                                   kABytes * (PAIR ? 2u : 1u));
                     __syncwarp();
-                    ptx::tma_gather4(sA + ring.stage * AST + lane * 4 * 128, &tmap_a,
-                                     &full_a[ring.stage], static_cast<int>(c0), row[0], row[1],
-                                     row[2], row[3]);
+                    if (PAIR)
+                        ptx::tma_gather4_pair(sA + ring.stage * AST + lane * 4 * 128, &tmap_a,
+                                              ptx::mapa(ptx::smem_addr(&full_a[ring.stage]), 0u),
+                                              static_cast<int>(c0), row[0], row[1], row[2],
+                                              row[3]);
+                    else
+                        ptx::tma_gather4(sA + ring.stage * AST + lane * 4 * 128, &tmap_a,
+                                         &full_a[ring.stage], static_cast<int>(c0), row[0],
+                                         row[1], row[2], row[3]);
                 }
             }
-            // Wait (bounded) for this warp's last gathers so none lands after exit.
-            if (lane == 0) {
+            // Wait (bounded) for this warp's last gathers so none lands after exit
+            // (a pair's complete on CTA 0's barriers, for both CTAs).
+            if (lane == 0 && rank == 0) {
                 const uint32_t first = it > S ? it - S : 0;
                 for (uint32_t i = first; i < it; ++i)
                     if (i % kGatherWarps == static_cast<uint32_t>(gw))
@@ -1307,7 +1322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        ptx::mbar_arrive_expect_tx(&full_b[ring.stage], kTx);
+                        if (rank == 0)
+                            ptx::mbar_arrive_expect_tx(&full_b[ring.stage],
+                                                       kTx * (PAIR ? 2u : 1u));
                         if (IM2WIN) {
                             ptx::tma_load_3d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, 0, u.m0);
@@ -1321,15 +1338,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else if (!GATHER)
                             ptx::tma_load_2d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, u.m0);
-                        if (!p.bres)
-                            ptx::tma_load_2d(sB + ring.stage * BB, &tmap_b,
-                                             &full_b[ring.stage], kb * BK, u.n0);
+                        if (!p.bres) {
+                            if (PAIR)  // this CTA's half of the column tile
+                                ptx::tma_load_2d_pair(
+                                    sB + ring.stage * BB, &tmap_b,
+                                    ptx::mapa(ptx::smem_addr(&full_b[ring.stage]), 0u), kb * BK,
+                                    u.n0 + static_cast<int>(rank) * (BN / 2));
+                            else
+                                ptx::tma_load_2d(sB + ring.stage * BB, &tmap_b,
+                                                 &full_b[ring.stage], kb * BK, u.n0);
+                        }
                     }
                 }
                 // Wait (bounded) for the last loads so none lands after the CTA exits.
                 const uint32_t first = issued > S ? issued - S : 0;
-                for (uint32_t i = first; i < issued; ++i)
-                    drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
+                if (rank == 0)
+                    for (uint32_t i = first; i < issued; ++i)
+                        drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
             }
         }
     }
@@ -1398,23 +1423,33 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
                       const IgemmParams& p, cudaStream_t st)
 {
     auto kern = igemm_kernel<BN, AMODE>;
-    static int configured_for = -1;  // device for which the smem attribute was set
+    // Per device (and per instantiation): the shared-memory opt-in, set once,
+    // and the pair mode's resident-cluster count for the last size asked.
+    constexpr int kDevs = 64;
+    static std::mutex mu;
+    static bool configured[kDevs] = {};
+    static int cluster_smem[kDevs] = {}, cluster_count[kDevs] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_for != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-        if (e != cudaSuccess) return e;
-        configured_for = dev;
+    if (dev < 0 || dev >= kDevs) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!configured[dev]) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
     }
     const int extra = (AMODE == kANarrowWin ? p.nw_slots * p.nw_slot_bytes : 0) +
                       (p.tma_store ? kEpiStageBytes + (p.epi_bufs - 1) * kEpiTileBytes : 0);
     constexpr bool kPlane = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
+    constexpr bool kPairMode = AMODE == kAWindowPair || AMODE == kATmaGatherPair;
     const int smem =
         kPlane
             ? plane_smem_bytes(BN, p.stages, p.a_stage_bytes, p.bres ? p.kb_total : p.b_stages,
                                extra)
-            : igemm_smem_bytes(AMODE == kAWindowPair ? BN / 2 : BN, p.stages, p.bres, p.kb_total,
+            : igemm_smem_bytes(kPairMode ? BN / 2 : BN, p.stages, p.bres, p.kb_total,
                                p.a_stage_bytes, p.b_per_stage, extra);
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
     if (kPlane &&
@@ -1426,7 +1461,7 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         (p.x_KH != 3 || p.win_kw != 3 || p.pl_u != (AMODE == kAPlane3U2 ? 2 : 1)))
         return cudaErrorInvalidValue;
     const int tiles = p.m_tiles * p.n_tiles * p.splits;  // pair mode: pair units
-    if (AMODE == kAWindowPair) {
+    if (kPairMode) {
         if (BN < 64) return cudaErrorInvalidValue;
         // Clusters of two CTAs, as many as can be resident at once (two SMs each).
         cudaLaunchConfig_t cfg = {};
@@ -1440,19 +1475,22 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         cfg.stream = st;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        static int cached_dev = -1, cached_smem = -1, cached_clusters = 0;
-        if (cached_dev != dev || cached_smem != smem) {
-            int nc = 0;
-            cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2));
-            if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess || nc < 1) {
-                (void)cudaGetLastError();
-                nc = num_sms() / 2;
+        int resident = 0;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            if (cluster_smem[dev] != smem || cluster_count[dev] < 1) {
+                int nc = 0;
+                cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2));
+                if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess || nc < 1) {
+                    (void)cudaGetLastError();
+                    nc = num_sms() / 2;
+                }
+                cluster_smem[dev] = smem;
+                cluster_count[dev] = nc;
             }
-            cached_dev = dev;
-            cached_smem = smem;
-            cached_clusters = nc;
+            resident = cluster_count[dev];
         }
-        const int clusters = tiles < cached_clusters ? tiles : cached_clusters;
+        const int clusters = tiles < resident ? tiles : resident;
         cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
         e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
         if (e != cudaSuccess) return e;
@@ -1516,6 +1554,7 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kAWindowPair: return launch_mode<kAWindowPair>(bn, ta, tb, ty, p, st);
     case kAIm2win: return launch_mode<kAIm2win>(bn, ta, tb, ty, p, st);
     case kAStrided: return launch_mode<kAStrided>(bn, ta, tb, ty, p, st);
+    case kATmaGatherPair: return launch_mode<kATmaGatherPair>(bn, ta, tb, ty, p, st);
     case kANarrowWin: return launch_mode<kANarrowWin>(bn, ta, tb, ty, p, st);
     case kAPlane: return launch_mode<kAPlane>(bn, ta, tb, ty, p, st);
     case kAPlane3: return launch_mode<kAPlane3>(bn, ta, tb, ty, p, st);

@@ -138,6 +138,8 @@ enum AMode : int {
     kAStrided = 11,   // 1x1 stride-s unpadded layers: A read from x itself by 4-D TMA boxes
                       // with element strides (1, s, s, 1), only the pixels the output
                       // uses; tiles of whole output rows of one image
+    kATmaGatherPair = 12,  // TMA gather4 on a cluster of two CTAs (tcgen05.mma.cta_group::2,
+                           // 256 rows); each CTA holds half of the weight columns
 };
 // Dynamic shared memory of one implicit-GEMM CTA, and the deepest ring that fits
 // (0 when none does).

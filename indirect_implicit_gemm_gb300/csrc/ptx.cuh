@@ -411,6 +411,20 @@ __device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// tile::gather4 into this CTA's shared memory, bytes completing on an mbarrier
+// of either CTA of the pair (bar is a shared::cluster address).
+__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster_addr, int c0, int r0,
+                                                 int r1, int r2, int r3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c0), "r"(r0), "r"(r1),
+        "r"(r2), "r"(r3)
+        : "memory");
+}
+
 // TMEM allocation shared by the pair: one warp of each CTA executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols)
 {

@@ -95,6 +95,11 @@ SMALL = [
       seed=49),
     S("strided_1x1_s2_cout300", N=2, C_in=128, H=12, W=16, C_out=300, KH=1, KW=1, stride=2,
       pad=0, seed=50),
+    # TMA gather on a CTA pair (256-wide column tiles): an odd tile count (the
+    # last pair's second CTA gathers zeros) and two ragged column tiles
+    S("tmagather_pair_c64_s2", N=4, C_in=64, H=18, W=20, C_out=256, stride=2, pad=1, seed=51),
+    S("tmagather_pair_c128_cout300", N=8, C_in=128, H=11, W=9, C_out=300, stride=2, pad=1,
+      seed=52),
 ]
 
 
