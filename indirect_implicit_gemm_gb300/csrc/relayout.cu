@@ -178,6 +178,64 @@ __global__ void __launch_bounds__(kThreads) im2win_padded_kernel(
     for (int v = threadIdx.x; v < out_vecs; v += blockDim.x) out[v] = outs[v];
 }
 
+// The same re-layout for compile-time KH and C_in (the 3-channel stems): each
+// thread assembles one column's KC values in registers, all indices static,
+// and writes it with 16-byte stores; the output needs no shared memory.
+X
+
+template <int KH_, int C_>
+__global__ void __launch_bounds__(kRowThreads) im2win_padded_fixed_kernel(
+    const uint16_t* __restrict__ x, uint16_t* __restrict__ win, int H, int W, int s, int p,
+    int H_out, int W_used)
+{
+    constexpr int KC = (KH_ * C_ + 7) / 8 * 8;
+    extern __shared__ uint4 smem_v[];  // rows [KH_][W*C_]
+    uint16_t* rows = reinterpret_cast<uint16_t*>(smem_v);
+    const int g = blockIdx.x;
+    const int n = g / H_out, ho = g - n * H_out;
+    const int rowlen = W * C_;
+    bool row_in[KH_];
+#pragma unroll
+    for (int kh = 0; kh < KH_; ++kh) {
+        const int h = ho * s - p + kh;
+        row_in[kh] = h >= 0 && h < H;
+        if (!row_in[kh]) continue;
+        const uint16_t* src = x + (static_cast<long long>(n) * H + h) * rowlen;
+        uint16_t* dst = rows + kh * rowlen;
+        if ((rowlen & 7) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+            for (int i = threadIdx.x; i < rowlen / 8; i += blockDim.x)
+                reinterpret_cast<uint4*>(dst)[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+        } else {
+            for (int i = threadIdx.x; i < rowlen; i += blockDim.x) dst[i] = src[i];
+        }
+    }
+    __syncthreads();
+    uint4* out = reinterpret_cast<uint4*>(win + static_cast<long long>(g) * W_used * KC);
+    for (int wc = threadIdx.x; wc < W_used; wc += blockDim.x) {
+        const int w = wc - p;
+        const bool inside = w >= 0 && w < W;
+        uint32_t e[KC / 2];
+#pragma unroll
+        for (int i = 0; i < KC / 2; ++i) e[i] = 0u;
+        if (inside) {
+#pragma unroll
+            for (int kh = 0; kh < KH_; ++kh) {
+                if (!row_in[kh]) continue;
+                const uint16_t* rp = rows + kh * rowlen + w * C_;
+#pragma unroll
+                for (int ci = 0; ci < C_; ++ci) {
+                    const int k = kh * C_ + ci;
+                    e[k / 2] |= static_cast<uint32_t>(rp[ci]) << (16 * (k & 1));
+                }
+            }
+        }
+        uint4* col = out + wc * (KC / 8);
+#pragma unroll
+        for (int v = 0; v < KC / 8; ++v)
+            col[v] = make_uint4(e[4 * v], e[4 * v + 1], e[4 * v + 2], e[4 * v + 3]);
+    }
+}
+
 // Weights [C_out][KH][KW][C_in] -> [C_out][KW*KC] in the im2win path's K order
 // (kw, kh, ci), each kw slice padded with zeros from KH*C_in to KC.
 __global__ void __launch_bounds__(kThreads) pack_im2win_weights_kernel(
@@ -203,7 +261,17 @@ cudaError_t launch_im2win_padded(const ConvShape& c, int KC, const uint16_t* x, 
                                  cudaStream_t st)
 {
     const int W_used = (c.W_out - 1) * c.s + (c.KW - 1) * c.d + 1;
-    const int smem = W_used * KC * 2 + (c.KH * c.W * c.C_in * 2 + 15) / 16 * 16;
+    const int rows_smem = (c.KH * c.W * c.C_in * 2 + 15) / 16 * 16;
+    if (c.C_in == 3 && (c.KH == 7 || c.KH == 11)) {
+        if (c.KH == 7)
+            im2win_padded_fixed_kernel<7, 3><<<c.N * c.H_out, kRowThreads, rows_smem, st>>>(
+                x, win, c.H, c.W, c.s, c.p, c.H_out, W_used);
+        else
+            im2win_padded_fixed_kernel<11, 3><<<c.N * c.H_out, kRowThreads, rows_smem, st>>>(
+                x, win, c.H, c.W, c.s, c.p, c.H_out, W_used);
+        return cudaGetLastError();
+    }
+    const int smem = W_used * KC * 2 + rows_smem;
     im2win_padded_kernel<<<c.N * c.H_out, kThreads, smem, st>>>(x, win, c.H, c.W, c.C_in, c.KH,
                                                                 c.s, c.p, c.H_out, W_used, KC);
     return cudaGetLastError();
