@@ -38,7 +38,14 @@ constexpr int kGatherWarps = 4;
 // the 64->128 3x3 layer).
 constexpr int kTmaWarp = kEpiWarps + kGatherWarps;  // 8
 constexpr int kMmaWarp = kTmaWarp + 1;              // 9
-constexpr int kThreads = (kMmaWarp + 1) * 32;       // 320
+// Waits on the stage and accumulator barriers for the MMA warp and hands each
+// stage over at a named barrier: an mbarrier wait on the MMA-issuing warp
+// stalls it until the MMAs already queued have drained (probe: +140 to +240
+// cycles per stage at N <= 128), while a named-barrier hand-off costs nothing.
+constexpr int kWaitWarp = kMmaWarp + 1;             // 10
+constexpr int kThreads = (kWaitWarp + 1) * 32;      // 352
+constexpr uint32_t kHandBar = 2;                    // named barrier of the hand-off
+constexpr uint32_t kHandThreads = 64;               // the MMA warp and the wait warp
 constexpr int kGatherThreads = kGatherWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kRowsPerGatherThread = BM * (BK / 8) / kGatherThreads;  // 8
@@ -56,7 +63,7 @@ constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kSmemLimit = 232448;    // opt-in dynamic shared memory per block
 constexpr int kMaxAcc = 4;
 constexpr int kMaxSlots = 4;  // narrow window: staged-row slots
-static_assert((4 * kMaxStages + 2 * kMaxAcc + 2 + 2 * kMaxSlots) * 8 + 8 + 36 <= kHeaderBytes,
+static_assert((4 * kMaxStages + 2 * kMaxAcc + 2 + 2 * kMaxSlots) * 8 + 8 + 36 + 8 <= kHeaderBytes,
               "header area");
 
 template <int BN>
@@ -350,6 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sBias = reinterpret_cast<float*>(sEpi + p.epi_bufs * kEpiTileBytes);
     uint32_t* sVote = reinterpret_cast<uint32_t*>(abort_flag + 1);  // up to 8 epilogue-warp votes
     volatile uint32_t* sTilesDone = sVote + 8;  // tiles the epilogue has finished (plane prefetch)
+    // wait warp -> MMA warp: 1 if the awaited barrier completed, 0 to unwind; two
+    // words used alternately, so a word is rewritten only after the MMA warp has
+    // passed the next hand-off and therefore has read it
+    volatile uint32_t* sHand = sTilesDone + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1058,7 +1069,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Make sure no MMA is still reading shared memory or writing TMEM.
             ptx::mma_commit(drain);
             drain_wait(drain, 0, 1000000000ull);
-        } else if (lane == 0 && rank == 0) {
+        } else if (!PLANE && rank == 0) {
+            // The whole warp walks the units; lane 0 issues.  Every barrier wait
+            // is done by the wait warp, which hands each one over at kHandBar
+            // with its outcome (the same sequence: weights, then per tile the
+            // accumulator and each K block).
             // (in a pair only CTA 0 issues: each MMA covers both CTAs' 128 rows)
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
             const uint64_t a_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
@@ -1066,15 +1081,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a_slot_step = AST >> 4;
             constexpr uint32_t b_blk_step = BB >> 4;
             const uint32_t col_step = static_cast<uint32_t>(p.win_d * 8);  // window: kw + 1
+            uint32_t hand = 0;
+            auto receive = [&]() -> bool {
+                ptx::named_barrier_sync(kHandBar, kHandThreads);
+                const bool good = sHand[hand & 1u] != 0u;
+                ++hand;
+                return good;
+            };
             Ring ring;
-            uint32_t lt = 0;
-            bool ok = !p.bres || wait_bar(bres_full, 0u, wc, kRoleMma);
+            bool ok = receive();  // resident weights (or nothing to wait for)
             Ring ar;
-            for (int tile = t_first; ok && tile < total_tiles;
-                 tile += t_step, ++lt, ar.next(C::kAcc)) {
+            for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
                 const Unit u = unit_of<BN, PAIR>(p, tile, rank);
                 const uint32_t acc = ar.stage;
-                if (!wait_bar(&tempty[acc], ar.phase ^ 1u, wc, kRoleMma, PAIR)) break;
+                if (!receive()) break;  // accumulator drained by the epilogue
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 // window mode: (kh, cc) of the K block, walked instead of divided
@@ -1084,72 +1104,109 @@ __global__ void __launch_bounds__(kThreads, 1)
                     win_cc = u.kb0 - win_kh * p.win_cc;
                 }
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
-                    if (GATHER && !wait_bar(&full_a[ring.stage], ring.phase, wc, kRoleMma)) {
+                    if (!receive()) {  // the stage's A and B have landed
                         ok = false;
                         break;
                     }
-                    if ((!GATHER || !p.bres) &&
-                        !wait_bar(&full_b[ring.stage], ring.phase, wc, kRoleMma)) {
-                        ok = false;
-                        break;
-                    }
-                    // Thread-written A stages (cp.async, st.shared) are read by the
-                    // tensor core through the async proxy.
-                    if (AMODE == kAGather || AMODE == kANarrow || NARROWWIN)
-                        ptx::fence_proxy_async_smem();
-                    ptx::tc_fence_after();
-                    // Descriptors as slot bases plus 16-byte-unit offsets: no
-                    // division or address arithmetic between MMA groups.
-                    const uint64_t ad = a_desc0 + ring.stage * a_slot_step;
-                    if (WINDOW) {
-                        // One staged (kh, cc) block feeds every kw tap: tap kw reads
-                        // the staging rows shifted down by kw*d.
-                        const uint64_t bd0 =
-                            p.bres ? b_desc0 + static_cast<uint32_t>(win_kh * p.win_kw * p.win_cc +
-                                                                     win_cc) *
-                                                   b_blk_step
-                                   : b_desc0 + ring.stage * p.b_per_stage * b_blk_step;
-                        const uint32_t bstep = p.bres ? p.win_cc * b_blk_step : b_blk_step;
-                        const uint32_t first = kb != u.kb0 ? 1u : 0u;
-                        if (p.win_kw == 3) {
+                    if (lane == 0) {
+                        // Thread-written A stages (cp.async, st.shared) are read by the
+                        // tensor core through the async proxy.
+                        if (AMODE == kAGather || AMODE == kANarrow || NARROWWIN)
+                            ptx::fence_proxy_async_smem();
+                        ptx::tc_fence_after();
+                        // Descriptors as slot bases plus 16-byte-unit offsets: no
+                        // division or address arithmetic between MMA groups.
+                        const uint64_t ad = a_desc0 + ring.stage * a_slot_step;
+                        if (WINDOW) {
+                            // One staged (kh, cc) block feeds every kw tap: tap kw reads
+                            // the staging rows shifted down by kw*d.
+                            const uint64_t bd0 =
+                                p.bres ? b_desc0 + static_cast<uint32_t>(win_kh * p.win_kw * p.win_cc +
+                                                                         win_cc) *
+                                                       b_blk_step
+                                       : b_desc0 + ring.stage * p.b_per_stage * b_blk_step;
+                            const uint32_t bstep = p.bres ? p.win_cc * b_blk_step : b_blk_step;
+                            const uint32_t first = kb != u.kb0 ? 1u : 0u;
+                            if (p.win_kw == 3) {
 #pragma unroll
-                            for (int kw = 0; kw < 3; ++kw)
+                                for (int kw = 0; kw < 3; ++kw)
 #pragma unroll
-                                for (int kk = 0; kk < BK / 16; ++kk)
-                                    mma_issue<PAIR>(d_tmem, ad + kw * col_step + 2 * kk,
-                                                  bd0 + kw * bstep + 2 * kk, idesc,
-                                                  (kw != 0 || kk != 0) ? 1u : first);
+                                    for (int kk = 0; kk < BK / 16; ++kk)
+                                        mma_issue<PAIR>(d_tmem, ad + kw * col_step + 2 * kk,
+                                                      bd0 + kw * bstep + 2 * kk, idesc,
+                                                      (kw != 0 || kk != 0) ? 1u : first);
+                            } else {
+                                for (int kw = 0; kw < p.win_kw; ++kw)
+#pragma unroll
+                                    for (int kk = 0; kk < BK / 16; ++kk)
+                                        mma_issue<PAIR>(d_tmem, ad + kw * col_step + 2 * kk,
+                                                      bd0 + kw * bstep + 2 * kk, idesc,
+                                                      (kw != 0 || kk != 0) ? 1u : first);
+                            }
                         } else {
-                            for (int kw = 0; kw < p.win_kw; ++kw)
+                            const uint64_t bd =
+                                b_desc0 + (p.bres ? static_cast<uint32_t>(kb) : ring.stage) * b_blk_step;
+                            // The last K block may hold fewer than 64 columns: skip the
+                            // all-zero 16-column steps.
+                            const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
 #pragma unroll
-                                for (int kk = 0; kk < BK / 16; ++kk)
-                                    mma_issue<PAIR>(d_tmem, ad + kw * col_step + 2 * kk,
-                                                  bd0 + kw * bstep + 2 * kk, idesc,
-                                                  (kw != 0 || kk != 0) ? 1u : first);
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                if (kk < ksteps)
+                                    mma_issue<PAIR>(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
+                                                  (kb != u.kb0 || kk != 0) ? 1u : 0u);
                         }
-                        if (++win_cc == p.win_cc) {
-                            win_cc = 0;
-                            ++win_kh;
-                        }
-                    } else {
-                        const uint64_t bd =
-                            b_desc0 + (p.bres ? static_cast<uint32_t>(kb) : ring.stage) * b_blk_step;
-                        // The last K block may hold fewer than 64 columns: skip the
-                        // all-zero 16-column steps.
-                        const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            if (kk < ksteps)
-                                mma_issue<PAIR>(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
-                                              (kb != u.kb0 || kk != 0) ? 1u : 0u);
+                        mma_commit_to<PAIR>(&empty[ring.stage]);
                     }
-                    mma_commit_to<PAIR>(&empty[ring.stage]);
+                    __syncwarp();
+                    if (WINDOW && ++win_cc == p.win_cc) {
+                        win_cc = 0;
+                        ++win_kh;
+                    }
                 }
-                if (ok) mma_commit_to<PAIR>(&tfull[acc]);
+                if (ok && lane == 0) mma_commit_to<PAIR>(&tfull[acc]);
+                __syncwarp();
             }
             // Make sure no MMA is still reading shared memory or writing TMEM.
-            mma_commit_to<PAIR>(drain, false);
-            drain_wait(drain, 0, 1000000000ull);
+            if (lane == 0) {
+                mma_commit_to<PAIR>(drain, false);
+                drain_wait(drain, 0, 1000000000ull);
+            }
+            __syncwarp();
+        }
+    } else if (warp == kWaitWarp) {
+        // ------------------------------------------------------------ barrier waits
+        // Mirrors the MMA warp's walk (non-plane modes): lane 0 waits, the warp
+        // hands the outcome over; a failed wait is handed over too, and both
+        // warps leave their loops at that same hand-off.
+        if (!PLANE && rank == 0) {
+            uint32_t hand = 0;
+            auto waited = [&](uint64_t* bar, uint32_t parity, bool cluster) -> bool {
+                uint32_t good = 0u;
+                if (lane == 0) good = wait_bar(bar, parity, wc, kRoleMma, cluster) ? 1u : 0u;
+                return __shfl_sync(0xffffffffu, good, 0) != 0u;
+            };
+            auto send = [&](bool good) -> bool {
+                if (lane == 0) sHand[hand & 1u] = good ? 1u : 0u;
+                ++hand;
+                ptx::named_barrier_sync(kHandBar, kHandThreads);
+                return good;
+            };
+            Ring ring;
+            bool ok = send(!p.bres || waited(bres_full, 0u, false));
+            Ring ar;
+            for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                if (!send(waited(&tempty[ar.stage], ar.phase ^ 1u, PAIR))) break;
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
+                    bool good = !GATHER || waited(&full_a[ring.stage], ring.phase, false);
+                    if (good && (!GATHER || !p.bres))
+                        good = waited(&full_b[ring.stage], ring.phase, false);
+                    if (!send(good)) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
         }
     } else if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
