@@ -497,12 +497,15 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         g.n_tiles = (c.C_out + g.bn - 1) / g.bn;
         // Two CTAs per MMA (256 rows) for 256-wide column tiles: each holds half
         // of the weight columns, so each SM reads half of B per MMA and a slot of
-        // streamed weights takes half the shared memory.  (Narrower tiles stay on
-        // one CTA: measured, their time is set by the epilogue, which the pair
-        // does not shorten.)
-        g.pair = (g.bn == 256 && g.m_tiles >= 2) ? 1 : 0;
-        auto bnb = [&] { return g.pair ? g.bn / 2 : g.bn; };
+        // streamed weights takes half the shared memory.  128-wide tiles go to a
+        // pair only when one CTA could not keep the weights resident (measured:
+        // 97 -> 92 us on the 128-channel 3x3 layer at 56x56; with the weights
+        // resident on one CTA, as on the 64->128 layer, the pair is slower).
         const int all_kb = c.KH * c.KW * (c.C_in / 64);
+        const bool solo_bres =
+            g.n_tiles == 1 && igemm_pick_stages(g.bn, 1, all_kb, g.a_stage_bytes, 1) >= 3;
+        g.pair = (g.m_tiles >= 2 && (g.bn == 256 || (g.bn == 128 && !solo_bres))) ? 1 : 0;
+        auto bnb = [&] { return g.pair ? g.bn / 2 : g.bn; };
         if (g.n_tiles == 1 && igemm_pick_stages(bnb(), 1, all_kb, g.a_stage_bytes, 1) >= 3) {
             g.bres = 1;
             g.b_per_stage = 1;

@@ -422,6 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Up to here only this CTA's shared memory, TMEM and the kernel parameters
+    // were touched.  Launched with programmatic stream serialization, the CTA
+    // may have started while the previous kernel on the stream still runs on
+    // other SMs: every global read or write below follows that kernel.  The
+    // next kernel may begin launching at once; it waits for this one the same
+    // way, so only its prologue overlaps this kernel's last tiles.
+    ptx::grid_dependency_wait();
+    if (threadIdx.x == 0) ptx::grid_launch_dependents();
 
     const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
     const int total_tiles = p.m_tiles * p.n_tiles * p.splits;
@@ -1518,27 +1526,36 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         (p.x_KH != 3 || p.win_kw != 3 || p.pl_u != (AMODE == kAPlane3U2 ? 2 : 1)))
         return cudaErrorInvalidValue;
     const int tiles = p.m_tiles * p.n_tiles * p.splits;  // pair mode: pair units
+    // Programmatic stream serialization: CTAs may start on SMs the previous
+    // kernel has left while its other CTAs finish (the kernel waits for it
+    // before touching global memory).
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (kPairMode) {
         if (BN < 64) return cudaErrorInvalidValue;
         // Clusters of two CTAs, as many as can be resident at once (two SMs each).
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-        cfg.stream = st;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         int resident = 0;
         {
             std::lock_guard<std::mutex> lock(mu);
             if (cluster_smem[dev] != smem || cluster_count[dev] < 1) {
                 int nc = 0;
-                cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2));
-                if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess || nc < 1) {
+                cudaLaunchConfig_t occ = cfg;  // the cluster shape alone
+                occ.attrs = attr + 1;
+                occ.numAttrs = 1;
+                occ.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2));
+                if (cudaOccupancyMaxActiveClusters(&nc, kern, &occ) != cudaSuccess || nc < 1) {
                     (void)cudaGetLastError();
                     nc = num_sms() / 2;
                 }
@@ -1554,7 +1571,9 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         return cudaGetLastError();
     }
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    kern<<<grid, kThreads, smem, st>>>(ta, tb, ty, p);
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

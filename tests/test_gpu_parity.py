@@ -100,6 +100,11 @@ SMALL = [
     S("tmagather_pair_c64_s2", N=4, C_in=64, H=18, W=20, C_out=256, stride=2, pad=1, seed=51),
     S("tmagather_pair_c128_cout300", N=8, C_in=128, H=11, W=9, C_out=300, stride=2, pad=1,
       seed=52),
+    # window path on a CTA pair with 128-wide column tiles (weights too large to
+    # stay resident on one CTA): resident halves, then streamed halves with an
+    # odd tile count and a ragged column tile
+    S("window_pair128_c128", N=3, C_in=128, H=12, W=12, C_out=128, seed=53),
+    S("window_pair128_c192_cout100_odd", N=1, C_in=192, H=25, W=9, C_out=100, seed=54),
 ]
 
 
@@ -273,3 +278,46 @@ def test_wait_timeout_is_reported_not_hung(gpu_lib):
     assert st == 0
     got, ref, mag = run_full(gpu_lib, SMALL[0])
     check(got, ref, mag, "after timeout")
+
+
+def test_dependent_layers_back_to_back(gpu_lib):
+    """A chain of layers on one stream with no host synchronisation: each layer
+    reads the previous layer's output and overwrites the buffer the layer
+    before it read.  The convolution kernel may start on SMs the previous
+    kernel has left (programmatic stream serialization) and must wait for that
+    kernel before touching global memory, so the chain must equal, bit for bit,
+    the same chain run with a full synchronisation after every layer (no split
+    K here: every output element has one fixed reduction order)."""
+    g = gpu_lib
+    x, _, _ = workloads.make_inputs(S("chain_x", N=2, C_in=64, H=14, W=14, C_out=64, seed=55))
+    layers = []
+    for i, (k, path) in enumerate([(3, 0), (1, 0), (3, g.PATH_GATHER), (3, 0)]):
+        sh = S("chain%d" % i, N=2, C_in=64, H=14, W=14, C_out=64, KH=k, KW=k, pad=k // 2,
+               seed=56 + i)
+        _, w, b = workloads.make_inputs(sh)
+        layers.append((sh, path, w.to(dev()), b.to(dev())))
+
+    def run(sync):
+        src = x.to(dev()).clone()
+        dst = torch.empty_like(src)
+        outs = []
+        for _ in range(3):
+            for sh, path, w, b in layers:
+                g.conv2d_fwd_path(path, src, w, b, sh.stride, sh.pad, sh.dilation, y=dst)
+                if sync:
+                    torch.cuda.synchronize()
+                    outs.append(dst.cpu())
+                src, dst = dst, src
+        torch.cuda.synchronize()
+        st, code = g.check_device_errors()
+        assert st == 0, "device error word %#x" % code
+        return src.cpu(), outs
+
+    chained, _ = run(False)
+    stepped, outs = run(True)
+    assert torch.equal(chained.view(torch.int16), stepped.view(torch.int16))
+    # the synchronised chain's last layer against the oracle on its own input
+    sh, path, w, b = layers[-1]
+    ref, mag = oracle.conv2d_direct(workloads.bits(outs[-2]), workloads.bits(w.cpu()),
+                                    workloads.bits(b.cpu()), sh.stride, sh.pad, sh.dilation)
+    check(outs[-1].float().numpy(), ref, mag, "chain, last layer")
