@@ -213,16 +213,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 // Row-major bf16 matrix [rows][cols] (cols contiguous), box [box_rows][64 cols],
 // 128-byte swizzle: exactly the K-major operand tile the MMA descriptors expect.
-bool encode_kmajor(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows)
+bool encode_kmajor(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows,
+                   bool narrow = false)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    // narrow: boxes of 32 columns (64-byte rows, 64-byte swizzle)
+    cuuint32_t box[2] = {narrow ? 32u : 64u, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -303,6 +306,7 @@ struct GemmPlan {
     int nw_slots = 0;
     int tma_store = 0;             // epilogue through a staging tile and TMA stores
     int epi_bufs = 1;              // staging tiles of that epilogue
+    int epi_c32 = 0;               // 1: 32-column chunks, 8 KB staging tiles
     int pl_u = 1, pl_nacc = 0, b_stages = 0;  // plane mode: sub-tiles, accumulators, B slots
     int pair = 0;                  // window mode on a CTA pair (each CTA holds bn/2 columns of B)
     long long M = 0, K = 0;
@@ -353,6 +357,24 @@ void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
     if (s2 >= 4 && s2 >= s - 1) {
         g.stages = s2;
         g.epi_bufs = 2;
+        return;
+    }
+    // A staging tile of 32-column chunks (half the bytes) when that buys one
+    // more ring stage and the tile's MMAs take long enough to hide the four
+    // serialised chunk stores (eight-warp epilogue modes only).  Measured: the
+    // 128-channel 3x3 layer at 56x56 (72 MMAs per tile, three to four stages)
+    // goes from 90.8 to 84.8 us; the 64->128 layer (36 MMAs per tile) slows
+    // from 17.1 to 18.4 us, so tiles below 64 MMAs keep 64-column chunks.
+    const bool window = g.amode == kAWindow || g.amode == kAWindowPair;
+    const bool epi8 = window || g.amode == kADense || g.amode == kAIm2win || g.amode == kAStrided;
+    const int mmas_per_tile = 4 * g.num_kb * (window ? c.KW : 1);
+    const int s3 = (epi8 && mmas_per_tile >= 64)
+                       ? igemm_pick_stages(bnb, g.bres, kb_res, g.a_stage_bytes, g.b_per_stage,
+                                           g.extra_smem + kEpiNarrowStageBytes)
+                       : 0;
+    if (s3 > s) {
+        g.stages = s3;
+        g.epi_c32 = 1;
     }
 }
 
@@ -735,7 +757,8 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
                                  ? g.win_rows * a.shape->W_out
                              : plane                             ? a.shape->W_out
                                                                  : 128;
-        if (!encode_kmajor(&out->ty, a.y, g.M, a.C_out, box_rows)) return CONVGB_ERR_CUDA;
+        if (!encode_kmajor(&out->ty, a.y, g.M, a.C_out, box_rows, g.epi_c32 != 0))
+            return CONVGB_ERR_CUDA;
     }
     unsigned* err = device_error_word();
     if (!err) return CONVGB_ERR_CUDA;
@@ -765,6 +788,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     p.ntile_div = FastDiv((uint32_t)g.n_tiles);
     p.tma_store = g.tma_store;
     p.epi_bufs = g.epi_bufs;
+    p.epi_c32 = g.epi_c32;
     p.stages = g.stages;
     p.bres = g.bres;
     p.m_step = g.m_step;

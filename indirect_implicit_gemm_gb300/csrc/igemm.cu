@@ -354,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA-store epilogue: a 128 x 64 bf16 staging tile (128-byte swizzle) and the
     // current column tile's bias in fp32.
     uint8_t* sEpi = sStg + (NARROWWIN ? NS * p.nw_slot_bytes : 0);
-    float* sBias = reinterpret_cast<float*>(sEpi + p.epi_bufs * kEpiTileBytes);
+    const int epi_tile = p.epi_c32 ? kEpiNarrowTileBytes : kEpiTileBytes;  // staging tile bytes
+    float* sBias = reinterpret_cast<float*>(sEpi + p.epi_bufs * epi_tile);
     uint32_t* sVote = reinterpret_cast<uint32_t*>(abort_flag + 1);  // up to 8 epilogue-warp votes
     volatile uint32_t* sTilesDone = sVote + 8;  // tiles the epilogue has finished (plane prefetch)
     // wait warp -> MMA warp: 1 if the awaited barrier completed, 0 to unwind; two
@@ -507,6 +508,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t taddr = tbase + static_cast<uint32_t>(sub * BN);
                 const bool live = m < p.M;
+                if (EPI8 && p.tma_store && p.epi_c32) {
+                    // Narrow staging: 32-column chunks in a 128 x 64-byte tile, 64-byte
+                    // swizzle (16-byte piece q of staged row s sits at q ^ ((s >> 1) & 3));
+                    // warp w converts the 16-column half w / 4 of each chunk.
+#pragma unroll 1
+                    for (int ch = 0; ch < BN / 32; ++ch) {
+                        uint32_t ra[16];
+                        ptx::tmem_ld_32x32b_x16(taddr + ch * 32 + half * 16, ra);
+                        ptx::tmem_ld_wait();
+                        if (last_sub && ch + 1 == BN / 32) release_acc(acc);
+                        uint8_t* sE = sEpi + ((p.epi_bufs == 2) ? (echunk & 1u) : 0u) * kEpiNarrowTileBytes;
+                        ++echunk;
+                        if (et == 0) {
+                            if (p.epi_bufs == 2)
+                                ptx::bulk_wait_read_1();
+                            else
+                                ptx::bulk_wait_read_all();
+                        }
+                        ptx::named_barrier_sync(1, kEpiN);
+                        const float4* bs = reinterpret_cast<const float4*>(sBias + ch * 32);
+                        const int srow = ROWTILES ? wrow * p.win_wout + wcol : r;
+                        const bool keep = !ROWTILES || (wcol < p.win_wout && wrow < p.win_rows);
+                        if (keep) {
+#pragma unroll
+                            for (int qq = 0; qq < 2; ++qq) {
+                                const int q = 2 * half + qq;  // 16-byte piece of the row
+                                const uint32_t* src = ra + 8 * qq;
+                                const float4 b0 = bs[2 * q], b1 = bs[2 * q + 1];
+                                uint4 v;
+                                v.x = pack_bf16x2(__uint_as_float(src[0]) + b0.x,
+                                                  __uint_as_float(src[1]) + b0.y);
+                                v.y = pack_bf16x2(__uint_as_float(src[2]) + b0.z,
+                                                  __uint_as_float(src[3]) + b0.w);
+                                v.z = pack_bf16x2(__uint_as_float(src[4]) + b1.x,
+                                                  __uint_as_float(src[5]) + b1.y);
+                                v.w = pack_bf16x2(__uint_as_float(src[6]) + b1.z,
+                                                  __uint_as_float(src[7]) + b1.w);
+                                *reinterpret_cast<uint4*>(sE + srow * 64 +
+                                                          ((q ^ ((srow >> 1) & 3)) << 4)) = v;
+                            }
+                        }
+                        ptx::fence_proxy_async_smem();
+                        ptx::named_barrier_sync(1, kEpiN);
+                        if (et == 0) {
+                            const int c0 = u.n0 + ch * 32;
+                            if (ROWTILES) {
+                                if (u.m0 < p.win_groups)
+                                    ptx::tma_store_2d(&tmap_y, sE, c0, u.m0 * p.win_wout);
+                            } else {
+                                ptx::tma_store_2d(&tmap_y, sE, c0, u.m0);
+                            }
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                    continue;
+                }
                 if (p.tma_store) {
 #pragma unroll 1
                     for (int c64 = 0; c64 < BN / 64; ++c64) {
@@ -1507,7 +1564,9 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         }
     }
     const int extra = (AMODE == kANarrowWin ? p.nw_slots * p.nw_slot_bytes : 0) +
-                      (p.tma_store ? kEpiStageBytes + (p.epi_bufs - 1) * kEpiTileBytes : 0);
+                      (p.tma_store ? (p.epi_c32 ? kEpiNarrowStageBytes + (p.epi_bufs - 1) * kEpiNarrowTileBytes
+                                                : kEpiStageBytes + (p.epi_bufs - 1) * kEpiTileBytes)
+                                   : 0);
     constexpr bool kPlane = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     constexpr bool kPairMode = AMODE == kAWindowPair || AMODE == kATmaGatherPair;
     const int smem =
@@ -1517,6 +1576,10 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
             : igemm_smem_bytes(kPairMode ? BN / 2 : BN, p.stages, p.bres, p.kb_total,
                                p.a_stage_bytes, p.b_per_stage, extra);
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
+    // 32-column staging exists for the eight-warp epilogue only
+    constexpr bool kEpi8 = AMODE == kAWindow || AMODE == kAWindowPair || AMODE == kADense ||
+                           AMODE == kAIm2win || AMODE == kAStrided;
+    if (p.epi_c32 && !(kEpi8 && p.tma_store)) return cudaErrorInvalidValue;
     if (kPlane &&
         ((!p.bres && (p.b_stages < 2 || p.b_stages > kMaxStages)) || p.pl_u < 1 || p.pl_u > 2 ||
          p.pl_nacc < 1 || p.pl_nacc > kMaxAcc || p.pl_nacc * p.pl_u * BN > 512))

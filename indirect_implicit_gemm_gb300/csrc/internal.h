@@ -89,6 +89,7 @@ struct IgemmParams {
     FastDiv hp_div;          // divides a virtual row index by H + 2p
     int tma_store;           // 1: epilogue stages 64-column chunks in shared memory and
                              //    stores them with TMA (bf16 y, C_out % 8 == 0, no split)
+    int epi_c32;             // TMA-store epilogue: 1 = 32-column chunks (8 KB staging tiles)
     int epi_bufs;            // TMA-store epilogue: staging tiles (2: chunk k+1 is staged
                              //    while chunk k's store still reads its tile)
     int bres;                // 1: all of W's single column tile resident in shared memory
@@ -160,6 +161,9 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& tmap_a,
 // and the column tile's bias; a second staging tile when double-buffered.
 constexpr int kEpiTileBytes = 16384;
 constexpr int kEpiStageBytes = kEpiTileBytes + 1024;
+// Narrow staging: 32-column chunks, a 128 x 64-byte tile with 64-byte swizzle.
+constexpr int kEpiNarrowTileBytes = 8192;
+constexpr int kEpiNarrowStageBytes = kEpiNarrowTileBytes + 1024;
 cudaError_t launch_finish_split(const float* partial, const uint16_t* bias, void* y, long long M,
                                 int C_out, int y_f32, cudaStream_t st);
 cudaError_t launch_selftest_timeout(unsigned long long timeout_ns, unsigned* err,

@@ -105,6 +105,10 @@ SMALL = [
     # odd tile count and a ragged column tile
     S("window_pair128_c128", N=3, C_in=128, H=12, W=12, C_out=128, seed=53),
     S("window_pair128_c192_cout100_odd", N=1, C_in=192, H=25, W=9, C_out=100, seed=54),
+    # 32-column epilogue staging (64-byte swizzle), taken when it buys a ring
+    # stage on tiles of at least 64 MMAs (a ragged last chunk in the second)
+    S("window_c128_narrow_staging", N=1, C_in=128, H=30, W=30, C_out=128, seed=57),
+    S("window_c128_cout120_narrow_staging", N=2, C_in=128, H=20, W=22, C_out=120, seed=58),
 ]
 
 
