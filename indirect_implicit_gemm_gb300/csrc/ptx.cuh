@@ -400,6 +400,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr)
                  : "memory");
 }
 
+// `count` arrivals at once on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster_count(uint32_t bar_cluster_addr, uint32_t count)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                     bar_cluster_addr),
+                 "r"(count)
+                 : "memory");
+}
+
 // try_wait with acquire at cluster scope: the phase was completed by arrivals
 // from the peer CTA.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity)
