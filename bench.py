@@ -313,25 +313,23 @@ def time_gemm_kernel(layer, steps, warmup, stream):
 
 
 def time_e2e(g, c, steps, warmup, dev, stream):
-    """conv2d_fwd from pinned host buffers: H2D inputs, compute, D2H output, per step."""
+    """conv2d_fwd_host (the C ABI's host-buffer entry point) from pinned host buffers:
+    every step copies x, w and bias in and y out, pipelined in chunks of the batch
+    against the convolution."""
     x, w, b = workloads.make_inputs(c, device=dev)
     xh = x.cpu().pin_memory()
     wh = w.cpu().pin_memory()
     bh = b.cpu().pin_memory()
     num = shape_numbers(g, c)
     out_dtype = torch.float32 if c.out_f32 else torch.bfloat16
-    yd = torch.empty((c.N, num["H_out"], num["W_out"], c.C_out), dtype=out_dtype, device=dev)
-    yh = torch.empty(yd.shape, dtype=out_dtype).pin_memory()
-    xd, wd, bd = torch.empty_like(x), torch.empty_like(w), torch.empty_like(b)
-    ws = torch.empty(max(num["workspace_bytes"], 1), dtype=torch.uint8, device=dev)
+    yh = torch.empty((c.N, num["H_out"], num["W_out"], c.C_out), dtype=out_dtype).pin_memory()
+    scratch = torch.empty(g.conv2d_fwd_host_scratch_size(
+        c.N, c.C_in, c.H, c.W, c.C_out, c.KH, c.KW, c.stride, c.pad, c.dilation, out_dtype, True),
+        dtype=torch.uint8, device=dev)
 
     def one(_):
-        xd.copy_(xh, non_blocking=True)
-        wd.copy_(wh, non_blocking=True)
-        bd.copy_(bh, non_blocking=True)
-        g.conv2d_fwd(xd, wd, bd, c.stride, c.pad, c.dilation, out_dtype=out_dtype, y=yd,
-                     workspace=ws)
-        yh.copy_(yd, non_blocking=True)
+        g.conv2d_fwd_host(xh, wh, bh, c.stride, c.pad, c.dilation, out_dtype=out_dtype, y=yh,
+                          scratch=scratch)
 
     for i in range(warmup):
         one(i)

@@ -22,12 +22,13 @@
  *  - Stride, padding and dilation are symmetric scalars: s >= 1, p >= 0, d >= 1.
  *    H_out = floor((H + 2p - d(KH-1) - 1)/s) + 1, likewise W_out; a shape with
  *    H_out < 1 or W_out < 1 is rejected.
- *  - Pointers named x, w, bias, y, workspace, win, ibuf are DEVICE pointers
+ *  - Pointers named x, w, bias, y, workspace, scratch, win, ibuf are DEVICE pointers
  *    owned by the caller, who must keep them alive until the work queued on
  *    `stream` has finished.  The library allocates no memory per call.
  *    They must be 16-byte aligned.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
- *    stream).  All work is queued asynchronously on it and on no other stream.
+ *    stream).  All work is queued asynchronously on it and on no other stream
+ *    (conv2d_fwd_host adds streams of its own, joined to `stream`).
  *  - Every argument, shape, alignment and workspace check happens before the
  *    first launch; a failed check returns an error and queues nothing.
  *    A failed launch returns CONVGB_ERR_CUDA.  Kernels never trap: a device-side
@@ -212,6 +213,47 @@ CONVGB_API convgb_status conv2d_fwd_noalloc(const void* x, const void* w, const 
                                             int C_in, int H, int W, int C_out, int KH, int KW,
                                             int stride, int pad, int dilation, void* y,
                                             int y_dtype, void* stream);
+
+/*
+ * conv2d_fwd_host -- conv2d_fwd with x, w and bias read from HOST memory and y
+ * written to host memory.  (An interface addition of this library, not from
+ * the pages; what it computes is conv2d_fwd's.)
+ *
+ *   x_host, w_host, bias_host (NULL for no bias), y_host
+ *             host memory, layouts and dtypes as conv2d_fwd.  Page-locked
+ *             (pinned) buffers let the copies run at full bandwidth and overlap
+ *             the computation; pageable ones work, staged by the driver.  They
+ *             must stay valid, and y_host unread, until the work queued on
+ *             `stream` has finished.  No alignment is required of them.
+ *   scratch   DEVICE memory of at least convgb_conv2d_fwd_host_scratch_size()
+ *             bytes (same shape arguments, y_dtype, and has_bias = 1 when a
+ *             bias is passed), 16-byte aligned, owned by the caller; contents
+ *             ignored on entry and unspecified on exit
+ *
+ * The batch is cut into up to four chunks of whole images.  Three streams of
+ * the library (created on first use on each device and kept until the process
+ * exits) copy chunk k+1 in, run conv2d_fwd on chunk k and copy chunk k-1 out at
+ * the same time; each chunk's input and output sit in one of two slots of the
+ * scratch.  The three streams wait for `stream` before the first copy and
+ * `stream` waits for them after the last, so the call behaves like work queued
+ * on `stream`.  Calls from several host threads on one device queue their work
+ * one call at a time.
+ *
+ * Returns CONVGB_ERR_INVALID_ARG (a NULL pointer, a bad shape or y_dtype),
+ * CONVGB_ERR_ALIGNMENT or CONVGB_ERR_WORKSPACE (the scratch) before any CUDA
+ * call; otherwise conv2d_fwd's statuses for the chunks' shapes, or
+ * CONVGB_ERR_CUDA when a copy, event or stream call fails.  On any failure
+ * after the first CUDA call, whatever was queued is still joined to `stream`.
+ */
+CONVGB_API size_t convgb_conv2d_fwd_host_scratch_size(int N, int C_in, int H, int W, int C_out,
+                                                      int KH, int KW, int stride, int pad,
+                                                      int dilation, int y_dtype, int has_bias);
+
+CONVGB_API convgb_status conv2d_fwd_host(const void* x_host, const void* w_host,
+                                         const void* bias_host, int N, int C_in, int H, int W,
+                                         int C_out, int KH, int KW, int stride, int pad,
+                                         int dilation, void* y_host, int y_dtype, void* scratch,
+                                         size_t scratch_bytes, void* stream);
 
 /* Bytes of the indirection buffer: H_out*W_out*KH*KW*4 (0 if invalid). */
 CONVGB_API size_t convgb_indirection_buffer_bytes(int H, int W, int KH, int KW, int stride, int pad,

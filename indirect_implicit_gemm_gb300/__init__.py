@@ -21,6 +21,7 @@ __all__ = [
     "indirection_buffer_bytes", "check_device_errors", "set_wait_timeout_ns",
     "selftest_wait_timeout", "ConvgbError", "PATH_AUTO", "PATH_GATHER", "PATH_DENSE",
     "PATH_STEM", "PATH_WINDOW", "PATH_PLANE", "PATH_IM2WIN", "EXPORTED_SYMBOLS", "library_path",
+    "conv2d_fwd_host", "conv2d_fwd_host_scratch_size",
 ]
 
 PATH_AUTO, PATH_GATHER, PATH_DENSE, PATH_STEM, PATH_WINDOW, PATH_PLANE, PATH_IM2WIN = (
@@ -40,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "conv2d_fwd_noalloc", "convgb_indirection_buffer_bytes",
     "build_indirection_buffer", "convgb_im2win_bytes", "im2win_transform",
     "convgb_check_device_errors", "convgb_set_wait_timeout_ns", "convgb_selftest_wait_timeout",
-    "convgb_version",
+    "convgb_version", "convgb_conv2d_fwd_host_scratch_size", "conv2d_fwd_host",
 )
 
 
@@ -83,6 +84,10 @@ def load():
     lib.conv2d_fwd_indirect.restype = I
     lib.conv2d_fwd_noalloc.argtypes = [P, P, P] + shape10 + [P, I, P]
     lib.conv2d_fwd_noalloc.restype = I
+    lib.convgb_conv2d_fwd_host_scratch_size.argtypes = shape10 + [I, I]
+    lib.convgb_conv2d_fwd_host_scratch_size.restype = Z
+    lib.conv2d_fwd_host.argtypes = conv_args
+    lib.conv2d_fwd_host.restype = I
     lib.convgb_indirection_buffer_bytes.argtypes = [I] * 7
     lib.convgb_indirection_buffer_bytes.restype = Z
     lib.build_indirection_buffer.argtypes = [I] * 8 + [P, Z, P]
@@ -200,6 +205,61 @@ def conv2d_fwd(x, w, bias=None, stride=1, pad=0, dilation=1, out_dtype=torch.bfl
     """y = conv(x, w) + bias on the path the library picks; see include/convgb.h."""
     return conv2d_fwd_path(PATH_AUTO, x, w, bias, stride, pad, dilation, out_dtype, y,
                            workspace, stream)
+
+
+def conv2d_fwd_host_scratch_size(N, C_in, H, W, C_out, KH, KW, stride=1, pad=0, dilation=1,
+                                 out_dtype=torch.bfloat16, has_bias=True) -> int:
+    return load().convgb_conv2d_fwd_host_scratch_size(
+        N, C_in, H, W, C_out, KH, KW, stride, pad, dilation,
+        _F32 if out_dtype == torch.float32 else _BF16, 1 if has_bias else 0)
+
+
+def _need_host(t, name, dtype):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError("%s must be a host (CPU) tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous (channels-last layout)" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def conv2d_fwd_host(x, w, bias=None, stride=1, pad=0, dilation=1, out_dtype=torch.bfloat16,
+                    y=None, scratch=None, stream=None, device=None):
+    """conv2d_fwd with x, w, bias and y in host memory (pinned for overlapped copies):
+    the library copies chunks of the batch in, convolves and copies out, all queued
+    on `stream`; y is valid once that stream has finished.  See include/convgb.h."""
+    lib = load()
+    _need_host(x, "x", torch.bfloat16)
+    _need_host(w, "w", torch.bfloat16)
+    if bias is not None:
+        _need_host(bias, "bias", torch.bfloat16)
+    N, H, W, C_in = x.shape
+    C_out, KH, KW, C_in2 = w.shape
+    if C_in2 != C_in:
+        raise ValueError("x has %d channels, w expects %d" % (C_in, C_in2))
+    if bias is not None and tuple(bias.shape) != (C_out,):
+        raise ValueError("bias must have shape [C_out]")
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be bfloat16 or float32")
+    H_out, W_out = output_dims(H, W, KH, KW, stride, pad, dilation)
+    if y is None:
+        y = torch.empty((N, H_out, W_out, C_out), dtype=out_dtype, pin_memory=True)
+    else:
+        _need_host(y, "y", out_dtype)
+        if tuple(y.shape) != (N, H_out, W_out, C_out):
+            raise ValueError("y has shape %s, expected %s" % (tuple(y.shape),
+                                                              (N, H_out, W_out, C_out)))
+    need = conv2d_fwd_host_scratch_size(N, C_in, H, W, C_out, KH, KW, stride, pad, dilation,
+                                        out_dtype, bias is not None)
+    if scratch is None:
+        scratch = torch.empty(need, dtype=torch.uint8, device=device or "cuda")
+    elif not scratch.is_cuda:
+        raise ValueError("scratch must be a CUDA tensor")
+    st = lib.conv2d_fwd_host(_ptr(x), _ptr(w), _ptr(bias), N, C_in, H, W, C_out, KH, KW, stride,
+                             pad, dilation, _ptr(y), _F32 if out_dtype == torch.float32 else _BF16,
+                             _ptr(scratch), scratch.numel(), _stream(stream))
+    _check(st, "conv2d_fwd_host")
+    return y
 
 
 def conv2d_fwd_indirect(x, w, bias, ibuf, stride=1, pad=0, dilation=1, out_dtype=torch.bfloat16,

@@ -183,3 +183,62 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert so.im2win_transform(None, 1, 8, 8, 8, 3, 3, 1, 1, 1, P(0x1000), 1 << 20, None) == 1
     assert so.im2win_transform(P(0x1000), 1, 8, 8, 8, 3, 3, 1, 1, 1, P(0x2000), 64, None) == 3
     assert so.im2win_transform(P(0x1002), 1, 8, 8, 8, 3, 3, 1, 1, 1, P(0x2000), 1 << 20, None) == 4
+
+
+def test_host_entry_scratch_layout(lib):
+    """conv2d_fwd_host's scratch: weights, bias, two input and two output slots of
+    one chunk (the batch in up to four chunks of whole images), each rounded to
+    256 bytes, plus the convolution workspace of the largest chunk."""
+    r = lambda v: (v + 255) // 256 * 256
+
+    def per_chunk(N):
+        chunks = min(N, 4)
+        return (N + chunks - 1) // chunks
+
+    # N=32 -> 4 chunks of 8 images; the window path needs no workspace
+    n = per_chunk(32)
+    assert n == 8
+    want = r(128 * 9 * 64 * 2) + r(128 * 2) + 2 * r(n * 56 * 56 * 64 * 2) + \
+        2 * r(n * 56 * 56 * 128 * 2)
+    assert lib.conv2d_fwd_host_scratch_size(32, 64, 56, 56, 128, 3, 3, 1, 1, 1) == want
+    # no bias: no bias slot; fp32 output: output slots twice as large
+    assert lib.conv2d_fwd_host_scratch_size(32, 64, 56, 56, 128, 3, 3, 1, 1, 1,
+                                            has_bias=False) == want - r(256)
+    import torch
+    want32 = want + 2 * r(n * 56 * 56 * 128 * 4) - 2 * r(n * 56 * 56 * 128 * 2)
+    assert lib.conv2d_fwd_host_scratch_size(32, 64, 56, 56, 128, 3, 3, 1, 1, 1,
+                                            out_dtype=torch.float32) == want32
+    # N=18 -> chunks of 5 images (four chunks, the last with three)
+    n = per_chunk(18)
+    assert n == 5
+    assert lib.conv2d_fwd_host_scratch_size(18, 8, 6, 6, 8, 3, 3, 1, 1, 1) == \
+        r(8 * 9 * 8 * 2) + r(16) + 2 * r(n * 36 * 8 * 2) + 2 * r(n * 36 * 8 * 2) + \
+        r(max(lib.workspace_size(n, 8, 6, 6, 8, 3, 3, 1, 1, 1),
+              lib.workspace_size(3, 8, 6, 6, 8, 3, 3, 1, 1, 1)))
+    # invalid shapes have no scratch size
+    assert lib.conv2d_fwd_host_scratch_size(1, 8, 2, 2, 8, 3, 3, 1, 0, 1) == 0
+    assert lib.conv2d_fwd_host_scratch_size(0, 8, 8, 8, 8, 3, 3, 1, 1, 1) == 0
+
+
+def test_host_entry_rejects_bad_arguments_before_cuda(lib):
+    """No GPU here: every one of these must return before the first CUDA call."""
+    so = lib.load()
+    P = ctypes.c_void_p
+    need = lib.conv2d_fwd_host_scratch_size(2, 8, 8, 8, 8, 3, 3, 1, 1, 1)
+
+    def call(x=0x1000, w=0x2000, b=0x3000, y=0x4000, scratch=0x10000, nbytes=need, N=2,
+             dtype=0, p=1):
+        return so.conv2d_fwd_host(P(x) if x else None, P(w) if w else None,
+                                  P(b) if b else None, N, 8, 8, 8, 8, 3, 3, 1, p, 1,
+                                  P(y) if y else None, dtype, P(scratch) if scratch else None,
+                                  nbytes, None)
+
+    assert call(x=0) == 1
+    assert call(w=0) == 1
+    assert call(y=0) == 1
+    assert call(scratch=0) == 1
+    assert call(N=0) == 1
+    assert call(dtype=7) == 1
+    assert call(p=-1) == 1
+    assert call(scratch=0x10008) == 4
+    assert call(nbytes=need - 1) == 3

@@ -325,3 +325,51 @@ def test_dependent_layers_back_to_back(gpu_lib):
     ref, mag = oracle.conv2d_direct(workloads.bits(outs[-2]), workloads.bits(w.cpu()),
                                     workloads.bits(b.cpu()), sh.stride, sh.pad, sh.dilation)
     check(outs[-1].float().numpy(), ref, mag, "chain, last layer")
+
+
+HOST_SHAPES = [
+    # three chunks of 2, 2 and 1 images on the window path
+    S("host_window_n5", N=5, C_in=64, H=12, W=12, C_out=64, seed=61),
+    # the stem (im2win path, whose workspace is per chunk), fp32 output
+    S("host_stem_n3", N=3, C_in=3, H=20, W=22, C_out=16, KH=7, KW=7, stride=2, pad=3, seed=62),
+    # four chunks of one image, 1x1
+    S("host_dense_n4", N=4, C_in=32, H=9, W=7, C_out=40, KH=1, KW=1, pad=0, seed=63),
+    # four chunks of 5 images: each of the two slots is reused
+    S("host_window_n20", N=20, C_in=64, H=10, W=10, C_out=64, seed=64),
+]
+
+
+@pytest.mark.parametrize("shape", HOST_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_buffers_match_oracle(gpu_lib, shape, pinned):
+    """conv2d_fwd_host: inputs read from and output written to host memory, the
+    batch pipelined in chunks; y is valid once the stream has finished."""
+    g = gpu_lib
+    x, w, b = workloads.make_inputs(shape)
+    out_dtype = torch.float32 if "stem" in shape.name else torch.bfloat16
+    y = None
+    if pinned:
+        x, w, b = x.pin_memory(), w.pin_memory(), b.pin_memory()
+    else:
+        ho, wo = g.output_dims(shape.H, shape.W, shape.KH, shape.KW, shape.stride, shape.pad,
+                               shape.dilation)
+        y = torch.empty((shape.N, ho, wo, shape.C_out), dtype=out_dtype)
+    y = g.conv2d_fwd_host(x, w, b, shape.stride, shape.pad, shape.dilation, out_dtype=out_dtype,
+                          y=y)
+    torch.cuda.current_stream().synchronize()
+    st, code = g.check_device_errors()
+    assert st == 0, "device error word %#x" % code
+    ref, mag = oracle.conv2d_direct(workloads.bits(x), workloads.bits(w), workloads.bits(b),
+                                    shape.stride, shape.pad, shape.dilation)
+    check(y.float().numpy(), ref, mag, shape.name)
+
+
+def test_host_buffers_without_bias(gpu_lib):
+    shape = HOST_SHAPES[0]
+    x, w, _ = workloads.make_inputs(shape)
+    y = gpu_lib.conv2d_fwd_host(x.pin_memory(), w.pin_memory(), None, shape.stride, shape.pad,
+                                shape.dilation)
+    torch.cuda.current_stream().synchronize()
+    ref, mag = oracle.conv2d_direct(workloads.bits(x), workloads.bits(w), None, shape.stride,
+                                    shape.pad, shape.dilation)
+    check(y.float().numpy(), ref, mag, "host, no bias")
