@@ -7,16 +7,20 @@
 // modified GEMM reads its A rows through pointers to input pixel rows), into a
 // 128-byte-swizzled shared-memory tile; W_row tiles arrive by TMA.  The GEMM
 // itself runs on the fifth-generation tensor cores: one thread issues
-// tcgen05.mma (bf16 x bf16 -> fp32) into a double-buffered accumulator in
-// tensor memory, and four epilogue warps read it back with tcgen05.ld, add the
-// bias and store channels-last y.  The dense variant (1x1 stride-1 layers and
-// kernels that cover the whole image) loads A by TMA as well.
+// tcgen05.mma (bf16 x bf16 -> fp32) into accumulators in tensor memory (up to
+// four, so the MMAs run ahead of the epilogue), and the epilogue warps read
+// them back with tcgen05.ld, add the bias and store channels-last y through a
+// staging tile and TMA.  The dense, window, plane, im2win and strided variants
+// load A by TMA as well (see AMode).
 //
-// CTA layout (320 threads, one persistent CTA per SM):
+// CTA layout (352 threads, one persistent CTA per SM; launched with
+// programmatic stream serialization):
 //   warps 0-3  epilogue: TMEM -> registers -> +bias -> bf16/fp32 -> global
-//   warps 4-7  A gather: cp.async 16-byte chunks through the indirection buffer
-//   warp  8    TMA producer for B (and for A in the dense and window variants)
-//   warp  9    TMEM allocation and the MMA-issuing thread
+//   warps 4-7  A gather (cp.async or TMA gather4 through the indirection
+//              buffer), or four more epilogue warps where A comes by TMA
+//   warp  8    TMA producer for B (and for A in the TMA-fed variants)
+//   warp  9    TMEM allocation and MMA issue (lane 0)
+//   warp 10    barrier waits for warp 9, handed over at a named barrier
 // Stages cycle through full/empty mbarrier pairs; every wait is bounded in
 // time and a timeout makes the whole CTA drain and return with an error code.
 #include <cuda_bf16.h>
@@ -33,9 +37,9 @@ constexpr int BM = 128;           // GEMM rows per tile (TMEM lanes)
 constexpr int BK = 64;            // K elements per stage: one 128-byte swizzle row
 constexpr int kEpiWarps = 4;
 constexpr int kGatherWarps = 4;
-// The MMA thread sits on warp 9 (scheduler 1), away from the window path's
-// L2-prefetch warp 4, which shares scheduler 0 with warp 8 (measured: 3% on
-// the 64->128 3x3 layer).
+// The MMA warp (9) and its wait warp (10) sit on schedulers 1 and 2, apart
+// from the TMA producer (warp 8, scheduler 0).  In plane mode the L2-prefetch
+// warp (5) shares scheduler 1 with the MMA warp and backs off between polls.
 constexpr int kTmaWarp = kEpiWarps + kGatherWarps;  // 8
 constexpr int kMmaWarp = kTmaWarp + 1;              // 9
 // Waits on the stage and accumulator barriers for the MMA warp and hands each
