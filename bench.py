@@ -107,13 +107,40 @@ KERNEL_SOURCES = ("indirect_implicit_gemm_gb300/csrc/igemm.cu",
                   "indirect_implicit_gemm_gb300/csrc/ptx.cuh")
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without // and /* */ comments, trailing spaces and blank lines
+    (string and character literals are kept as they are), so that editing a
+    comment does not change what the hash below says about the code."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash():
-    """sha256 over the sources that define the implicit-GEMM kernel and its plan."""
+    """sha256 over the sources that define the implicit-GEMM kernel and its plan,
+    comments and blank lines removed."""
     import hashlib
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()
 
 

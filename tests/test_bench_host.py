@@ -74,3 +74,16 @@ def test_reference_arm_prints_one_contract_line():
 def test_warmup_below_three_is_refused():
     r = run_bench(["--impl", "reference", "--steps", "1", "--warmup", "2"], {})
     assert r.returncode != 0
+
+
+def test_source_hash_ignores_comments_only():
+    """The traffic figure is tied to the kernel's code: comments and blank lines
+    do not change the hash, any code edit does, and literals are left intact."""
+    import bench
+    src = ('// header\nint a = 1;  // trailing\n/* block\n   comment */\n\n'
+           'const char* s = "a // b /* c */";\nchar q = \'/\';\nint b = 2; /* x */ int c = 3;\n')
+    assert bench.strip_comments(src) == (
+        'int a = 1;\nconst char* s = "a // b /* c */";\nchar q = \'/\';\nint b = 2;  int c = 3;')
+    assert bench.strip_comments(src.replace("trailing", "other words")) == bench.strip_comments(src)
+    assert bench.strip_comments(src.replace("int a = 1", "int a = 2")) != bench.strip_comments(src)
+    assert len(bench.kernel_source_hash()) == 64
