@@ -48,6 +48,9 @@ METRIC = "conv2d fwd TFLOPS & % of GB300 bf16 roofline; workspace bytes vs im2co
 HEADLINE = workloads.RESNET_3X3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
+# bf16 tcgen05 rate per SM per cycle: a 128x128x16 MMA (524,288 flop) issues
+# every 64 cycles (measured with back-to-back MMAs on one SM)
+TC_FLOP_PER_CLK_SM = 8192
 
 
 def load_peaks():
@@ -145,11 +148,12 @@ def kernel_source_hash():
 
 
 def profiled_traffic(workload):
-    """DRAM bytes per launch of the GEMM kernel on `workload`, from the committed
-    ncu summary under profiles/, or None when no summary covers this workload
-    or the kernel sources changed since it was taken.  The summary carries
-    lines `workload: <name>`, `source_sha256: <hex>` and
-    `dram_bytes_per_launch: <int>`."""
+    """DRAM bytes per launch of the GEMM kernel on `workload` ({"total", "read",
+    "write"}), from the committed ncu summary under profiles/, or None when no
+    summary covers this workload or the kernel sources changed since it was
+    taken.  The summary carries lines `workload: <name>`, `source_sha256:
+    <hex>`, `dram_bytes_per_launch: <int>` and optionally
+    `dram_read_bytes_per_launch` / `dram_write_bytes_per_launch`."""
     d = os.path.join(ROOT, "profiles")
     if not os.path.isdir(d):
         return None
@@ -161,14 +165,18 @@ def profiled_traffic(workload):
         with open(os.path.join(d, fn)) as f:
             for line in f:
                 if ":" in line and line.split(":", 1)[0].strip() in (
-                        "workload", "source_sha256", "dram_bytes_per_launch"):
+                        "workload", "source_sha256", "dram_bytes_per_launch",
+                        "dram_read_bytes_per_launch", "dram_write_bytes_per_launch"):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip().strip("`")
         if kv.get("workload") == workload and kv.get("source_sha256") == want:
             try:
-                return int(kv["dram_bytes_per_launch"])
+                tot = int(kv["dram_bytes_per_launch"])
             except (KeyError, ValueError):
                 return None
+            rd, wr = kv.get("dram_read_bytes_per_launch"), kv.get("dram_write_bytes_per_launch")
+            return {"total": tot, "read": int(rd) if rd else None,
+                    "write": int(wr) if wr else None}
     return None
 
 
@@ -285,11 +293,20 @@ def event_time_ms(fn, steps, stream):
 
 
 class Layer:
-    """Device-resident inputs (rotated) and outputs for one configuration."""
+    """Device-resident inputs (rotated) and outputs for one configuration.
 
-    def __init__(self, g, c, dev, sets=None):
-        self.g, self.c, self.dev = g, c, dev
+    path: the CONVGB_PATH_* value to run (0: the library's choice); cin_pad: run
+    the layer with its channels zero-padded to this many (ablation of the stem
+    paths against the gather path, which needs C_in % 8 == 0).  FLOPs and
+    algorithmic bytes are always those of the unpadded layer."""
+
+    def __init__(self, g, c, dev, sets=None, path=0, cin_pad=0):
+        self.g, self.c, self.dev, self.path = g, c, dev, path
         x, w, b = workloads.make_inputs(c, device=dev)
+        if cin_pad and cin_pad > c.C_in:
+            x = torch.nn.functional.pad(x, (0, cin_pad - c.C_in)).contiguous()
+            w = torch.nn.functional.pad(w, (0, cin_pad - c.C_in)).contiguous()
+        self.cin = x.shape[3]
         self.w, self.b = w, b
         self.out_dtype = torch.float32 if c.out_f32 else torch.bfloat16
         self.num = shape_numbers(g, c)
@@ -300,14 +317,21 @@ class Layer:
         Ho, Wo = self.num["H_out"], self.num["W_out"]
         self.ys = [torch.empty((c.N, Ho, Wo, c.C_out), dtype=self.out_dtype, device=dev)
                    for _ in range(self.sets)]
-        ws = self.num["workspace_bytes"]
+        ws = g.workspace_size(c.N, self.cin, c.H, c.W, c.C_out, c.KH, c.KW, c.stride, c.pad,
+                              c.dilation, path=path)
         self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
         self.ibuf = None
 
     def step(self, i):
         c = self.c
-        self.g.conv2d_fwd(self.xs[i % self.sets], self.w, self.b, c.stride, c.pad, c.dilation,
-                          out_dtype=self.out_dtype, y=self.ys[i % self.sets], workspace=self.ws)
+        self.g.conv2d_fwd_path(self.path, self.xs[i % self.sets], self.w, self.b, c.stride, c.pad,
+                               c.dilation, out_dtype=self.out_dtype, y=self.ys[i % self.sets],
+                               workspace=self.ws)
+
+    def plan(self):
+        c = self.c
+        return self.g.plan_info(c.N, self.cin, c.H, c.W, c.C_out, c.KH, c.KW, c.stride, c.pad,
+                                c.dilation, path=self.path, out_dtype=self.out_dtype)
 
     def gemm_only(self, i):
         """The implicit-GEMM kernel alone (indirection buffer prebuilt)."""
@@ -317,8 +341,18 @@ class Layer:
                                    y=self.ys[i % self.sets])
 
     def launches_per_step(self):
-        return {"gather": 2, "dense": 1, "stem": 3, "window": 1, "plane": 1,
-                "im2win": 3}[self.num["path"]]
+        """Kernels of this library one conv2d_fwd launches, from its plan: the
+        implicit GEMM, plus the indirection-buffer build (gather modes), the weight
+        re-pack (stem modes), the window-order re-layout (im2win mode) and the
+        split-K finishing pass."""
+        p = self.plan()
+        a = p["a_mode"]
+        n = 1
+        n += 1 if a in (1, 2, 3, 12) else 0      # build_indirection_kernel
+        n += 1 if a in (2, 5, 10) else 0         # weight re-pack
+        n += 1 if a == 10 else 0                 # im2win re-layout
+        n += 1 if p["splits"] > 1 else 0         # finish_split_kernel
+        return n
 
 
 def time_layer(layer, steps, warmup, stream):
@@ -364,6 +398,38 @@ def time_e2e(g, c, steps, warmup, dev, stream):
     h2d = xh.numel() * 2 + wh.numel() * 2 + bh.numel() * 2
     d2h = yh.numel() * yh.element_size()
     return ms, h2d, d2h
+
+
+def time_link(h2d_bytes, d2h_bytes, steps, dev):
+    """Plain pinned copies of the e2e step's bytes, no convolution: the host->device
+    and device->host legs on two streams at once (what a perfect overlap of the
+    copies could reach), and each alone.  Milliseconds per step."""
+    hin = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    hout = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    din = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    dout = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(which):
+        for _ in range(3):
+            _copies(which, hin, hout, din, dout, s1, s2)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            _copies(which, hin, hout, din, dout, s1, s2)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / steps * 1e3
+
+    return {"both_ms": run("both"), "h2d_ms": run("h2d"), "d2h_ms": run("d2h")}
+
+
+def _copies(which, hin, hout, din, dout, s1, s2):
+    if which in ("both", "h2d"):
+        with torch.cuda.stream(s1):
+            din.copy_(hin, non_blocking=True)
+    if which in ("both", "d2h"):
+        with torch.cuda.stream(s2):
+            hout.copy_(dout, non_blocking=True)
 
 
 def time_im2win(g, c, steps, warmup, dev, stream):
@@ -444,6 +510,60 @@ def run_reference(args):
     return 0
 
 
+# --------------------------------------------------------------------------- ablations
+# (layer, label, tuning bn, tuning max_stages, path, cin_pad): each group runs in
+# one process, one after another, so its rows compare like with like.
+def ablation_rows():
+    R = workloads.BY_NAME
+    rows = []
+    for st in (2, 3, 0):
+        rows.append(("resnet_3x3_64to128_56", "stages<=%d" % st if st else "default", 0, st, 0, 0))
+    for st in (2, 3, 0):
+        rows.append(("sweep_3x3_256c_28", "stages<=%d" % st if st else "default", 0, st, 0, 0))
+    for st in (2, 3, 4, 6, 0):
+        rows.append(("pointwise_1x1_256to64_56", "stages<=%d" % st if st else "default", 0, st,
+                     0, 0))
+    for st in (4, 5, 0):  # the TMA gather's four warps take turns: at least four stages
+        rows.append(("strided_3x3_s2_128to256_56", "stages<=%d" % st if st else "default", 0,
+                     st, 0, 0))
+    for st in (2, 4, 0):
+        rows.append(("sweep_3x3_32c_150", "stages<=%d" % st if st else "default", 0, st, 0, 0))
+    for bn in (64, 128, 256):
+        rows.append(("sweep_3x3_256c_28", "bn=%d" % bn, bn, 0, 0, 0))
+        rows.append(("strided_3x3_s2_128to256_56", "bn=%d" % bn, bn, 0, 0, 0))
+        rows.append(("sweep_1x1_512to2048_7", "bn=%d" % bn, bn, 0, 0, 0))
+    for name in ("stem_7x7_s2_3to64_224", "sweep_11x11_s4_3to64_224"):
+        rows.append((name, "im2win path", 0, 0, 6, 0))
+        rows.append((name, "staged-row stem path", 0, 0, 3, 0))
+        rows.append((name, "gather path, C_in padded to 8", 0, 0, 1, 8))
+    return [(R[a],) + r[1:] for r in rows for a in (r[0],)]
+
+
+def run_ablation(g, dev, stream, steps):
+    out = []
+    for c, label, bn, st, path, cin_pad in ablation_rows():
+        g.set_tuning(bn, st)
+        try:
+            L = Layer(g, c, dev, path=path, cin_pad=cin_pad)
+            ms = time_layer(L, steps, 3, stream)
+            plan = L.plan()
+            st_, code = g.check_device_errors()
+            ent = {"workload": c.name, "variant": label, "us": ms * 1e3,
+                   "tflops": L.num["flops"] / (ms * 1e-3) / 1e12,
+                   "plan": {k: plan[k] for k in ("path", "a_mode", "bn", "stages",
+                                                 "weights_resident", "cta_pair", "splits")},
+                   "device_status": st_}
+            del L
+            torch.cuda.empty_cache()
+        except Exception as e:
+            ent = {"workload": c.name, "variant": label, "error": str(e)[:200]}
+        finally:
+            g.set_tuning(0, 0)
+        print("ablation " + json.dumps(ent), flush=True)
+        out.append(ent)
+    return out
+
+
 # --------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -459,6 +579,11 @@ def main():
                     help="profiling mode: run this many eager conv2d_fwd calls of --config "
                          "(batch --batch) and exit without timing or output")
     ap.add_argument("--batch", type=int, default=0, help="override N of --config (profiling)")
+    ap.add_argument("--profile-op", choices=["conv", "im2win"], default="conv",
+                    help="profiling mode: conv2d_fwd (default) or the exported im2win_transform")
+    ap.add_argument("--ablate", action="store_true",
+                    help="run the ablation study (tile width, ring depth, stem paths) and exit; "
+                         "one 'ablation {json}' line per row")
     ap.add_argument("--clock-probe-s", type=float, default=0.5,
                     help="seconds of untimed steps before the timed region, so the clock "
                          "sampler sees the GPU under load (0 disables)")
@@ -485,13 +610,21 @@ def main():
     if args.batch:
         c = c.scaled(args.batch, "_n%d" % args.batch)
     if args.profile_launches:
-        layer = Layer(g, c, dev, sets=1)
-        for i in range(args.profile_launches):
-            layer.step(i)
+        if args.profile_op == "im2win":
+            x, _, _ = workloads.make_inputs(c, device=dev)
+            for i in range(args.profile_launches):
+                g.im2win_transform(x, c.KH, c.KW, c.stride, c.pad, c.dilation)
+        else:
+            layer = Layer(g, c, dev, sets=1)
+            for i in range(args.profile_launches):
+                layer.step(i)
         torch.cuda.synchronize()
         st, code = g.check_device_errors()
         return 0 if st == 0 else 1
     stream = torch.cuda.current_stream()
+    if args.ablate:
+        run_ablation(g, dev, stream, args.sweep_steps)
+        return 0
     layer = Layer(g, c, dev)
     num = layer.num
 
@@ -527,6 +660,7 @@ def main():
     if k_ms is None and layer.launches_per_step() == 1:
         k_ms = time_layer(layer, max(args.steps, 50), 5, stream)
     t_roof, bound = roofline_time_s(num, peaks)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     roof = None
     if k_ms is not None:
         if bound == "tensor":
@@ -537,18 +671,36 @@ def main():
             achieved = num["bytes"] / (k_ms * 1e-3) / 1e9
             peak = peaks["hbm_gbs"]
             unit = "GB/s"
+        tr = profiled_traffic(c.name)
         roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": profiled_traffic(c.name),
+                "frac": achieved / peak, "traffic": tr["total"] if tr else None,
+                "traffic_read": tr["read"] if tr else None,
+                "traffic_write": tr["write"] if tr else None,
+                "traffic_note": "DRAM bytes read + written while the launch runs (ncu); "
+                                "output lines still dirty in L2 when it ends are written "
+                                "back later and are not in the figure",
+                "algorithmic_bytes": num["bytes"],
                 "kernel": "igemm_kernel (%s path, tcgen05)" % num["path"],
                 "kernel_us": k_ms * 1e3,
                 "peak_source": "%s (MEASURED_PEAKS.json %s)" % (
                     peak_src, "bf16_tflops burst" if bound == "tensor" else "hbm_gbs"),
                 "roofline_us": t_roof * 1e6,
                 "frac_of_roofline": (t_roof * 1e3) / k_ms}
+        if clocks.get("sm_mhz"):
+            # the tensor cores' rate at the clock the kernel ran at: 8192 bf16
+            # flop per SM per cycle (a 128x128x16 MMA issues every 64 cycles)
+            clk_peak = sms * TC_FLOP_PER_CLK_SM * clocks["sm_mhz"] * 1e6 / 1e12
+            roof["tensor_peak_at_clock_tflops"] = clk_peak
+            roof["tensor_frac_at_clock"] = num["flops"] / (k_ms * 1e-3) / 1e12 / clk_peak
 
     e2e_ms, h2d, d2h = time_e2e(g, c, max(10, args.steps // 10), 3, dev, stream)
+    link = time_link(h2d, d2h, max(10, args.steps // 10), dev)
     e2e = {"value": world * num["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "link_ms_per_step": link["both_ms"], "link_h2d_ms": link["h2d_ms"],
+           "link_d2h_ms": link["d2h_ms"], "frac_of_link": link["both_ms"] / e2e_ms,
+           "link_note": "plain pinned cudaMemcpyAsync of the same bytes, both directions "
+                        "at once on two streams, no convolution"}
 
     sweep = []
     if not args.no_sweep:
@@ -573,11 +725,13 @@ def main():
                     ent["im2win_us"] = iw[0] * 1e3
                     ent["im2win_gbs"] = iw[1] / (iw[0] * 1e-3) / 1e9
                     ent["im2win_frac_hbm"] = ent["im2win_gbs"] / peaks["hbm_gbs"]
-                sweep.append(ent)
                 del L
                 torch.cuda.empty_cache()
             except Exception as e:  # keep the headline line even if one sweep entry fails
-                sweep.append({"workload": sc.name, "error": str(e)[:200]})
+                ent = {"workload": sc.name, "error": str(e)[:200]}
+            sweep.append(ent)
+            if rank == 0:  # one line per configuration, ahead of the headline line
+                print("sweep " + json.dumps(ent), flush=True)
 
     cpu = None
     if rank == 0 and not args.no_cpu:

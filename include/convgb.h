@@ -133,6 +133,49 @@ CONVGB_API size_t convgb_im2col_bytes(int N, int C_in, int H, int W, int KH, int
                            int pad, int dilation);
 
 /*
+ * How conv2d_fwd_path() maps a shape onto the implicit-GEMM kernel: the plan
+ * it would launch.  (An interface addition of this library for tests,
+ * benchmarks and tuning; the pages describe no plan.)  The GEMM of
+ * "Unifying Convolutions and GEMM", sections 2-3, is cut into output tiles of
+ * `tile_rows` consecutive GEMM rows (output pixels in (n, ho, wo) order) by
+ * `bn` columns (output channels).
+ */
+typedef struct convgb_plan {
+    int path;             /* the CONVGB_PATH_* value the call takes */
+    int a_mode;           /* how the A operand reaches shared memory (kernel-internal code) */
+    int bn;               /* GEMM columns (output channels) per tile */
+    int m_tiles;          /* tiles along M */
+    int tile_rows;        /* GEMM rows per tile: tile t covers rows [t*tile_rows,
+                             (t+1)*tile_rows) of M; 0 when a tile is not one range of M
+                             (the plane path, whose tiles hold padding-border pixels) */
+    int n_tiles;          /* tiles along C_out */
+    int splits;           /* K partitions per tile (1: none; >1: fp32 partial sums) */
+    int k_blocks;         /* pipeline stages per tile (one K block each) */
+    int stages;           /* shared-memory ring depth */
+    int weights_resident; /* 1: the whole weight column tile stays in shared memory */
+    int cta_pair;         /* 1: tiles run on pairs of CTAs (tcgen05 cta_group::2) */
+    int tma_store;        /* 1: the epilogue stores y through shared memory with TMA */
+    int epilogue_tiles;   /* staging tiles of that epilogue (0, 1 or 2) */
+    int epilogue_c32;     /* 1: 32-column staging chunks instead of 64 */
+} convgb_plan;
+
+/* Fills *plan with what conv2d_fwd_path(path, ...) would launch for this shape
+ * and y_dtype; nothing is launched.  Returns the same shape and path errors as
+ * conv2d_fwd_path (CONVGB_ERR_INVALID_ARG, CONVGB_ERR_UNSUPPORTED). */
+CONVGB_API convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_out,
+                                          int KH, int KW, int stride, int pad, int dilation,
+                                          int y_dtype, convgb_plan* plan);
+
+/* Overrides two choices of the planner for every later call in this process,
+ * for tuning and ablation studies (an interface addition; not from the pages):
+ * bn = 32, 64, 128 or 256 forces that tile width (0 = the planner's choice);
+ * max_stages = 2..8 caps the shared-memory ring depth of the finished plan
+ * (0 = no cap).  Other values mean 0.  Results stay exact, only speed changes;
+ * a forced width may also change the workspace size, so query it after this
+ * call.  Not synchronised with calls running on other host threads. */
+CONVGB_API void convgb_set_tuning(int bn, int max_stages);
+
+/*
  * conv2d_fwd -- forward convolution, y = conv(x, w) + bias.
  *
  * Defined by the formula at the top of this file.  Picks a path with
@@ -261,8 +304,9 @@ CONVGB_API size_t convgb_indirection_buffer_bytes(int H, int W, int KH, int KW, 
 
 /*
  * build_indirection_buffer -- the indirection buffer of "The Indirect
- * Convolution Algorithm" (Abstract: a buffer of pointers to the start of each
- * row of image pixels), as int32 element offsets.
+ * Convolution Algorithm" (Abstract: the modified GEMM finds its input rows
+ * through a buffer that points at pixel rows of the image), as int32 element
+ * offsets.
  *
  *   ibuf  device, int32 [H_out*W_out][KH*KW].  Entry (ho*W_out + wo, kh*KW + kw)
  *         holds ((h*W) + w)*C_in with h = ho*s + kh*d - p, w = wo*s + kw*d - p,

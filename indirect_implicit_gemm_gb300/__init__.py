@@ -21,7 +21,7 @@ __all__ = [
     "indirection_buffer_bytes", "check_device_errors", "set_wait_timeout_ns",
     "selftest_wait_timeout", "ConvgbError", "PATH_AUTO", "PATH_GATHER", "PATH_DENSE",
     "PATH_STEM", "PATH_WINDOW", "PATH_PLANE", "PATH_IM2WIN", "EXPORTED_SYMBOLS", "library_path",
-    "conv2d_fwd_host", "conv2d_fwd_host_scratch_size",
+    "conv2d_fwd_host", "conv2d_fwd_host_scratch_size", "plan_info", "set_tuning", "Plan",
 ]
 
 PATH_AUTO, PATH_GATHER, PATH_DENSE, PATH_STEM, PATH_WINDOW, PATH_PLANE, PATH_IM2WIN = (
@@ -42,7 +42,18 @@ EXPORTED_SYMBOLS = (
     "build_indirection_buffer", "convgb_im2win_bytes", "im2win_transform",
     "convgb_check_device_errors", "convgb_set_wait_timeout_ns", "convgb_selftest_wait_timeout",
     "convgb_version", "convgb_conv2d_fwd_host_scratch_size", "conv2d_fwd_host",
+    "convgb_plan_info", "convgb_set_tuning",
 )
+
+
+class Plan(ctypes.Structure):
+    """convgb_plan: what conv2d_fwd_path launches for a shape (include/convgb.h)."""
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "path", "a_mode", "bn", "m_tiles", "tile_rows", "n_tiles", "splits", "k_blocks", "stages",
+        "weights_resident", "cta_pair", "tma_store", "epilogue_tiles", "epilogue_c32")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 class ConvgbError(RuntimeError):
@@ -102,6 +113,10 @@ def load():
     lib.convgb_set_wait_timeout_ns.restype = None
     lib.convgb_selftest_wait_timeout.argtypes = [U64, P]
     lib.convgb_selftest_wait_timeout.restype = I
+    lib.convgb_plan_info.argtypes = [I] + shape10 + [I, ctypes.POINTER(Plan)]
+    lib.convgb_plan_info.restype = I
+    lib.convgb_set_tuning.argtypes = [I, I]
+    lib.convgb_set_tuning.restype = None
     lib.convgb_version.argtypes = []
     lib.convgb_version.restype = I
     _lib = lib
@@ -132,6 +147,21 @@ def _need_cuda(t, name, dtype=None):
         raise ValueError("%s must be contiguous (channels-last layout)" % name)
     if dtype is not None and t.dtype != dtype:
         raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def plan_info(N, C_in, H, W, C_out, KH, KW, stride=1, pad=0, dilation=1, path=PATH_AUTO,
+              out_dtype=torch.bfloat16) -> dict:
+    """The tiling conv2d_fwd_path(path, ...) would launch for this shape (no launch)."""
+    p = Plan()
+    _check(load().convgb_plan_info(path, N, C_in, H, W, C_out, KH, KW, stride, pad, dilation,
+                                   _F32 if out_dtype == torch.float32 else _BF16,
+                                   ctypes.byref(p)), "plan_info")
+    return p.as_dict()
+
+
+def set_tuning(bn: int = 0, max_stages: int = 0):
+    """Force the tile width and/or cap the ring depth of later plans (0 = automatic)."""
+    load().convgb_set_tuning(int(bn), int(max_stages))
 
 
 def output_dims(H, W, KH, KW, stride=1, pad=0, dilation=1):

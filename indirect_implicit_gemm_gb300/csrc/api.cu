@@ -23,6 +23,10 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kAlign = 256;  // alignment of each workspace region
 
 std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
+// Planner overrides for tuning and ablation studies (convgb_set_tuning); 0 =
+// the planner's own choice.
+std::atomic<int> g_tune_bn{0};
+std::atomic<int> g_tune_stages{0};
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -285,6 +289,8 @@ bool encode_strided(CUtensorMap* m, const void* x, const ConvShape& c, int R)
 
 int pick_bn(int C_out)
 {
+    const int forced = g_tune_bn.load(std::memory_order_relaxed);
+    if (forced) return forced;
     if (C_out <= 32) return 32;
     if (C_out <= 64) return 64;
     if (C_out <= 128) return 128;
@@ -347,7 +353,8 @@ void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
     const int bnb = g.pair ? g.bn / 2 : g.bn;
     const int s = igemm_pick_stages(bnb, g.bres, kb_res, g.a_stage_bytes, g.b_per_stage,
                                     g.extra_smem + kEpiStageBytes);
-    if (s < 2) return;
+    const bool turns = g.amode == kATmaGather || g.amode == kATmaGatherPair;
+    if (s < (turns ? kMinGatherTurnStages : 2)) return;
     g.stages = s;
     g.tma_store = 1;
     g.epi_bufs = 1;
@@ -381,11 +388,26 @@ void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
 GemmPlan plan_gemm_ring(int path, const ConvShape& c);
 GemmPlan plan_plane(const ConvShape& c, int y_f32);
 
+// A ring-depth cap from convgb_set_tuning applies to the finished plan, so
+// that every other choice (resident weights, epilogue staging) stays the
+// planner's own.
+void cap_stages(GemmPlan& g)
+{
+    int cap = g_tune_stages.load(std::memory_order_relaxed);
+    if (cap == 0) return;
+    // The TMA-gather warps fill the ring by turns, one stage in four each: a
+    // ring of fewer than four stages would let a warp's wait on a stage's
+    // release run two phases ahead, where the barrier's parity cannot tell
+    // them apart.
+    if (g.amode == kATmaGather || g.amode == kATmaGatherPair) cap = std::max(cap, kMinGatherTurnStages);
+    if (g.stages > cap) g.stages = cap;
+}
+
 GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32)
 {
-    if (path == CONVGB_PATH_PLANE) return plan_plane(c, y_f32);
-    GemmPlan g = plan_gemm_ring(path, c);
-    plan_epilogue(g, c, y_f32);
+    GemmPlan g = path == CONVGB_PATH_PLANE ? plan_plane(c, y_f32) : plan_gemm_ring(path, c);
+    if (path != CONVGB_PATH_PLANE) plan_epilogue(g, c, y_f32);
+    cap_stages(g);
     return g;
 }
 
@@ -648,6 +670,17 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         igemm_pick_stages(bnb, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
         g.bres = 1;
     g.stages = igemm_pick_stages(bnb, g.bres, g.num_kb, g.a_stage_bytes, 1);
+    if ((g.amode == kATmaGather || g.amode == kATmaGatherPair) &&
+        g.stages < kMinGatherTurnStages) {
+        // too shallow a ring for the gather warps' turns: 16-byte cp.async instead
+        g.amode = kAGather;
+        g.pair = 0;
+        g.bres = 0;
+        if (g.n_tiles == 1 && g.splits == 1 &&
+            igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
+            g.bres = 1;
+        g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb, g.a_stage_bytes, 1);
+    }
     return g;
 }
 
@@ -656,6 +689,17 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
 bool window_applies(const ConvShape& c)
 {
     return window_geometry(c) && plan_gemm(CONVGB_PATH_WINDOW, c).stages >= 2;
+}
+
+// The gather path's plan without split K (conv2d_fwd_indirect and
+// conv2d_fwd_noalloc have nowhere to keep partial sums).
+GemmPlan plan_indirect(const ConvShape& c, int y_f32)
+{
+    GemmPlan plan = plan_gemm_ring(CONVGB_PATH_GATHER, c);
+    plan.splits = 1;
+    plan_epilogue(plan, c, y_f32);
+    cap_stages(plan);
+    return plan;
 }
 
 // Workspace regions of each path, in order; every region starts 256-byte aligned.
@@ -985,6 +1029,50 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
 
 }  // namespace
 
+// conv2d_fwd_indirect, and conv2d_fwd_noalloc with build_ibuf = 1: every
+// check and the whole plan (tensor maps included) before the first launch;
+// then, when asked, the indirection buffer is built into ibuf on the stream,
+// and the GEMM follows.
+convgb_status conv_indirect(const void* x, const void* w, const void* bias, int N, int C_in, int H,
+                            int W, int C_out, int KH, int KW, int stride, int pad, int dilation,
+                            int32_t* ibuf, size_t ibuf_bytes, int build_ibuf, void* y,
+                            int y_dtype, void* stream)
+{
+    ConvShape c;
+    convgb_status st = make_shape(N, C_in, H, W, C_out, KH, KW, stride, pad, dilation, &c);
+    if (st != CONVGB_OK) return st;
+    if (!x || !w || !y || !ibuf) return CONVGB_ERR_INVALID_ARG;
+    if (y_dtype != CONVGB_BF16 && y_dtype != CONVGB_F32) return CONVGB_ERR_INVALID_ARG;
+    if (!path_supports(CONVGB_PATH_GATHER, c)) return CONVGB_ERR_UNSUPPORTED;
+    if (ibuf_bytes < (size_t)c.H_out * c.W_out * KH * KW * sizeof(int32_t))
+        return CONVGB_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        !aligned16(ibuf))
+        return CONVGB_ERR_ALIGNMENT;
+    // Reusing a caller's buffer leaves no room for split-K partial sums.
+    const GemmPlan plan = plan_indirect(c, y_dtype == CONVGB_F32 ? 1 : 0);
+    IgemmArgs a;
+    a.x = static_cast<const uint16_t*>(x);
+    a.ibuf = ibuf;
+    a.w = w;
+    a.bias = bias;
+    a.y = y;
+    a.y_f32 = y_dtype == CONVGB_F32 ? 1 : 0;
+    a.C_out = C_out;
+    a.C_in = C_in;
+    a.taps = KH * KW;
+    a.HWo = c.H_out * c.W_out;
+    a.img_elems = (long long)H * W * C_in;
+    a.img_rows = H * W;
+    a.x_rows = (long long)N * H * W;
+    PreparedGemm pg;
+    st = prepare_gemm(plan, a, &pg);
+    if (st != CONVGB_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (build_ibuf && launch_build_indirection(c, ibuf, cs) != cudaSuccess) return CONVGB_ERR_CUDA;
+    return launch_gemm(pg, cs);
+}
+
 unsigned* device_error_word()
 {
     static unsigned* addr[kMaxDevices] = {};
@@ -1103,39 +1191,8 @@ convgb_status conv2d_fwd_indirect(const void* x, const void* w, const void* bias
                                   int dilation, const int32_t* ibuf, size_t ibuf_bytes, void* y,
                                   int y_dtype, void* stream)
 {
-    ConvShape c;
-    convgb_status st = make_shape(N, C_in, H, W, C_out, KH, KW, stride, pad, dilation, &c);
-    if (st != CONVGB_OK) return st;
-    if (!x || !w || !y || !ibuf) return CONVGB_ERR_INVALID_ARG;
-    if (y_dtype != CONVGB_BF16 && y_dtype != CONVGB_F32) return CONVGB_ERR_INVALID_ARG;
-    if (!path_supports(CONVGB_PATH_GATHER, c)) return CONVGB_ERR_UNSUPPORTED;
-    if (ibuf_bytes < (size_t)c.H_out * c.W_out * KH * KW * sizeof(int32_t))
-        return CONVGB_ERR_WORKSPACE;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
-        !aligned16(ibuf))
-        return CONVGB_ERR_ALIGNMENT;
-    // Reusing a caller's buffer leaves no room for split-K partial sums.
-    GemmPlan plan = plan_gemm_ring(CONVGB_PATH_GATHER, c);
-    plan.splits = 1;
-    plan_epilogue(plan, c, y_dtype == CONVGB_F32 ? 1 : 0);
-    IgemmArgs a;
-    a.x = static_cast<const uint16_t*>(x);
-    a.ibuf = ibuf;
-    a.w = w;
-    a.bias = bias;
-    a.y = y;
-    a.y_f32 = y_dtype == CONVGB_F32 ? 1 : 0;
-    a.C_out = C_out;
-    a.C_in = C_in;
-    a.taps = KH * KW;
-    a.HWo = c.H_out * c.W_out;
-    a.img_elems = (long long)H * W * C_in;
-    a.img_rows = H * W;
-    a.x_rows = (long long)N * H * W;
-    PreparedGemm pg;
-    st = prepare_gemm(plan, a, &pg);
-    if (st != CONVGB_OK) return st;
-    return launch_gemm(pg, static_cast<cudaStream_t>(stream));
+    return conv_indirect(x, w, bias, N, C_in, H, W, C_out, KH, KW, stride, pad, dilation,
+                         const_cast<int32_t*>(ibuf), ibuf_bytes, 0, y, y_dtype, stream);
 }
 
 size_t convgb_indirection_buffer_bytes(int H, int W, int KH, int KW, int stride, int pad,
@@ -1222,6 +1279,44 @@ convgb_status convgb_selftest_wait_timeout(uint64_t timeout_ns, void* stream)
                : CONVGB_ERR_CUDA;
 }
 
-int convgb_version(void) { return 100; }
+convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_out, int KH, int KW,
+                               int stride, int pad, int dilation, int y_dtype, convgb_plan* out)
+{
+    if (!out) return CONVGB_ERR_INVALID_ARG;
+    memset(out, 0, sizeof *out);
+    ConvShape c;
+    convgb_status st = make_shape(N, C_in, H, W, C_out, KH, KW, stride, pad, dilation, &c);
+    if (st != CONVGB_OK) return st;
+    if (y_dtype != CONVGB_BF16 && y_dtype != CONVGB_F32) return CONVGB_ERR_INVALID_ARG;
+    if (path == CONVGB_PATH_AUTO) path = select_path(c);
+    if (!path_supports(path, c)) return CONVGB_ERR_UNSUPPORTED;
+    const GemmPlan g = plan_gemm(path, c, y_dtype == CONVGB_F32 ? 1 : 0);
+    const bool plane = g.amode == kAPlane || g.amode == kAPlane3 || g.amode == kAPlane3U2;
+    const bool rowtiles = g.amode == kAWindow || g.amode == kAWindowPair ||
+                          g.amode == kANarrowWin || g.amode == kAIm2win || g.amode == kAStrided;
+    out->path = path;
+    out->a_mode = g.amode;
+    out->bn = g.bn;
+    out->m_tiles = g.m_tiles;
+    out->tile_rows = plane ? 0 : rowtiles ? g.m_step * c.W_out : 128;
+    out->n_tiles = g.n_tiles;
+    out->splits = g.splits;
+    out->k_blocks = g.num_kb;
+    out->stages = g.stages;
+    out->weights_resident = g.bres;
+    out->cta_pair = g.pair;
+    out->tma_store = g.tma_store;
+    out->epilogue_tiles = g.tma_store ? g.epi_bufs : 0;
+    out->epilogue_c32 = g.epi_c32;
+    return CONVGB_OK;
+}
+
+void convgb_set_tuning(int bn, int max_stages)
+{
+    g_tune_bn.store((bn == 32 || bn == 64 || bn == 128 || bn == 256) ? bn : 0);
+    g_tune_stages.store((max_stages >= 2 && max_stages <= 8) ? max_stages : 0);
+}
+
+int convgb_version(void) { return 101; }
 
 }  // extern "C"

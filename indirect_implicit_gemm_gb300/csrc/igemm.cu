@@ -1588,6 +1588,10 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
             : igemm_smem_bytes(kPairMode ? BN / 2 : BN, p.stages, p.bres, p.kb_total,
                                p.a_stage_bytes, p.b_per_stage, extra);
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
+    // gather warps taking turns: at most one phase ahead needs kGatherWarps stages
+    static_assert(kMinGatherTurnStages == kGatherWarps, "turn-taking ring depth");
+    if ((AMODE == kATmaGather || AMODE == kATmaGatherPair) && p.stages < kMinGatherTurnStages)
+        return cudaErrorInvalidValue;
     // 32-column staging exists for the eight-warp epilogue only
     constexpr bool kEpi8 = AMODE == kAWindow || AMODE == kAWindowPair || AMODE == kADense ||
                            AMODE == kAIm2win || AMODE == kAStrided;

@@ -142,6 +142,10 @@ enum AMode : int {
     kATmaGatherPair = 12,  // TMA gather4 on a cluster of two CTAs (tcgen05.mma.cta_group::2,
                            // 256 rows); each CTA holds half of the weight columns
 };
+// Fewest ring stages the TMA-gather modes run with: their four gather warps
+// fill the stages by turns, and each warp's wait on a stage's release must be
+// at most one barrier phase ahead of it.
+constexpr int kMinGatherTurnStages = 4;
 // Dynamic shared memory of one implicit-GEMM CTA, and the deepest ring that fits
 // (0 when none does).
 int igemm_smem_bytes(int bn, int stages, int bres, int num_kb, int a_stage_bytes,
@@ -172,5 +176,12 @@ cudaError_t launch_selftest_timeout(unsigned long long timeout_ns, unsigned* err
 // Shared helpers from api.cu.
 unsigned* device_error_word();  // address of this device's error word (host-visible pointer)
 int num_sms();
+// The gather-path convolution with the indirection buffer at `ibuf`: every
+// check and the plan first, nothing launched on failure; then, if build_ibuf,
+// the buffer is built into ibuf on the stream; then the GEMM (no split K).
+convgb_status conv_indirect(const void* x, const void* w, const void* bias, int N, int C_in, int H,
+                            int W, int C_out, int KH, int KW, int stride, int pad, int dilation,
+                            int32_t* ibuf, size_t ibuf_bytes, int build_ibuf, void* y,
+                            int y_dtype, void* stream);
 
 }  // namespace convgb

@@ -44,8 +44,10 @@ int32_t* scratch_on_current_device()
     std::lock_guard<std::mutex> lock(mu);
     if (addr[dev] == nullptr) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();  // leave no error of this call for the caller's next check
             return nullptr;
+        }
         addr[dev] = static_cast<int32_t*>(p);
     }
     return addr[dev];
@@ -62,7 +64,8 @@ extern "C" convgb_status conv2d_fwd_noalloc(const void* x, const void* w, const 
                                             int y_dtype, void* stream)
 {
     using namespace convgb;
-    // Every check happens before the first launch.
+    // Every check, and the whole plan of the GEMM, happens before the first
+    // launch: a call that fails queues nothing and leaves the array untouched.
     int H_out = 0, W_out = 0;
     if (convgb_output_dims(H, W, KH, KW, stride, pad, dilation, &H_out, &W_out) != CONVGB_OK)
         return CONVGB_ERR_INVALID_ARG;
@@ -80,9 +83,6 @@ extern "C" convgb_status conv2d_fwd_noalloc(const void* x, const void* w, const 
     int32_t* scratch = scratch_on_current_device();
     if (scratch == nullptr) return CONVGB_ERR_CUDA;
 
-    convgb_status st = build_indirection_buffer(H, W, C_in, KH, KW, stride, pad, dilation,
-                                                scratch, kNoAllocScratchBytes, stream);
-    if (st != CONVGB_OK) return st;
-    return conv2d_fwd_indirect(x, w, bias, N, C_in, H, W, C_out, KH, KW, stride, pad, dilation,
-                               scratch, kNoAllocScratchBytes, y, y_dtype, stream);
+    return conv_indirect(x, w, bias, N, C_in, H, W, C_out, KH, KW, stride, pad, dilation, scratch,
+                         kNoAllocScratchBytes, 1, y, y_dtype, stream);
 }

@@ -28,7 +28,7 @@ Functions and the passages they follow
     of every output pixel of row ho is one contiguous run of Win.
 ``indirection_buffer``
     The indirection buffer ("The Indirect Convolution Algorithm", Abstract:
-    a buffer of pointers to the start of each row of image pixels).  Reading:
+    a buffer that points the GEMM at the pixel rows of the image).  Reading:
     one entry per (output pixel, tap), holding the element offset
     ((h*W) + w)*C_in of that input pixel's C_in-vector within one image, or
     -1 where the tap falls in the zero padding; batch-independent, laid out

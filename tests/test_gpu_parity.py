@@ -189,6 +189,78 @@ def test_stem_path_explicit_matches_oracle(gpu_lib, shape):
     check(got, ref, mag, shape.name)
 
 
+# One shape per A-operand mode whose grid hands every persistent CTA at least
+# six work units (accumulator slots reused, the ring wrapped many times, pair
+# tails at scale), with small K so the oracle checks every element in seconds.
+MULTI_TILE = [
+    (S("multi_gather_c32", N=130, C_in=32, H=30, W=30, C_out=32, seed=70), 0, 1),
+    (S("multi_tmagather_c64_s2", N=519, C_in=64, H=30, W=30, C_out=64, stride=2, seed=71), 0, 3),
+    (S("multi_tmagather_pair_1x1_p1_s2", N=456, C_in=64, H=30, W=30, C_out=256, KH=1, KW=1,
+       stride=2, pad=1, seed=72), 0, 12),
+    (S("multi_window_pair_1x3", N=456, C_in=64, H=14, W=14, C_out=256, KH=1, KW=3, seed=73),
+     0, 9),
+    (S("multi_window_c64_1x3", N=456, C_in=64, H=14, W=14, C_out=64, KH=1, KW=3, seed=74), 0, 4),
+    (S("multi_strided_1x1_s2", N=456, C_in=64, H=32, W=32, C_out=64, KH=1, KW=1, stride=2,
+       pad=0, seed=75), 0, 11),
+    (S("multi_dense_1x1", N=456, C_in=64, H=16, W=16, C_out=64, KH=1, KW=1, pad=0, seed=76),
+     0, 0),
+    (S("multi_narrowwin_c3", N=114, C_in=3, H=32, W=32, C_out=32, seed=77), 3, 5),
+    (S("multi_narrow_c3_d2", N=114, C_in=3, H=32, W=32, C_out=32, pad=2, dilation=2, seed=78),
+     3, 2),
+    (S("multi_im2win_c3_7x7_s2", N=456, C_in=3, H=32, W=32, C_out=64, KH=7, KW=7, stride=2,
+       pad=3, seed=79), 6, 10),
+    (S("multi_plane3_c64", N=456, C_in=64, H=14, W=14, C_out=64, seed=80), 5, None),
+]
+
+
+@pytest.mark.parametrize("case", MULTI_TILE, ids=lambda c: c[0].name)
+def test_many_tiles_per_cta_every_element(gpu_lib, case):
+    shape, path, amode = case
+    plan = gpu_lib.plan_info(shape.N, shape.C_in, shape.H, shape.W, shape.C_out, shape.KH,
+                             shape.KW, shape.stride, shape.pad, shape.dilation, path=path)
+    if amode is not None:
+        assert plan["a_mode"] == amode, plan
+    units = plan["m_tiles"] * plan["n_tiles"] * plan["splits"]
+    if plan["cta_pair"]:
+        units = (plan["m_tiles"] + 1) // 2 * plan["n_tiles"]
+        ctas = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    else:
+        ctas = torch.cuda.get_device_properties(0).multi_processor_count
+    assert units >= 6 * ctas, (units, ctas, plan)
+    got, ref, mag = run_full(gpu_lib, shape, path=path)
+    check(got, ref, mag, shape.name)
+
+
+# Planner overrides used by the ablation study (convgb_set_tuning): forced tile
+# widths and capped ring depths must still give exact results on every path.
+TUNED_SHAPES = [sh for sh in SMALL if sh.name in (
+    "gather_cout_200", "gather_cout_300_k_tail", "tmagather_c64_5x3", "dense_1x1",
+    "window_c64_cout200_streamed", "window_c128_narrow_staging", "strided_1x1_s2_cout300",
+    "stem_c3_7x7_s2", "stem_c5", "tmagather_pair_c128_cout300", "window_pair128_c128")]
+TUNINGS = [(32, 0), (64, 0), (128, 2), (256, 0), (0, 2), (0, 3)]
+
+
+@pytest.fixture
+def tuning(gpu_lib):
+    yield gpu_lib.set_tuning
+    gpu_lib.set_tuning(0, 0)
+
+
+@pytest.mark.parametrize("shape", TUNED_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("bn,stages", TUNINGS, ids=lambda v: str(v))
+def test_tuned_plans_match_oracle(gpu_lib, tuning, shape, bn, stages):
+    tuning(bn, stages)
+    plan = gpu_lib.plan_info(shape.N, shape.C_in, shape.H, shape.W, shape.C_out, shape.KH,
+                             shape.KW, shape.stride, shape.pad, shape.dilation)
+    if stages:
+        # the TMA-gather modes never run on fewer than four stages
+        floor = 4 if plan["a_mode"] in (3, 12) else 2
+        assert plan["stages"] <= max(stages, floor)
+        assert plan["stages"] >= floor
+    got, ref, mag = run_full(gpu_lib, shape)
+    check(got, ref, mag, "%s bn=%d stages<=%d" % (shape.name, bn, stages))
+
+
 def test_tiny_config_full_output(gpu_lib):
     """3 -> 4 channels, 8x8, 3x3, fp32 output: every output element."""
     shape = workloads.TINY

@@ -262,3 +262,26 @@ def test_im2win_is_smaller_than_im2col_for_3x3():
     once per tap column: for KW > stride it is smaller than im2col."""
     args = (32, 64, 56, 56, 3, 3, 1, 1, 1)
     assert oracle.im2win_elements(*args) < oracle.im2col_elements(*args)
+
+
+@pytest.mark.parametrize("geom", GEOMS)
+def test_im2win_width_is_the_tightest_span_of_the_columns_read(geom):
+    """The window-order buffer keeps one contiguous span of input columns per
+    output row (the reading of the layout).  That span must contain every column
+    the 7-loop convolution's index map reads (w = wo*s + kw*d - p) and start and
+    end on a column that is read: no dead column at either end (a W_used that is
+    too large would still reproduce unfold above) and none missing.  With
+    stride > dilation the columns between read ones stay in the span.  The set
+    of columns read is enumerated from the loop indices, not from the W_used
+    formula."""
+    N, C_in, H, W, C_out, KH, KW, s, p, d = geom
+    x, _, _ = rand_case(52, N, C_in, H, W, C_out, KH, KW)
+    win = oracle.im2win(workloads.bits(x), KH, KW, s, p, d)
+    W_out = oracle.output_size(W, KW, s, p, d)
+    read = {wo * s + kw * d - p for wo in range(W_out) for kw in range(KW)}
+    # buffer column wc holds input column wc - p
+    kept = [wc - p for wc in range(win.shape[2])]
+    assert read <= set(kept)
+    assert kept[0] == min(read) and kept[-1] == max(read)
+    assert oracle.im2win_elements(N, C_in, H, W, KH, KW, s, p, d) == \
+        N * win.shape[1] * (max(read) - min(read) + 1) * KH * C_in
