@@ -99,7 +99,8 @@ def shape_numbers(g, c: workloads.ConvShape):
                                             c.dilation),
                 im2win_bytes=g.im2win_bytes(c.N, c.C_in, c.H, c.W, c.KH, c.KW, c.stride, c.pad,
                                             c.dilation),
-                path={1: "gather", 2: "dense", 3: "stem", 4: "window", 5: "plane", 6: "im2win"}.get(
+                path={1: "gather", 2: "dense", 3: "stem", 4: "window", 5: "plane", 6: "im2win",
+                      7: "stemwin"}.get(
                     g.select_path(c.N, c.C_in, c.H, c.W, c.C_out, c.KH, c.KW, c.stride, c.pad,
                                   c.dilation), "?"))
 

@@ -89,12 +89,21 @@ typedef enum convgb_path {
                                  is staged once per (tile, 64-channel block) and read by all
                                  KH*KW taps; rows and columns of the padding border are
                                  computed and discarded.  No workspace. */
-    CONVGB_PATH_IM2WIN = 6    /* C_in < 16, undilated, W_out <= 128: x re-laid out in window
+    CONVGB_PATH_IM2WIN = 6,   /* C_in < 16, undilated, W_out <= 128: x re-laid out in window
                                  order ("Im2win", Abstract), each column's (kh, ci) vector
                                  padded to a multiple of 8; every output pixel's A row is then
                                  one contiguous run of KW columns, loaded by TMA.  Workspace:
                                  the re-laid-out input (less than half of im2col, else the
                                  path does not apply) and the re-packed weights. */
+    CONVGB_PATH_STEMWIN = 7   /* C_in = 3, stride 1, 2 or 4, undilated, W_out + ceil(KW/s) - 1
+                                 <= 128, at most 16 MMA steps of 16 per stage (KW*KC <= 256,
+                                 KC = 64/s), C_in*W*2 and C_out*KH*KW*C_in*2 multiples of 16,
+                                 C_out <= 256: the window order of "Im2win" (Abstract) built
+                                 in shared memory per output row, with each output pixel's
+                                 next s input columns one 128-byte row further on, so the
+                                 tensor core reads every K block of the window from the same
+                                 rows at shifted starts.  No workspace: nothing goes through
+                                 HBM but x, w and y. */
 } convgb_path;
 
 /* Short English text for a status code; never NULL. */

@@ -20,12 +20,14 @@ __all__ = [
     "output_dims", "select_path", "workspace_size", "im2col_bytes", "im2win_bytes",
     "indirection_buffer_bytes", "check_device_errors", "set_wait_timeout_ns",
     "selftest_wait_timeout", "ConvgbError", "PATH_AUTO", "PATH_GATHER", "PATH_DENSE",
-    "PATH_STEM", "PATH_WINDOW", "PATH_PLANE", "PATH_IM2WIN", "EXPORTED_SYMBOLS", "library_path",
+    "PATH_STEM", "PATH_WINDOW", "PATH_PLANE", "PATH_IM2WIN", "PATH_STEMWIN", "EXPORTED_SYMBOLS",
+    "library_path",
     "conv2d_fwd_host", "conv2d_fwd_host_scratch_size", "plan_info", "set_tuning", "Plan",
 ]
 
 PATH_AUTO, PATH_GATHER, PATH_DENSE, PATH_STEM, PATH_WINDOW, PATH_PLANE, PATH_IM2WIN = (
     0, 1, 2, 3, 4, 5, 6)
+PATH_STEMWIN = 7
 _BF16, _F32 = 0, 1
 OK, ERR_INTERNAL = 0, 6
 

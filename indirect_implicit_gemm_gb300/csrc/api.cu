@@ -162,8 +162,50 @@ bool im2win_applies(const ConvShape& c)
     return g.buf_bytes < c.M * c.K * 2 / 2;
 }
 
+// Staged-window stem geometry.  For stride s in {1, 2, 4} and C_in = 3, each
+// 128-byte row r of a shared-memory stage holds the s input columns
+// s*r - p .. s*r - p + s - 1 of one output row, KC = 64/s values (kh, ci) per
+// column (khg = KC / C_in kernel rows of a group, the rest zero).  Output pixel
+// wo then reads its K block kb (columns s*(wo+kb) - p ..) from row wo + kb, so
+// the MMA takes every K block of a stage from the same rows at shifted
+// descriptor starts, as the window path does for its taps.  A tile is R
+// output rows, each a segment of seg = W_out + nkb - 1 stage rows.
+struct StemWinGeom {
+    bool ok = false;
+    int KC = 0, khg = 0, groups = 0, nkb = 0, seg = 0, R = 0, last_steps = 0;
+    int a0 = 0, rb = 0, slot = 0;  // staged input rows, as the narrow window lays them out
+    long long wbytes = 0;          // raw weights [C_out][KH*KW*C_in], bf16
+};
+StemWinGeom stemwin_geom(const ConvShape& c)
+{
+    StemWinGeom g;
+    if (c.C_in != 3 || c.d != 1 || c.KH > 31) return g;
+    if (c.s != 1 && c.s != 2 && c.s != 4) return g;
+    if (((long long)c.W * c.C_in * 2) % 16 != 0) return g;  // bulk copies of whole rows
+    g.wbytes = (long long)c.C_out * c.KH * c.KW * c.C_in * 2;
+    if (g.wbytes % 16 != 0) return g;  // one bulk copy of the raw weights
+    g.KC = 64 / c.s;
+    g.khg = g.KC / c.C_in;
+    g.groups = (c.KH + g.khg - 1) / g.khg;
+    g.nkb = (c.KW + c.s - 1) / c.s;
+    g.seg = c.W_out + g.nkb - 1;
+    if (g.seg > 128) return g;
+    g.R = 128 / g.seg;
+    g.last_steps = ((c.KW - c.s * (g.nkb - 1)) * g.KC + 15) / 16;
+    if ((g.nkb - 1) * 4 + g.last_steps > 16) return g;  // the kernel's unrolled MMA sequence
+    g.a0 = (c.p * c.C_in * 2 + 15) / 16 * 16;
+    const int lead = g.a0 - c.p * c.C_in * 2;  // byte of pixel -p
+    const int data_end = g.a0 + c.W * c.C_in * 2;
+    const int read_end = lead + c.s * g.seg * c.C_in * 2;  // past the last column a row reads
+    g.rb = (std::max(data_end, read_end) + 15) / 16 * 16;
+    g.slot = (g.R * c.KH * g.rb + 511) / 512 * 512;
+    g.ok = true;
+    return g;
+}
+
 struct GemmPlan;
 GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32 = 0);
+bool stemwin_applies(const ConvShape& c);
 bool window_applies(const ConvShape& c);
 bool plane_applies(const ConvShape& c);
 
@@ -178,6 +220,7 @@ bool path_supports(int path, const ConvShape& c)
     case CONVGB_PATH_DENSE:
         return c.C_in % 8 == 0 && (is_pointwise(c) || is_full_spatial(c) || strided_rows(c) > 0);
     case CONVGB_PATH_STEM: return c.C_in % 8 != 0;
+    case CONVGB_PATH_STEMWIN: return stemwin_applies(c);
     default: return false;
     }
 }
@@ -185,7 +228,10 @@ bool path_supports(int path, const ConvShape& c)
 int select_path(const ConvShape& c)
 {
     if (path_supports(CONVGB_PATH_DENSE, c)) return CONVGB_PATH_DENSE;
-    if (c.C_in % 8 != 0) return im2win_applies(c) ? CONVGB_PATH_IM2WIN : CONVGB_PATH_STEM;
+    if (c.C_in % 8 != 0)
+        return stemwin_applies(c)  ? CONVGB_PATH_STEMWIN
+               : im2win_applies(c) ? CONVGB_PATH_IM2WIN
+                                   : CONVGB_PATH_STEM;
     if (path_supports(CONVGB_PATH_WINDOW, c)) return CONVGB_PATH_WINDOW;
     return CONVGB_PATH_GATHER;
 }
@@ -315,6 +361,7 @@ struct GemmPlan {
     int epi_c32 = 0;               // 1: 32-column chunks, 8 KB staging tiles
     int pl_u = 1, pl_nacc = 0, b_stages = 0;  // plane mode: sub-tiles, accumulators, B slots
     int pair = 0;                  // window mode on a CTA pair (each CTA holds bn/2 columns of B)
+    int min_stages = 2;            // shallowest ring the mode runs with (a tuning cap stops here)
     long long M = 0, K = 0;
     int num_kb = 0, m_tiles = 0, n_tiles = 0;
 };
@@ -400,6 +447,7 @@ void cap_stages(GemmPlan& g)
     // release run two phases ahead, where the barrier's parity cannot tell
     // them apart.
     if (g.amode == kATmaGather || g.amode == kATmaGatherPair) cap = std::max(cap, kMinGatherTurnStages);
+    cap = std::max(cap, g.min_stages);
     if (g.stages > cap) g.stages = cap;
 }
 
@@ -523,6 +571,13 @@ GemmPlan plan_plane(const ConvShape& c, int y_f32)
 
 bool plane_applies(const ConvShape& c) { return plan_plane(c, 0).stages >= 2; }
 
+bool stemwin_applies(const ConvShape& c)
+{
+    if (!stemwin_geom(c).ok) return false;
+    const GemmPlan g = plan_gemm_ring(CONVGB_PATH_STEMWIN, c);
+    return g.stages >= 2;
+}
+
 // Operand producers, tiles, splits and the shared-memory ring.
 GemmPlan plan_gemm_ring(int path, const ConvShape& c)
 {
@@ -590,6 +645,39 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         if (g.n_tiles == 1 && igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
             g.bres = 1;
         g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb, g.a_stage_bytes, 1);
+        return g;
+    }
+    if (path == CONVGB_PATH_STEMWIN) {
+        // A stages built in shared memory from staged input rows; one stage per
+        // kernel-row group, each feeding nkb K blocks; weights packed by the
+        // kernel into resident tiles.
+        const StemWinGeom sg = stemwin_geom(c);
+        g.amode = stemwin_amode(c.s);
+        if (!sg.ok) return g;  // stages == 0: not applicable
+        g.M = c.M;
+        g.K = (long long)sg.groups * sg.nkb * 64;
+        g.num_kb = sg.groups;
+        g.win_wv = sg.seg;
+        g.win_rows = sg.R;
+        g.m_step = sg.R;
+        g.m_tiles = (int)(((long long)c.N * c.H_out + sg.R - 1) / sg.R);
+        g.bn = pick_bn(c.C_out);
+        g.n_tiles = (c.C_out + g.bn - 1) / g.bn;
+        if (g.n_tiles != 1) return g;  // the packed weights are one resident column tile
+        g.bres = 1;
+        g.a_stage_bytes = ((128 + sg.nkb - 1) * 128 + 1023) / 1024 * 1024;
+        const int kbt = (int)(g.K / 64);
+        for (int slots = 4; slots >= 2; slots -= 2) {
+            g.nw_slots = slots;
+            g.extra_smem = slots * sg.slot;
+            if (igemm_pick_stages(g.bn, 1, kbt, g.a_stage_bytes, 1, g.extra_smem + kEpiStageBytes) >=
+                4)
+                break;
+        }
+        g.stages = igemm_pick_stages(g.bn, 1, kbt, g.a_stage_bytes, 1, g.extra_smem);
+        // the raw weights land in the A stages before they are packed
+        g.min_stages = std::max(2, (int)((sg.wbytes + g.a_stage_bytes - 1) / g.a_stage_bytes));
+        if (g.stages < g.min_stages) g.stages = 0;
         return g;
     }
     if (path == CONVGB_PATH_IM2WIN) {
@@ -771,7 +859,10 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     if (g.K % 8 != 0) return CONVGB_ERR_UNSUPPORTED;  // TMA row pitch must be 16-byte aligned
     memset(out, 0, sizeof *out);
     out->plan = g;
-    if (!encode_kmajor(&out->tb, a.w, a.C_out, g.K, g.pair ? g.bn / 2 : g.bn)) return CONVGB_ERR_CUDA;
+    // (the staged-window stem packs its weights in the kernel: no weight map)
+    if (!is_stemwin(g.amode) &&
+        !encode_kmajor(&out->tb, a.w, a.C_out, g.K, g.pair ? g.bn / 2 : g.bn))
+        return CONVGB_ERR_CUDA;
     if (g.amode == kADense && !encode_kmajor(&out->ta, a.a_dense, g.M, g.K, 128))
         return CONVGB_ERR_CUDA;
     if (g.amode == kAIm2win) {
@@ -797,7 +888,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         // row tiles: the tile's win_rows output rows, consecutive in y; plane
         // tiles: one output row per box (their rows are not consecutive)
         const int box_rows = (window || g.amode == kANarrowWin || g.amode == kAIm2win ||
-                              g.amode == kAStrided)
+                              g.amode == kAStrided || is_stemwin(g.amode))
                                  ? g.win_rows * a.shape->W_out
                              : plane                             ? a.shape->W_out
                                                                  : 128;
@@ -858,6 +949,33 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.nw_kwcp = nr.kwcp;
         p.nw_slot_bytes = nr.slot;
         p.nw_slots = g.nw_slots;
+    }
+    if (is_stemwin(g.amode)) {
+        const ConvShape& c = *a.shape;
+        const StemWinGeom sg = stemwin_geom(c);
+        p.w = static_cast<const uint16_t*>(a.w);
+        p.win_wv = sg.seg;
+        p.win_rows = sg.R;
+        p.win_groups = c.N * c.H_out;
+        p.win_wout = c.W_out;
+        p.ho_div = FastDiv((uint32_t)c.H_out);
+        p.nw_H = c.H;
+        p.nw_W = c.W;
+        p.nw_KH = c.KH;
+        p.nw_s = c.s;
+        p.nw_p = c.p;
+        p.nw_cin = c.C_in;
+        p.nw_rb = sg.rb;
+        p.nw_a0 = sg.a0;
+        p.nw_slot_bytes = sg.slot;
+        p.nw_slots = g.nw_slots;
+        p.sw_kc = sg.KC;
+        p.sw_khg = sg.khg;
+        p.sw_nkb = sg.nkb;
+        p.sw_last = sg.last_steps;
+        p.sw_steps = (sg.nkb - 1) * 4 + sg.last_steps;
+        p.sw_kw = c.KW;
+        p.sw_wbytes = (int)sg.wbytes;
     }
     if (g.amode == kAIm2win || g.amode == kAStrided) {
         const ConvShape& c = *a.shape;
@@ -939,7 +1057,8 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
     if (y_dtype != CONVGB_BF16 && y_dtype != CONVGB_F32) return CONVGB_ERR_INVALID_ARG;
     if (path == CONVGB_PATH_AUTO) path = select_path(c);
     if (path != CONVGB_PATH_GATHER && path != CONVGB_PATH_DENSE && path != CONVGB_PATH_STEM &&
-        path != CONVGB_PATH_WINDOW && path != CONVGB_PATH_PLANE && path != CONVGB_PATH_IM2WIN)
+        path != CONVGB_PATH_WINDOW && path != CONVGB_PATH_PLANE && path != CONVGB_PATH_IM2WIN &&
+        path != CONVGB_PATH_STEMWIN)
         return CONVGB_ERR_INVALID_ARG;
     if (!path_supports(path, c)) return CONVGB_ERR_UNSUPPORTED;
     WsLayout L = workspace_layout(path, c);
@@ -966,7 +1085,8 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
         // 1x1 stride s: x read by element-strided boxes.
         a.a_dense = x;
         a.shape = &c;
-    } else if (path == CONVGB_PATH_WINDOW || path == CONVGB_PATH_PLANE) {
+    } else if (path == CONVGB_PATH_WINDOW || path == CONVGB_PATH_PLANE ||
+               path == CONVGB_PATH_STEMWIN) {
         a.x = static_cast<const uint16_t*>(x);
         a.C_in = C_in;
         a.shape = &c;
@@ -1293,7 +1413,8 @@ convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_ou
     const GemmPlan g = plan_gemm(path, c, y_dtype == CONVGB_F32 ? 1 : 0);
     const bool plane = g.amode == kAPlane || g.amode == kAPlane3 || g.amode == kAPlane3U2;
     const bool rowtiles = g.amode == kAWindow || g.amode == kAWindowPair ||
-                          g.amode == kANarrowWin || g.amode == kAIm2win || g.amode == kAStrided;
+                          g.amode == kANarrowWin || g.amode == kAIm2win || g.amode == kAStrided ||
+                          is_stemwin(g.amode);
     out->path = path;
     out->a_mode = g.amode;
     out->bn = g.bn;

@@ -67,7 +67,12 @@ constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kSmemLimit = 232448;    // opt-in dynamic shared memory per block
 constexpr int kMaxAcc = 4;
 constexpr int kMaxSlots = 4;  // narrow window: staged-row slots
-static_assert((4 * kMaxStages + 2 * kMaxAcc + 2 + 2 * kMaxSlots) * 8 + 8 + 36 + 8 <= kHeaderBytes,
+// Staged-window stem: 16-column MMA steps per stage.  The issue sequence is
+// unrolled to this length; measured on the 7x7 stride-2 stem, a 32-step
+// sequence ran 111 us against 65 us at 16 (the hot loops of all roles have to
+// share the instruction caches).
+constexpr int kStemWinMaxSteps = 16;
+static_assert((4 * kMaxStages + 2 * kMaxAcc + 3 + 2 * kMaxSlots) * 8 + 8 + 36 + 8 <= kHeaderBytes,
               "header area");
 
 template <int BN>
@@ -298,6 +303,81 @@ __device__ __forceinline__ void mma_commit_to(uint64_t* bar, bool both = true)
         ptx::mma_commit(bar);
 }
 
+// ------------------------------------------------------------ staged-window stem
+// Three input channels; the stride (a template argument) fixes KC = 64/s values
+// per input column and khg = KC / 3 kernel rows per group, so the builders below
+// have static register indices.
+
+// Row i of a staged-window stage (128-byte swizzle): the S input columns
+// s*r - p .. s*r - p + S - 1 of tile row j (the caller's col_e is the element
+// of the first of them inside a staged input row), each as KC values: value
+// kl*C + ci of column q is x[h = ho*s - p + kh0 + kl][column][ci], zero where
+// kh0 + kl >= KH, where row h lies outside the image (bit kh of hvalid clear),
+// and in the KC - khg*C padding values.  Columns outside the image read the
+// staged rows' zero borders.
+template <int C, int S>
+__device__ __forceinline__ void stemwin_row(uint8_t* stage, int i, const uint16_t* rows_j, int rbe,
+                                            int col_e, int kh0, int KH, uint32_t hvalid)
+{
+    constexpr int KC = 64 / S, KHG = KC / C;
+    uint32_t v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = 0u;
+#pragma unroll
+    for (int kl = 0; kl < KHG; ++kl) {
+        const int kh = kh0 + kl;
+        if (kh < KH && ((hvalid >> kh) & 1u)) {
+            const uint16_t* src = rows_j + kh * rbe + col_e;
+#pragma unroll
+            for (int q = 0; q < S; ++q)
+#pragma unroll
+                for (int ci = 0; ci < C; ++ci) {
+                    const int idx = q * KC + kl * C + ci;
+                    v[idx >> 1] |= static_cast<uint32_t>(src[q * C + ci]) << (16 * (idx & 1));
+                }
+        }
+    }
+#pragma unroll
+    for (int q16 = 0; q16 < 8; ++q16)
+        *reinterpret_cast<uint4*>(stage + i * 128 + ((q16 ^ (i & 7)) << 4)) =
+            make_uint4(v[4 * q16], v[4 * q16 + 1], v[4 * q16 + 2], v[4 * q16 + 3]);
+}
+
+// Resident weights of the staged-window stem, from the raw [C_out][KH][KW][C_in]
+// weights parked in shared memory: block b = group * nkb + kb holds, for column
+// co, K value q*KC + kl*C + ci = w[co][group*khg + kl][kb*S + q][ci] (zero past
+// KH, KW and khg), as 128-byte swizzled K-major rows like a TMA-loaded tile.
+template <int C, int S>
+__device__ __forceinline__ void stemwin_pack(uint8_t* sB, const uint16_t* raw, int bn, int C_out,
+                                             int KH, int KW, int nkb, int kbt, int tid, int nthr)
+{
+    constexpr int KC = 64 / S, KHG = KC / C;
+    const int total = kbt * bn * 8;  // 16-byte chunks
+    const int rowlen = KH * KW * C;
+    for (int e = tid; e < total; e += nthr) {
+        const int b = e / (bn * 8);
+        const int rem = e - b * bn * 8;
+        const int co = rem >> 3, cc = rem & 7;
+        const int grp = b / nkb, kb = b - grp * nkb;
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+        if (co < C_out) {
+            const uint16_t* wr = raw + co * rowlen;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int k = cc * 8 + t;
+                const int q = k / KC, r2 = k - q * KC;
+                const int kl = r2 / C, ci = r2 - kl * C;
+                const int kw = kb * S + q, kh = grp * KHG + kl;
+                uint32_t val = 0u;
+                if (kl < KHG && kh < KH && kw < KW) val = wr[(kh * KW + kw) * C + ci];
+                v[t >> 1] |= val << (16 * (t & 1));
+            }
+        }
+        *reinterpret_cast<uint4*>(sB + b * (bn * 128) + co * 128 + ((cc ^ (co & 7)) << 4)) =
+            make_uint4(v[0], v[1], v[2], v[3]);
+    }
+}
+
 template <int BN, int AMODE>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -308,8 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A written by the gather warps (signalled on full_a) or by the TMA warp
     // together with B (signalled on full_b).
     constexpr bool NARROWWIN = AMODE == kANarrowWin;
+    constexpr bool STEMWIN = is_stemwin(AMODE);
+    constexpr int SW_S = AMODE == kAStemWin1 ? 1 : AMODE == kAStemWin4 ? 4 : 2;  // its stride
+    constexpr bool STAGEDROWS = NARROWWIN || STEMWIN;  // input rows bulk-copied per tile
     constexpr bool TMAGATHER = AMODE == kATmaGather || AMODE == kATmaGatherPair;
-    constexpr bool GATHER = AMODE == kAGather || AMODE == kANarrow || TMAGATHER || NARROWWIN;
+    constexpr bool GATHER =
+        AMODE == kAGather || AMODE == kANarrow || TMAGATHER || NARROWWIN || STEMWIN;
     constexpr bool PAIR = AMODE == kAWindowPair || AMODE == kATmaGatherPair;  // CTA pair
     constexpr bool WINDOW = AMODE == kAWindow || AMODE == kAWindowPair;
     // B block bytes in this CTA's shared memory (a pair splits B's columns)
@@ -317,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool PLANE = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     constexpr bool IM2WIN = AMODE == kAIm2win;
     constexpr bool STRIDED = AMODE == kAStrided;
-    constexpr bool ROWTILES = WINDOW || NARROWWIN || IM2WIN || STRIDED;  // whole output rows
+    constexpr bool ROWTILES = WINDOW || STAGEDROWS || IM2WIN || STRIDED;  // whole output rows
     // Modes whose gather warps have nothing to gather run the epilogue on eight
     // warps: each thread converts 32 of a 64-column chunk's columns instead of
     // all 64 (the epilogue is latency-bound with one warp per scheduler).
@@ -337,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bres_full = drain + 1;          // resident weights loaded (tx bytes), count 1
     uint64_t* stg_full = bres_full + 1;       // narrow window: tile's rows staged (tx bytes)
     uint64_t* stg_empty = stg_full + kMaxSlots;  // narrow window: staged rows consumed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_empty + kMaxSlots);
+    uint64_t* wpack = stg_empty + kMaxSlots;     // staged-window stem: weights packed, count 1
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wpack + 1);
     uint32_t* abort_flag = tmem_slot + 1;
     // The 128-byte swizzle is a function of shared-memory address bits, so the
     // stage buffers must start on 1024-byte boundaries of the shared window.
@@ -354,10 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kTmemAlloc = PLANE ? 512u : static_cast<uint32_t>(C::kTmemCols);
     uint8_t* sA = data + b_blocks * BB;
     uint8_t* sStg = sA + S * AST;  // narrow window: nw_slots slots of staged input rows
-    const uint32_t NS = NARROWWIN ? static_cast<uint32_t>(p.nw_slots) : 1u;
+    const uint32_t NS = STAGEDROWS ? static_cast<uint32_t>(p.nw_slots) : 1u;
     // TMA-store epilogue: a 128 x 64 bf16 staging tile (128-byte swizzle) and the
     // current column tile's bias in fp32.
-    uint8_t* sEpi = sStg + (NARROWWIN ? NS * p.nw_slot_bytes : 0);
+    uint8_t* sEpi = sStg + (STAGEDROWS ? NS * p.nw_slot_bytes : 0);
     const int epi_tile = p.epi_c32 ? kEpiNarrowTileBytes : kEpiTileBytes;  // staging tile bytes
     float* sBias = reinterpret_cast<float*>(sEpi + p.epi_bufs * epi_tile);
     uint32_t* sVote = reinterpret_cast<uint32_t*>(abort_flag + 1);  // up to 8 epilogue-warp votes
@@ -389,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(bres_full, 1);
+        ptx::mbar_init(wpack, 1);
         for (int i = 0; i < kMaxSlots; ++i) {
             ptx::mbar_init(&stg_full[i], 1);
             ptx::mbar_init(&stg_empty[i], kGatherThreads);
@@ -400,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kTmaWarp && lane == 0) {
         if (AMODE == kADense || TMAGATHER || WINDOW || PLANE || IM2WIN || STRIDED)
             ptx::prefetch_tensormap(&tmap_a);
-        ptx::prefetch_tensormap(&tmap_b);
+        if (!STEMWIN) ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == kMmaWarp) {
         if (PAIR) {
@@ -411,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_relinquish();
         }
     }
-    if (NARROWWIN) {
+    if (STAGEDROWS) {
         // Staged rows keep their zero borders for the whole kernel: the bulk
         // copies only ever write row interiors.
         uint4* z = reinterpret_cast<uint4*>(sStg);
@@ -466,6 +552,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive(&tempty[acc]);
             }
         };
+        if (STEMWIN) {
+            // The raw weights land in the A stages (bres_full); pack them into the
+            // resident B tiles, then release the stages to the gather warps and
+            // the weights to the MMA thread (wpack).
+            if (wait_bar(bres_full, 0u, wc, kRoleEpilogue))
+                stemwin_pack<3, SW_S>(sB, reinterpret_cast<const uint16_t*>(sA), BN, p.C_out,
+                                      p.nw_KH, p.sw_kw, p.sw_nkb, p.kb_total, et, kEpiN);
+            ptx::fence_proxy_async_smem();
+            ptx::named_barrier_sync(1, kEpiN);
+            if (et == 0) ptx::mbar_arrive(wpack);
+        }
         const int wrow = (ROWTILES || PLANE) ? r / p.win_wv : 0;
         const int wcol = (ROWTILES || PLANE) ? r - wrow * p.win_wv : 0;
         uint32_t lt = 0;
@@ -849,6 +946,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (i % kGatherWarps == static_cast<uint32_t>(gw))
                         drain_wait(&full_a[i % S], (i / S) & 1u, 1000000000ull);
             }
+        } else if (STEMWIN) {
+            // Thread t builds stage row t = (tile row j, r) of every group of the
+            // tile; rows past the tile's segments keep stale values, which only
+            // discarded accumulator rows read.  Nothing is built before the
+            // weights are packed: their raw copy sits in the A stages until then.
+            const int t = threadIdx.x - kEpiThreads;  // 0..127
+            const int j = t / p.win_wv, r = t - j * p.win_wv;
+            const int rbe = p.nw_rb / 2;
+            const int col_e = (p.nw_a0 - p.nw_p * p.nw_cin * 2) / 2 + p.nw_s * r * p.nw_cin;
+            Ring ring;
+            uint32_t slot = 0, slot_phase = 0;
+            bool ok = wait_bar(wpack, 0u, wc, kRoleGather);
+            for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                const int rows = min(p.win_rows, p.win_groups - u.m0);
+                const bool live = j < rows;
+                uint32_t hvalid = 0u;
+                if (live) {
+                    uint32_t nn, hh;
+                    p.ho_div.divmod(static_cast<uint32_t>(u.m0 + j), nn, hh);
+                    const int h0 = static_cast<int>(hh) * p.nw_s - p.nw_p;
+                    for (int kh = 0; kh < p.nw_KH; ++kh)
+                        if (h0 + kh >= 0 && h0 + kh < p.nw_H) hvalid |= 1u << kh;
+                }
+                if (!wait_bar(&stg_full[slot], slot_phase, wc, kRoleGather)) {
+                    ok = false;
+                    break;
+                }
+                const uint16_t* rows_j = reinterpret_cast<const uint16_t*>(sStg + slot * p.nw_slot_bytes) +
+                                         j * p.nw_KH * rbe;
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
+                    if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleGather)) {
+                        ok = false;
+                        break;
+                    }
+                    if (live)
+                        stemwin_row<3, SW_S>(sA + ring.stage * AST, t, rows_j, rbe, col_e,
+                                             kb * p.sw_khg, p.nw_KH, hvalid);
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(&full_a[ring.stage]);
+                }
+                ptx::mbar_arrive(&stg_empty[slot]);
+                if (++slot == NS) {
+                    slot = 0;
+                    slot_phase ^= 1u;
+                }
+            }
         } else if (NARROWWIN) {
             // Thread t builds A row t: output pixel (tile row j, column wo).  K is
             // (kh, kw*C_in + c) with each kh slice padded to nw_kwcp, so the slice
@@ -1188,7 +1332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         // Thread-written A stages (cp.async, st.shared) are read by the
                         // tensor core through the async proxy.
-                        if (AMODE == kAGather || AMODE == kANarrow || NARROWWIN)
+                        if (AMODE == kAGather || AMODE == kANarrow || NARROWWIN || STEMWIN)
                             ptx::fence_proxy_async_smem();
                         ptx::tc_fence_after();
                         // Descriptors as slot bases plus 16-byte-unit offsets: no
@@ -1220,6 +1364,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                       bd0 + kw * bstep + 2 * kk, idesc,
                                                       (kw != 0 || kk != 0) ? 1u : first);
                             }
+                        } else if (STEMWIN) {
+                            // One stage (kernel-row group kb) feeds its nkb K blocks: K
+                            // block j of output pixel (row) i is stage row i + j.  The
+                            // sequence is unrolled with compile-time descriptor offsets
+                            // (step q: K block q / 4, 16-column step q % 4) so that no
+                            // arithmetic sits between the MMAs (an N=64 MMA lasts ~48
+                            // cycles, less than a run-time loop's descriptor updates).
+                            const uint64_t bd0 =
+                                b_desc0 + static_cast<uint32_t>(kb * p.sw_nkb) * b_blk_step;
+                            const int nsteps = p.sw_steps;
+                            const uint32_t acc0 = kb != u.kb0 ? 1u : 0u;
+#pragma unroll
+                            for (int q = 0; q < kStemWinMaxSteps; ++q)
+                                if (q < nsteps)
+                                    mma_issue<PAIR>(d_tmem, ad + 8 * (q >> 2) + 2 * (q & 3),
+                                                    bd0 + (q >> 2) * b_blk_step + 2 * (q & 3), idesc,
+                                                    q != 0 ? 1u : acc0);
                         } else {
                             const uint64_t bd =
                                 b_desc0 + (p.bres ? static_cast<uint32_t>(kb) : ring.stage) * b_blk_step;
@@ -1269,7 +1430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return good;
             };
             Ring ring;
-            bool ok = send(!p.bres || waited(bres_full, 0u, false));
+            // (the staged-window stem's weights are ready once packed: wpack)
+            bool ok = send(!p.bres || waited(STEMWIN ? wpack : bres_full, 0u, false));
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
                 const Unit u = unit_of<BN, PAIR>(p, tile, rank);
@@ -1288,7 +1450,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            if (p.bres) {
+            if (STEMWIN) {
+                // raw weights into the A stages, packed there by the epilogue warps
+                ptx::mbar_arrive_expect_tx(bres_full, static_cast<uint32_t>(p.sw_wbytes));
+                ptx::bulk_copy_g2s(sA, p.w, static_cast<uint32_t>(p.sw_wbytes), bres_full);
+            } else if (p.bres) {
                 // Weights resident: every K block of the one column tile, once (in
                 // a pair each CTA holds half of the columns; CTA 0's barrier counts
                 // both halves).
@@ -1306,7 +1472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (the A loads below are issued at once; the weights' arrival is
                 // awaited by the MMA thread, and here only before exiting)
             }
-            if (NARROWWIN) {
+            if (STAGEDROWS) {
                 // Per tile: every input row its output rows read (KH per output row),
                 // copied whole into the tile's staging slot; rows outside the image
                 // are skipped (the consumer writes zeros for them).
@@ -1575,7 +1741,8 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
             configured[dev] = true;
         }
     }
-    const int extra = (AMODE == kANarrowWin ? p.nw_slots * p.nw_slot_bytes : 0) +
+    const int extra = ((AMODE == kANarrowWin || is_stemwin(AMODE)) ? p.nw_slots * p.nw_slot_bytes
+                                                                    : 0) +
                       (p.tma_store ? (p.epi_c32 ? kEpiNarrowStageBytes + (p.epi_bufs - 1) * kEpiNarrowTileBytes
                                                 : kEpiStageBytes + (p.epi_bufs - 1) * kEpiTileBytes)
                                    : 0);
@@ -1596,6 +1763,23 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
     constexpr bool kEpi8 = AMODE == kAWindow || AMODE == kAWindowPair || AMODE == kADense ||
                            AMODE == kAIm2win || AMODE == kAStrided;
     if (p.epi_c32 && !(kEpi8 && p.tma_store)) return cudaErrorInvalidValue;
+    if ((AMODE == kANarrowWin || is_stemwin(AMODE)) && (p.nw_slots < 1 || p.nw_slots > kMaxSlots))
+        return cudaErrorInvalidValue;
+    if (is_stemwin(AMODE)) {
+        // every shared-memory access of the stem's stages and packing stays in bounds:
+        // one stage row per gather thread, 128 + nkb - 1 rows per stage, the raw
+        // weights inside the A stages, kernel rows in the 32-bit validity mask, and a
+        // (C_in, stride) pair the builder is compiled for
+        constexpr int kS = AMODE == kAStemWin1 ? 1 : AMODE == kAStemWin4 ? 4 : 2;
+        const bool cs_ok = p.nw_cin == 3 && p.nw_s == kS && p.sw_kc == 64 / p.nw_s &&
+                           p.sw_khg == p.sw_kc / p.nw_cin;
+        if (!cs_ok || !p.bres || p.n_tiles != 1 || p.win_rows * p.win_wv > kGatherThreads ||
+            (BM + p.sw_nkb - 1) * 128 > p.a_stage_bytes || p.nw_KH > 31 ||
+            p.sw_wbytes > p.stages * p.a_stage_bytes || p.sw_wbytes % 16 != 0 ||
+            p.kb_total != p.num_kb * p.sw_nkb || p.sw_last < 1 || p.sw_last > 4 ||
+            p.sw_steps != (p.sw_nkb - 1) * 4 + p.sw_last || p.sw_steps > kStemWinMaxSteps)
+            return cudaErrorInvalidValue;
+    }
     if (kPlane &&
         ((!p.bres && (p.b_stages < 2 || p.b_stages > kMaxStages)) || p.pl_u < 1 || p.pl_u > 2 ||
          p.pl_nacc < 1 || p.pl_nacc > kMaxAcc || p.pl_nacc * p.pl_u * BN > 512))
@@ -1714,6 +1898,9 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kAPlane: return launch_mode<kAPlane>(bn, ta, tb, ty, p, st);
     case kAPlane3: return launch_mode<kAPlane3>(bn, ta, tb, ty, p, st);
     case kAPlane3U2: return launch_mode<kAPlane3U2>(bn, ta, tb, ty, p, st);
+    case kAStemWin: return launch_mode<kAStemWin>(bn, ta, tb, ty, p, st);
+    case kAStemWin1: return launch_mode<kAStemWin1>(bn, ta, tb, ty, p, st);
+    case kAStemWin4: return launch_mode<kAStemWin4>(bn, ta, tb, ty, p, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -76,6 +76,13 @@ struct IgemmParams {
     int nw_kwc, nw_kwcp;     // KW*C_in, and that padded to a multiple of 8
     int nw_slot_bytes;       // bytes of one tile's staged rows
     int nw_slots;            // staged-row slots (2 or 4)
+    // staged-window stem (kAStemWin): KC = 64/s values (kh, ci) per input column,
+    // sw_khg kernel rows per stage (a group), sw_nkb K blocks read from a stage,
+    // the last of them sw_last 16-column steps long; the raw weights [C_out][K]
+    // (sw_wbytes bytes at w) are packed into the resident B tiles by the kernel
+    const uint16_t* w;
+    int sw_kc, sw_khg, sw_nkb, sw_last, sw_kw, sw_wbytes;
+    int sw_steps;            // 16-column MMA steps per stage: (sw_nkb - 1) * 4 + sw_last
     // plane mode (stride 1): the batch is one tall padded image of N*(H+2p)
     // virtual rows; a tile is pl_u sub-tiles of win_rows virtual output rows,
     // its A stage for channel block cc holds pl_srows whole padded input rows,
@@ -141,7 +148,22 @@ enum AMode : int {
                       // uses; tiles of whole output rows of one image
     kATmaGatherPair = 12,  // TMA gather4 on a cluster of two CTAs (tcgen05.mma.cta_group::2,
                            // 256 rows); each CTA holds half of the weight columns
+    kAStemWin = 13,   // three input channels, stride 2 (kAStemWin1, kAStemWin4: stride 1, 4):
+                      // per tile, a window-order stage in shared memory whose 128-byte row
+                      // r holds input columns s*r-p .. s*r-p+s-1, each as KC = 64/s values
+                      // (kh, ci); output pixel wo's K block kb is row wo + kb, so one stage
+                      // feeds every K block at shifted starts.  One kernel per stride: each
+                      // holds the one stage builder it runs (with the builders of all three
+                      // strides in one kernel the 7x7 stride-2 stem ran 100 us, not 65)
+    kAStemWin1 = 14,
+    kAStemWin4 = 15,
 };
+// The staged-window stem's A mode for a stride (1, 2 or 4).
+constexpr int stemwin_amode(int s) { return s == 1 ? kAStemWin1 : s == 4 ? kAStemWin4 : kAStemWin; }
+constexpr bool is_stemwin(int amode)
+{
+    return amode == kAStemWin || amode == kAStemWin1 || amode == kAStemWin4;
+}
 // Fewest ring stages the TMA-gather modes run with: their four gather warps
 // fill the stages by turns, and each warp's wait on a stage's release must be
 // at most one barrier phase ahead of it.

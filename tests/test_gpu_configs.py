@@ -146,5 +146,8 @@ def test_full_size_plane_path_sampled(gpu_lib, shape):
 
 
 @pytest.mark.parametrize("shape", [c for c in FULL if c.C_in % 8 != 0], ids=lambda s: s.name)
-def test_full_size_stem_path_sampled(gpu_lib, shape):
-    check_per_tile(gpu_lib, shape, gpu_lib.PATH_STEM)
+@pytest.mark.parametrize("path", ["stem", "im2win"])
+def test_full_size_other_stem_paths_sampled(gpu_lib, shape, path):
+    """The staged-row and im2win paths, which conv2d_fwd no longer picks for
+    these layers, at full size."""
+    check_per_tile(gpu_lib, shape, gpu_lib.PATH_STEM if path == "stem" else gpu_lib.PATH_IM2WIN)
