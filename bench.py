@@ -352,7 +352,7 @@ class Layer:
         n += 1 if a in (1, 2, 3, 12) else 0      # build_indirection_kernel
         n += 1 if a in (2, 5, 10) else 0         # weight re-pack
         n += 1 if a == 10 else 0                 # im2win re-layout
-        n += 1 if p["splits"] > 1 else 0         # finish_split_kernel
+        n += 1 if p["splits"] > 1 or p["stream_k"] else 0  # finish_split_kernel
         return n
 
 
@@ -534,16 +534,19 @@ def ablation_rows():
         rows.append(("strided_3x3_s2_128to256_56", "bn=%d" % bn, bn, 0, 0, 0))
         rows.append(("sweep_1x1_512to2048_7", "bn=%d" % bn, bn, 0, 0, 0))
     for name in ("stem_7x7_s2_3to64_224", "sweep_11x11_s4_3to64_224"):
+        rows.append((name, "staged-window stem path (default)", 0, 0, 0, 0))
         rows.append((name, "im2win path", 0, 0, 6, 0))
         rows.append((name, "staged-row stem path", 0, 0, 3, 0))
         rows.append((name, "gather path, C_in padded to 8", 0, 0, 1, 8))
-    return [(R[a],) + r[1:] for r in rows for a in (r[0],)]
+    rows.append(("sweep_3x3_512c_7", "whole units (default)", 0, 0, 0, 0))
+    rows.append(("sweep_3x3_512c_7", "stream-K", 0, 0, 0, 0, 1))
+    return [(R[r[0]],) + tuple(r[1:]) + ((0,) if len(r) == 6 else ()) for r in rows]
 
 
 def run_ablation(g, dev, stream, steps):
     out = []
-    for c, label, bn, st, path, cin_pad in ablation_rows():
-        g.set_tuning(bn, st)
+    for c, label, bn, st, path, cin_pad, sk in ablation_rows():
+        g.set_tuning(bn, st, sk)
         try:
             L = Layer(g, c, dev, path=path, cin_pad=cin_pad)
             ms = time_layer(L, steps, 3, stream)
@@ -552,7 +555,8 @@ def run_ablation(g, dev, stream, steps):
             ent = {"workload": c.name, "variant": label, "us": ms * 1e3,
                    "tflops": L.num["flops"] / (ms * 1e-3) / 1e12,
                    "plan": {k: plan[k] for k in ("path", "a_mode", "bn", "stages",
-                                                 "weights_resident", "cta_pair", "splits")},
+                                                 "weights_resident", "cta_pair", "splits",
+                                                 "stream_k")},
                    "device_status": st_}
             del L
             torch.cuda.empty_cache()

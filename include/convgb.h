@@ -166,6 +166,8 @@ typedef struct convgb_plan {
     int tma_store;        /* 1: the epilogue stores y through shared memory with TMA */
     int epilogue_tiles;   /* staging tiles of that epilogue (0, 1 or 2) */
     int epilogue_c32;     /* 1: 32-column staging chunks instead of 64 */
+    int stream_k;         /* 1: each CTA (pair) takes an equal share of all (tile, K block)
+                             steps; tiles split between CTAs meet in fp32 partial sums */
 } convgb_plan;
 
 /* Fills *plan with what conv2d_fwd_path(path, ...) would launch for this shape
@@ -175,14 +177,18 @@ CONVGB_API convgb_status convgb_plan_info(int path, int N, int C_in, int H, int 
                                           int KH, int KW, int stride, int pad, int dilation,
                                           int y_dtype, convgb_plan* plan);
 
-/* Overrides two choices of the planner for every later call in this process,
- * for tuning and ablation studies (an interface addition; not from the pages):
+/* Overrides choices of the planner for every later call in this process, for
+ * tuning and ablation studies (an interface addition; not from the pages):
  * bn = 32, 64, 128 or 256 forces that tile width (0 = the planner's choice);
  * max_stages = 2..8 caps the shared-memory ring depth of the finished plan
- * (0 = no cap).  Other values mean 0.  Results stay exact, only speed changes;
- * a forced width may also change the workspace size, so query it after this
- * call.  Not synchronised with calls running on other host threads. */
-CONVGB_API void convgb_set_tuning(int bn, int max_stages);
+ * (0 = no cap; the TMA-gather modes keep at least four stages);
+ * stream_k = 1 lets layers whose units fill less than nine tenths of a wave
+ * share out all (tile, K block) steps equally between CTAs, meeting in fp32
+ * partial sums (0 = whole units, the default).  Other values mean 0.  Results
+ * stay within the parity bounds, only speed changes; a setting may change the
+ * workspace size, so query it after this call.  Not synchronised with calls
+ * running on other host threads. */
+CONVGB_API void convgb_set_tuning(int bn, int max_stages, int stream_k);
 
 /*
  * conv2d_fwd -- forward convolution, y = conv(x, w) + bias.

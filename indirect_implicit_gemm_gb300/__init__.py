@@ -52,7 +52,8 @@ class Plan(ctypes.Structure):
     """convgb_plan: what conv2d_fwd_path launches for a shape (include/convgb.h)."""
     _fields_ = [(n, ctypes.c_int) for n in (
         "path", "a_mode", "bn", "m_tiles", "tile_rows", "n_tiles", "splits", "k_blocks", "stages",
-        "weights_resident", "cta_pair", "tma_store", "epilogue_tiles", "epilogue_c32")]
+        "weights_resident", "cta_pair", "tma_store", "epilogue_tiles", "epilogue_c32",
+        "stream_k")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -117,7 +118,7 @@ def load():
     lib.convgb_selftest_wait_timeout.restype = I
     lib.convgb_plan_info.argtypes = [I] + shape10 + [I, ctypes.POINTER(Plan)]
     lib.convgb_plan_info.restype = I
-    lib.convgb_set_tuning.argtypes = [I, I]
+    lib.convgb_set_tuning.argtypes = [I, I, I]
     lib.convgb_set_tuning.restype = None
     lib.convgb_version.argtypes = []
     lib.convgb_version.restype = I
@@ -161,9 +162,10 @@ def plan_info(N, C_in, H, W, C_out, KH, KW, stride=1, pad=0, dilation=1, path=PA
     return p.as_dict()
 
 
-def set_tuning(bn: int = 0, max_stages: int = 0):
-    """Force the tile width and/or cap the ring depth of later plans (0 = automatic)."""
-    load().convgb_set_tuning(int(bn), int(max_stages))
+def set_tuning(bn: int = 0, max_stages: int = 0, stream_k: int = 0):
+    """Force the tile width, cap the ring depth and/or allow stream-K in later plans
+    (0 = the planner's own choice)."""
+    load().convgb_set_tuning(int(bn), int(max_stages), int(stream_k))
 
 
 def output_dims(H, W, KH, KW, stride=1, pad=0, dilation=1):

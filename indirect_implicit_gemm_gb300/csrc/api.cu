@@ -27,6 +27,7 @@ std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
 // the planner's own choice.
 std::atomic<int> g_tune_bn{0};
 std::atomic<int> g_tune_stages{0};
+std::atomic<int> g_tune_stream_k{0};
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -362,6 +363,7 @@ struct GemmPlan {
     int pl_u = 1, pl_nacc = 0, b_stages = 0;  // plane mode: sub-tiles, accumulators, B slots
     int pair = 0;                  // window mode on a CTA pair (each CTA holds bn/2 columns of B)
     int min_stages = 2;            // shallowest ring the mode runs with (a tuning cap stops here)
+    int sk = 0;                    // stream-K: CTAs share out all (unit, K block) iterations
     long long M = 0, K = 0;
     int num_kb = 0, m_tiles = 0, n_tiles = 0;
 };
@@ -395,7 +397,7 @@ int choose_splits(long long tiles, int num_kb, long long partial_bytes, long lon
 // aligned, no split) and the ring still has two stages with its staging tile.
 void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
 {
-    if (y_f32 || c.C_out % 8 != 0 || g.splits != 1 || g.bn < 64 || g.stages < 2) return;
+    if (y_f32 || c.C_out % 8 != 0 || g.splits != 1 || g.sk || g.bn < 64 || g.stages < 2) return;
     const int kb_res = g.bres ? (int)((g.K + 63) / 64) : g.num_kb;
     const int bnb = g.pair ? g.bn / 2 : g.bn;
     const int s = igemm_pick_stages(bnb, g.bres, kb_res, g.a_stage_bytes, g.b_per_stage,
@@ -451,9 +453,37 @@ void cap_stages(GemmPlan& g)
     if (g.stages > cap) g.stages = cap;
 }
 
+// Stream-K for layers whose work units fill less than one wave of the GPU
+// (e.g. 64 pairs of 512-channel 3x3 tiles at 7x7 on 76 SM pairs): every CTA
+// (pair) takes an equal share of all (unit, K block) iterations instead of
+// whole units, and the units split between CTAs meet in the fp32 partial-sum
+// buffer, which a finishing pass turns into y.  Eligible when at least a tenth
+// of the CTAs would otherwise idle and the sums stay small enough to live in
+// L2.  Taken only when asked for (convgb_set_tuning): on the 512-channel 3x3
+// layer at 7x7 it measured 45.7 us against 35.7 us for whole units (the fp32
+// round trip and its atomics cost more than the idle pairs; that layer is
+// bound by streaming its weights through L2).
+void plan_stream_k(GemmPlan& g, const ConvShape& c)
+{
+    if (g_tune_stream_k.load(std::memory_order_relaxed) != 1) return;
+    const bool mode = g.amode == kAWindow || g.amode == kAWindowPair || g.amode == kADense ||
+                      g.amode == kAGather || g.amode == kATmaGather ||
+                      g.amode == kATmaGatherPair;
+    if (!mode || g.splits != 1 || (g.bres && g.n_tiles > 1) || g.stages < 2) return;
+    constexpr int kNominalSms = 148;
+    const long long units = (long long)(g.pair ? (g.m_tiles + 1) / 2 : g.m_tiles) * g.n_tiles;
+    const int ctas = g.pair ? kNominalSms / 2 : kNominalSms;
+    if (units >= ctas || (double)units >= 0.9 * ctas) return;
+    const long long partial = c.M * c.C_out * 4;
+    if (partial > (32LL << 20) || partial >= c.M * c.K * 2 / 2) return;
+    if ((long long)g.num_kb * units < 2LL * ctas) return;  // too few iterations to share
+    g.sk = 1;
+}
+
 GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32)
 {
     GemmPlan g = path == CONVGB_PATH_PLANE ? plan_plane(c, y_f32) : plan_gemm_ring(path, c);
+    if (path != CONVGB_PATH_PLANE) plan_stream_k(g, c);
     if (path != CONVGB_PATH_PLANE) plan_epilogue(g, c, y_f32);
     cap_stages(g);
     return g;
@@ -642,7 +672,11 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         g.m_tiles = (int)((long long)c.N * c.H_out / R);
         g.bn = pick_bn(c.C_out);
         g.n_tiles = (c.C_out + g.bn - 1) / g.bn;
-        if (g.n_tiles == 1 && igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
+        // Weights resident: the whole matrix, or with several column tiles the
+        // CTA's own one (each CTA then takes the tiles of one column tile only)
+        // when it leaves a 4-deep ring beside the epilogue's staging.
+        if ((g.n_tiles == 1 && igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1) >= 4) ||
+            igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1, kEpiStageBytes) >= 4)
             g.bres = 1;
         g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb, g.a_stage_bytes, 1);
         return g;
@@ -754,8 +788,13 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
     const int bnb = g.pair ? g.bn / 2 : g.bn;
     // Layers whose whole weight matrix is one column tile: keep it in shared
     // memory for the CTA's lifetime when that still leaves a 4-deep A ring.
-    if (g.n_tiles == 1 && g.splits == 1 &&
-        igemm_pick_stages(bnb, 1, g.num_kb, g.a_stage_bytes, 1) >= 4)
+    // With several column tiles, a CTA keeps its own column tile's weights when
+    // they leave that ring beside the epilogue's staging: the launch makes the
+    // grid a multiple of the column tiles, so each CTA's tiles share one.
+    if (g.splits == 1 &&
+        ((g.n_tiles == 1 && igemm_pick_stages(bnb, 1, g.num_kb, g.a_stage_bytes, 1) >= 4) ||
+         (g.n_tiles > 1 && !g.pair &&
+          igemm_pick_stages(bnb, 1, g.num_kb, g.a_stage_bytes, 1, kEpiStageBytes) >= 4)))
         g.bres = 1;
     g.stages = igemm_pick_stages(bnb, g.bres, g.num_kb, g.a_stage_bytes, 1);
     if ((g.amode == kATmaGather || g.amode == kATmaGatherPair) &&
@@ -820,7 +859,7 @@ WsLayout workspace_layout(int path, const ConvShape& c)
         L.wpad_bytes = (size_t)c.C_out * g.K * 2;
         at = align_up(at + L.wpad_bytes, kAlign);
     }
-    if (g.splits > 1) {
+    if (g.splits > 1 || g.sk) {
         L.part_off = at;
         L.part_bytes = (size_t)c.M * c.C_out * sizeof(float);
         at = align_up(at + L.part_bytes, kAlign);
@@ -920,6 +959,9 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     p.n_tiles = g.n_tiles;
     p.splits = g.splits;
     p.split_div = FastDiv((uint32_t)g.splits);
+    p.sk = g.sk;
+    p.sk_iters = (long long)(g.pair ? (g.m_tiles + 1) / 2 : g.m_tiles) * g.n_tiles * g.num_kb;
+    p.sk_ctas = 1;  // set at launch
     p.ntile_div = FastDiv((uint32_t)g.n_tiles);
     p.tma_store = g.tma_store;
     p.epi_bufs = g.epi_bufs;
@@ -1026,7 +1068,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     p.y_f32 = a.y_f32;
     p.timeout_ns = g_timeout_ns.load();
     p.err = err;
-    if (g.splits > 1 && a.partial == nullptr) return CONVGB_ERR_WORKSPACE;
+    if ((g.splits > 1 || g.sk) && a.partial == nullptr) return CONVGB_ERR_WORKSPACE;
     return CONVGB_OK;
 }
 
@@ -1035,12 +1077,13 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
 convgb_status launch_gemm(const PreparedGemm& pg, cudaStream_t st)
 {
     const IgemmParams& p = pg.p;
-    if (p.splits > 1 &&
+    const bool sums = p.splits > 1 || p.sk;  // partial sums in the fp32 buffer
+    if (sums &&
         cudaMemsetAsync(p.partial, 0, (size_t)p.M * p.C_out * sizeof(float), st) != cudaSuccess)
         return CONVGB_ERR_CUDA;
     if (launch_igemm(pg.plan.amode, pg.plan.bn, pg.ta, pg.tb, pg.ty, p, st) != cudaSuccess)
         return CONVGB_ERR_CUDA;
-    if (p.splits > 1 &&
+    if (sums &&
         launch_finish_split(p.partial, p.bias, p.y, p.M, p.C_out, p.y_f32, st) != cudaSuccess)
         return CONVGB_ERR_CUDA;
     return CONVGB_OK;
@@ -1429,13 +1472,15 @@ convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_ou
     out->tma_store = g.tma_store;
     out->epilogue_tiles = g.tma_store ? g.epi_bufs : 0;
     out->epilogue_c32 = g.epi_c32;
+    out->stream_k = g.sk;
     return CONVGB_OK;
 }
 
-void convgb_set_tuning(int bn, int max_stages)
+void convgb_set_tuning(int bn, int max_stages, int stream_k)
 {
     g_tune_bn.store((bn == 32 || bn == 64 || bn == 128 || bn == 256) ? bn : 0);
     g_tune_stages.store((max_stages >= 2 && max_stages <= 8) ? max_stages : 0);
+    g_tune_stream_k.store(stream_k == 1 ? 1 : 0);
 }
 
 int convgb_version(void) { return 101; }

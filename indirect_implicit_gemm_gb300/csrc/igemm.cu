@@ -237,6 +237,12 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, int m, int co0
 struct Unit {
     int m0, n0, kb0, kb1;
 };
+// Stream-K: this CTA's (or pair's) share of the flattened (unit, K block)
+// iterations, [g0, g1), which starts in unit u0 and ends in unit u1.
+struct SkRange {
+    long long g0 = 0, g1 = 0;
+    int u0 = 0, u1 = -1;
+};
 // Every role evaluates this once per tile, and on the MMA thread it sits
 // between two tiles' MMA groups, so it uses the host-prepared multiply-shift
 // dividers (a run-time division, and above all a 64-bit one, costs hundreds of
@@ -244,8 +250,22 @@ struct Unit {
 // Pair mode: unit `tile` is a pair of consecutive output tiles, the CTA of
 // rank r taking tile 2*m + r.
 template <int BN, bool PAIRED = false>
-__device__ __forceinline__ Unit unit_of(const IgemmParams& p, int tile, uint32_t rank = 0)
+__device__ __forceinline__ Unit unit_of(const IgemmParams& p, int tile, uint32_t rank,
+                                        const SkRange& sk)
 {
+    if (p.sk) {
+        // stream-K: the CTA's tile-th segment, unit u0 + tile, cut to [g0, g1)
+        const int uu = sk.u0 + tile;
+        uint32_t mt = static_cast<uint32_t>(uu), nt = 0;
+        if (p.n_tiles > 1) p.ntile_div.divmod(static_cast<uint32_t>(uu), mt, nt);
+        Unit u;
+        u.m0 = static_cast<int>(PAIRED ? 2u * mt + rank : mt) * p.m_step;
+        u.n0 = static_cast<int>(nt) * BN;
+        u.kb0 = tile == 0 ? static_cast<int>(sk.g0 - static_cast<long long>(sk.u0) * p.num_kb) : 0;
+        u.kb1 = uu == sk.u1 ? static_cast<int>(sk.g1 - static_cast<long long>(sk.u1) * p.num_kb)
+                            : p.num_kb;
+        return u;
+    }
     uint32_t mn = static_cast<uint32_t>(tile), ks = 0;
     if (p.splits > 1) p.split_div.divmod(static_cast<uint32_t>(tile), mn, ks);
     uint32_t mt = mn, nt = 0;
@@ -456,8 +476,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     // Pair mode: both CTAs walk the same sequence of pair units.
     const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
-    const int t_first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int t_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    // Work units: unit t_first, t_first + t_step, ... below total_tiles.  In
+    // stream-K mode the CTA (a pair: the cluster) takes the contiguous share
+    // [c*W/G, (c+1)*W/G) of the W = units * num_kb (unit, K block) iterations,
+    // walked as segments 0, 1, ... of the units it touches; partial sums meet
+    // in the fp32 buffer.
+    const int cta_idx = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    SkRange skr;
+    if (p.sk) {
+        const long long G = p.sk_ctas, W = p.sk_iters;
+        skr.g0 = cta_idx * W / G;
+        skr.g1 = (cta_idx + 1) * W / G;
+        skr.u0 = static_cast<int>(skr.g0 / p.num_kb);
+        skr.u1 = skr.g1 > skr.g0 ? static_cast<int>((skr.g1 - 1) / p.num_kb) : skr.u0 - 1;
+    }
+    const int t_first = p.sk ? 0 : cta_idx;
+    const int t_step = p.sk ? 1 : PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; ++s) {
@@ -523,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) ptx::grid_launch_dependents();
 
     const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
-    const int total_tiles = p.m_tiles * p.n_tiles * p.splits;
+    const int total_tiles = p.sk ? skr.u1 - skr.u0 + 1 : p.m_tiles * p.n_tiles * p.splits;
 
     if (warp < kEpiWarps || (EPI8 && warp < kEpiWarps + kGatherWarps)) {
         // ------------------------------------------------------------ epilogue
@@ -570,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int bias_n0 = -1;
         Ring ar;  // accumulator index and the parity of its current use
         for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt, ar.next(NACC)) {
-            const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+            const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
             const uint32_t acc = ar.stage;
             // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds,
             // and with the TMA store all four warps do (they share named barriers).
@@ -770,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         const int co0 = u.n0 + ch * 32;
                         if (live && co0 < p.C_out) {
-                            if (p.splits > 1)
+                            if (p.splits > 1 || p.sk)
                                 reduce_chunk(p, m, co0, ra);
                             else
                                 store_chunk(p, m, co0, ra);
@@ -787,13 +821,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (last_sub && ch + 2 >= BN / 32) release_acc(acc);
                         const int co0 = u.n0 + ch * 32;
                         if (live && co0 < p.C_out) {
-                            if (p.splits > 1)
+                            if (p.splits > 1 || p.sk)
                                 reduce_chunk(p, m, co0, ra);
                             else
                                 store_chunk(p, m, co0, ra);
                         }
                         if (live && ch + 1 < BN / 32 && co0 + 32 < p.C_out) {
-                            if (p.splits > 1)
+                            if (p.splits > 1 || p.sk)
                                 reduce_chunk(p, m, co0 + 32, rb);
                             else
                                 store_chunk(p, m, co0 + 32, rb);
@@ -820,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t issued = 0;
                 bool ok = true;
                 for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                    const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                    const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
                         if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleGather)) {
                             ok = false;
@@ -864,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      ++spin)
                     __nanosleep(256);
                 if (*aborted) break;
-                const Unit v = unit_of<BN, PAIR>(p, tile, rank);
+                const Unit v = unit_of<BN, PAIR>(p, tile, rank, skr);
                 if (v.n0 != 0 || v.kb0 != 0) continue;  // one prefetch per row block
                 for (int j = 0; j < p.pl_srows; ++j) {
                     uint32_t n, hp;
@@ -890,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring ring;
             bool ok = true;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                 int ib4[4];  // first indirection entry of the row's pixel, or -1
                 int nb4[4];  // first row of the pixel's image
 #pragma unroll
@@ -959,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t slot = 0, slot_phase = 0;
             bool ok = wait_bar(wpack, 0u, wc, kRoleGather);
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                 const int rows = min(p.win_rows, p.win_groups - u.m0);
                 const bool live = j < rows;
                 uint32_t hvalid = 0u;
@@ -1006,7 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t slot = 0, slot_phase = 0;
             bool ok = true;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                 const int rows = min(p.win_rows, p.win_groups - u.m0);
                 const bool row_live = j < rows;
                 int ho = 0;
@@ -1076,7 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring ring;
             bool ok = true;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                 int ib[kRowsPerGatherThread];        // pixel's first ibuf entry, or -1
                 long long xb[kRowsPerGatherThread];  // image base (elements)
 #pragma unroll
@@ -1207,7 +1241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles;
                  tile += t_step, ++lt, ar.next(NACC)) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                 const uint32_t acc = ar.stage;
                 if (!wait_bar(&tempty[acc], ar.phase ^ 1u, wc, kRoleMma)) break;
                 ptx::tc_fence_after();
@@ -1313,7 +1347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = receive();  // resident weights (or nothing to wait for)
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                 const uint32_t acc = ar.stage;
                 if (!receive()) break;  // accumulator drained by the epilogue
                 ptx::tc_fence_after();
@@ -1434,7 +1468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = send(!p.bres || waited(STEMWIN ? wpack : bres_full, 0u, false));
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                 if (!send(waited(&tempty[ar.stage], ar.phase ^ 1u, PAIR))) break;
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
                     bool good = !GATHER || waited(&full_a[ring.stage], ring.phase, false);
@@ -1462,12 +1496,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(bres_full, static_cast<uint32_t>(p.kb_total) * BB *
                                                               (PAIR ? 2u : 1u));
                 const uint32_t bres_bar = PAIR ? ptx::mapa(ptx::smem_addr(bres_full), 0u) : 0u;
+                // several column tiles: this CTA's (the grid is a multiple of their
+                // count, so every unit of the CTA has column tile blockIdx.x % n_tiles)
+                const int n0_res =
+                    p.n_tiles > 1 ? static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_tiles)) * BN
+                                  : 0;
                 for (int kb = 0; kb < p.kb_total; ++kb) {
                     if (PAIR)
                         ptx::tma_load_2d_pair(sB + kb * BB, &tmap_b, bres_bar, kb * BK,
                                               static_cast<int>(rank) * (BN / 2));
                     else
-                        ptx::tma_load_2d(sB + kb * BB, &tmap_b, bres_full, kb * BK, 0);
+                        ptx::tma_load_2d(sB + kb * BB, &tmap_b, bres_full, kb * BK, n0_res);
                 }
                 // (the A loads below are issued at once; the weights' arrival is
                 // awaited by the MMA thread, and here only before exiting)
@@ -1479,7 +1518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t row_bytes = static_cast<uint32_t>(p.nw_W * p.nw_cin * 2);
                 uint32_t slot = 0, slot_phase = 0, issued = 0;
                 for (int tile = t_first; tile < total_tiles; tile += t_step, ++issued) {
-                    const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                    const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                     if (!wait_bar(&stg_empty[slot], slot_phase ^ 1u, wc, kRoleTma)) break;
                     const int rows = min(p.win_rows, p.win_groups - u.m0);
                     uint32_t copies = 0;
@@ -1522,7 +1561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t issued = 0;
                     bool ok = true;
                     for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                        const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                        const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                         for (int kb = u.kb0; ok && kb < u.kb1; ++kb)
                             for (int t = 0; t < taps; ++t, ++issued, rb.next(SB)) {
                                 if (!wait_bar(&empty_b[rb.stage], rb.phase ^ 1u, wc, kRoleTma)) {
@@ -1553,11 +1592,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // that barrier, so CTA 0's drain below covers the peer's copies too
                 // (neither CTA exits before the final cluster barrier).
                 for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                    const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                    const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                     const int rows = max(0, min(p.win_rows, p.win_groups - u.m0));
                     int rows_peer = 0;
                     if (PAIR) {
-                        const Unit v = unit_of<BN, PAIR>(p, tile, 1u);
+                        const Unit v = unit_of<BN, PAIR>(p, tile, 1u, skr);
                         rows_peer = max(0, min(p.win_rows, p.win_groups - v.m0));
                     }
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
@@ -1616,7 +1655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t issued = 0;
                 bool ok = true;
                 for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                    const Unit u = unit_of<BN, PAIR>(p, tile, rank);
+                    const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
                         if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleTma)) {
                             ok = false;
@@ -1789,6 +1828,15 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         (p.x_KH != 3 || p.win_kw != 3 || p.pl_u != (AMODE == kAPlane3U2 ? 2 : 1)))
         return cudaErrorInvalidValue;
     const int tiles = p.m_tiles * p.n_tiles * p.splits;  // pair mode: pair units
+    IgemmParams q = p;  // this launch's copy: stream-K records its grid in it
+    if (p.sk) {
+        // stream-K shares out every (unit, K block) iteration: as many CTAs (pairs)
+        // as fit, each with at least one iteration; no split, no column-resident
+        // weights (a CTA's iterations cross column tiles), no plane mode
+        if (kPlane || p.splits != 1 || (p.bres && p.n_tiles > 1) || p.sk_iters < 1 ||
+            p.sk_iters != static_cast<long long>(p.m_tiles) * p.n_tiles * p.num_kb)
+            return cudaErrorInvalidValue;
+    }
     // Programmatic stream serialization: CTAs may start on SMs the previous
     // kernel has left while its other CTAs finish (the kernel waits for it
     // before touching global memory).
@@ -1827,15 +1875,29 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
             }
             resident = cluster_count[dev];
         }
-        const int clusters = tiles < resident ? tiles : resident;
+        int clusters = tiles < resident ? tiles : resident;
+        if (p.sk) {
+            clusters = p.sk_iters < resident ? static_cast<int>(p.sk_iters) : resident;
+            q.sk_ctas = clusters;
+        }
         cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, q);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    const int grid = tiles < num_sms() ? tiles : num_sms();
+    int grid = tiles < num_sms() ? tiles : num_sms();
+    if (p.sk) {
+        grid = p.sk_iters < num_sms() ? static_cast<int>(p.sk_iters) : num_sms();
+        q.sk_ctas = grid;
+    }
+    // Resident weights with several column tiles: each CTA must see one column
+    // tile only, so the grid is a whole multiple of their count.
+    if (p.bres && p.n_tiles > 1) {
+        if (kPlane || p.splits != 1) return cudaErrorInvalidValue;
+        grid = grid >= p.n_tiles ? grid / p.n_tiles * p.n_tiles : p.n_tiles;
+    }
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, p);
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, ty, q);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

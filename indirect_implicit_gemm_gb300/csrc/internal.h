@@ -58,6 +58,10 @@ struct IgemmParams {
     int m_tiles, n_tiles;
     int m_step;              // tile origin step: 128 GEMM rows, or win_rows output rows
     int splits;              // K partitions per output tile (1: no split)
+    int sk;                  // 1: stream-K (each CTA a contiguous share of all K blocks;
+                             //    partial sums added into `partial`), splits == 1
+    int sk_ctas;             // stream-K: CTAs (pairs: clusters) sharing the work
+    long long sk_iters;      // stream-K: units * num_kb
     FastDiv split_div;       // divides by splits
     FastDiv ntile_div;       // divides by n_tiles
     int stages;              // shared-memory ring depth (2..8)

@@ -137,10 +137,21 @@ def test_split_k_only_for_underfilled_layers(lib):
     # full-spatial 7x7 -> 4096 at N=128: 16 output tiles, K split, fp32 sums [128][4096]
     assert lib.workspace_size(128, 512, 7, 7, 4096, 7, 7, 1, 0, 1) == 128 * 4096 * 4
     # the same 512-channel 7x7 layer on the gather path: 98 tiles, split;
-    # ibuf (49*9*4 -> 1792 B) + sums.  The window path tiles it 256 ways: no split.
+    # ibuf (49*9*4 -> 1792 B) + sums.  The window path runs it as 64 CTA-pair
+    # units, less than a wave of pairs, with no workspace; asked for stream-K,
+    # its sums need the same [6272][512] fp32 buffer (12.8 MB, under half of the
+    # 57.8 MB im2col)
     assert lib.workspace_size(128, 512, 7, 7, 512, 3, 3, 1, 1, 1, path=lib.PATH_GATHER) == \
         1792 + 6272 * 512 * 4
     assert lib.workspace_size(128, 512, 7, 7, 512, 3, 3, 1, 1, 1) == 0
+    assert lib.plan_info(128, 512, 7, 7, 512, 3, 3, 1, 1, 1)["stream_k"] == 0
+    lib.set_tuning(0, 0, 1)
+    try:
+        assert lib.workspace_size(128, 512, 7, 7, 512, 3, 3, 1, 1, 1) == 6272 * 512 * 4
+        p = lib.plan_info(128, 512, 7, 7, 512, 3, 3, 1, 1, 1)
+        assert p["stream_k"] == 1 and p["cta_pair"] == 1 and p["splits"] == 1
+    finally:
+        lib.set_tuning(0, 0, 0)
     # plenty of tiles: no split; the gather path needs only its indirection buffer
     assert lib.workspace_size(32, 64, 56, 56, 128, 3, 3, 1, 1, 1, path=lib.PATH_GATHER) == \
         56 * 56 * 9 * 4

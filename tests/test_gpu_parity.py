@@ -233,6 +233,9 @@ MULTI_TILE = [
        pad=0, seed=75), 0, 11),
     (S("multi_dense_1x1", N=456, C_in=64, H=16, W=16, C_out=64, KH=1, KW=1, pad=0, seed=76),
      0, 0),
+    # two column tiles, each CTA keeping its own column tile's weights resident
+    (S("multi_strided_1x1_s2_cout512", N=228, C_in=64, H=32, W=32, C_out=512, KH=1, KW=1,
+       stride=2, pad=0, seed=82), 0, 11),
     (S("multi_narrowwin_c3", N=114, C_in=3, H=32, W=32, C_out=32, seed=77), 3, 5),
     (S("multi_narrow_c3_d2", N=114, C_in=3, H=32, W=32, C_out=32, pad=2, dilation=2, seed=78),
      3, 2),
@@ -275,7 +278,7 @@ TUNINGS = [(32, 0), (64, 0), (128, 2), (256, 0), (0, 2), (0, 3)]
 @pytest.fixture
 def tuning(gpu_lib):
     yield gpu_lib.set_tuning
-    gpu_lib.set_tuning(0, 0)
+    gpu_lib.set_tuning(0, 0, 0)
 
 
 @pytest.mark.parametrize("shape", TUNED_SHAPES, ids=lambda s: s.name)
@@ -293,6 +296,26 @@ def test_tuned_plans_match_oracle(gpu_lib, tuning, shape, bn, stages):
         assert plan["stages"] >= floor
     got, ref, mag = run_full(gpu_lib, shape)
     check(got, ref, mag, "%s bn=%d stages<=%d" % (shape.name, bn, stages))
+
+
+# Stream-K: units that fill less than a wave of CTA pairs share out all (unit,
+# K block) steps equally; units cut between CTAs meet in fp32 partial sums.
+STREAMK_SHAPES = [
+    S("streamk_window_pair_c256_cout512_7x7", N=128, C_in=256, H=7, W=7, C_out=512, seed=85),
+    S("streamk_window_pair_c128_cout160", N=64, C_in=128, H=10, W=10, C_out=160, seed=86),
+]
+
+
+@pytest.mark.parametrize("shape", STREAMK_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_stream_k_matches_oracle(gpu_lib, tuning, shape, out_dtype):
+    tuning(0, 0, 1)
+    plan = gpu_lib.plan_info(shape.N, shape.C_in, shape.H, shape.W, shape.C_out, shape.KH,
+                             shape.KW, shape.stride, shape.pad, shape.dilation,
+                             out_dtype=out_dtype)
+    assert plan["stream_k"] == 1, plan
+    got, ref, mag = run_full(gpu_lib, shape, out_dtype=out_dtype)
+    check(got, ref, mag, shape.name)
 
 
 def test_tiny_config_full_output(gpu_lib):
