@@ -466,9 +466,7 @@ void cap_stages(GemmPlan& g)
 void plan_stream_k(GemmPlan& g, const ConvShape& c)
 {
     if (g_tune_stream_k.load(std::memory_order_relaxed) != 1) return;
-    const bool mode = g.amode == kAWindow || g.amode == kAWindowPair || g.amode == kADense ||
-                      g.amode == kAGather || g.amode == kATmaGather ||
-                      g.amode == kATmaGatherPair;
+    const bool mode = g.amode == kAWindow || g.amode == kAWindowPair;  // built there only
     if (!mode || g.splits != 1 || (g.bres && g.n_tiles > 1) || g.stages < 2) return;
     constexpr int kNominalSms = 148;
     const long long units = (long long)(g.pair ? (g.m_tiles + 1) / 2 : g.m_tiles) * g.n_tiles;

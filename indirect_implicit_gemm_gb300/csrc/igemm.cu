@@ -249,11 +249,13 @@ struct SkRange {
 // cycles there).
 // Pair mode: unit `tile` is a pair of consecutive output tiles, the CTA of
 // rank r taking tile 2*m + r.
-template <int BN, bool PAIRED = false>
+// SK: the kernel is built with stream-K (window modes only: every other mode's
+// loops stay as short as before, which matters to the instruction caches).
+template <int BN, bool PAIRED, bool SK>
 __device__ __forceinline__ Unit unit_of(const IgemmParams& p, int tile, uint32_t rank,
                                         const SkRange& sk)
 {
-    if (p.sk) {
+    if (SK && p.sk) {
         // stream-K: the CTA's tile-th segment, unit u0 + tile, cut to [g0, g1)
         const int uu = sk.u0 + tile;
         uint32_t mt = static_cast<uint32_t>(uu), nt = 0;
@@ -482,16 +484,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // walked as segments 0, 1, ... of the units it touches; partial sums meet
     // in the fp32 buffer.
     const int cta_idx = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    constexpr bool SKM = WINDOW;  // stream-K is built into the window kernels only
     SkRange skr;
-    if (p.sk) {
+    if (SKM && p.sk) {
         const long long G = p.sk_ctas, W = p.sk_iters;
         skr.g0 = cta_idx * W / G;
         skr.g1 = (cta_idx + 1) * W / G;
         skr.u0 = static_cast<int>(skr.g0 / p.num_kb);
         skr.u1 = skr.g1 > skr.g0 ? static_cast<int>((skr.g1 - 1) / p.num_kb) : skr.u0 - 1;
     }
-    const int t_first = p.sk ? 0 : cta_idx;
-    const int t_step = p.sk ? 1 : PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const bool sk_on = SKM && p.sk;
+    const int t_first = sk_on ? 0 : cta_idx;
+    const int t_step = sk_on ? 1 : PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; ++s) {
@@ -557,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) ptx::grid_launch_dependents();
 
     const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
-    const int total_tiles = p.sk ? skr.u1 - skr.u0 + 1 : p.m_tiles * p.n_tiles * p.splits;
+    const int total_tiles = sk_on ? skr.u1 - skr.u0 + 1 : p.m_tiles * p.n_tiles * p.splits;
 
     if (warp < kEpiWarps || (EPI8 && warp < kEpiWarps + kGatherWarps)) {
         // ------------------------------------------------------------ epilogue
@@ -604,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int bias_n0 = -1;
         Ring ar;  // accumulator index and the parity of its current use
         for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt, ar.next(NACC)) {
-            const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+            const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
             const uint32_t acc = ar.stage;
             // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds,
             // and with the TMA store all four warps do (they share named barriers).
@@ -854,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t issued = 0;
                 bool ok = true;
                 for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                    const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                    const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
                         if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleGather)) {
                             ok = false;
@@ -898,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      ++spin)
                     __nanosleep(256);
                 if (*aborted) break;
-                const Unit v = unit_of<BN, PAIR>(p, tile, rank, skr);
+                const Unit v = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 if (v.n0 != 0 || v.kb0 != 0) continue;  // one prefetch per row block
                 for (int j = 0; j < p.pl_srows; ++j) {
                     uint32_t n, hp;
@@ -924,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring ring;
             bool ok = true;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 int ib4[4];  // first indirection entry of the row's pixel, or -1
                 int nb4[4];  // first row of the pixel's image
 #pragma unroll
@@ -993,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t slot = 0, slot_phase = 0;
             bool ok = wait_bar(wpack, 0u, wc, kRoleGather);
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 const int rows = min(p.win_rows, p.win_groups - u.m0);
                 const bool live = j < rows;
                 uint32_t hvalid = 0u;
@@ -1040,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t slot = 0, slot_phase = 0;
             bool ok = true;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 const int rows = min(p.win_rows, p.win_groups - u.m0);
                 const bool row_live = j < rows;
                 int ho = 0;
@@ -1110,7 +1114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring ring;
             bool ok = true;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 int ib[kRowsPerGatherThread];        // pixel's first ibuf entry, or -1
                 long long xb[kRowsPerGatherThread];  // image base (elements)
 #pragma unroll
@@ -1241,7 +1245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles;
                  tile += t_step, ++lt, ar.next(NACC)) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 const uint32_t acc = ar.stage;
                 if (!wait_bar(&tempty[acc], ar.phase ^ 1u, wc, kRoleMma)) break;
                 ptx::tc_fence_after();
@@ -1347,7 +1351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = receive();  // resident weights (or nothing to wait for)
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 const uint32_t acc = ar.stage;
                 if (!receive()) break;  // accumulator drained by the epilogue
                 ptx::tc_fence_after();
@@ -1468,7 +1472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = send(!p.bres || waited(STEMWIN ? wpack : bres_full, 0u, false));
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
-                const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 if (!send(waited(&tempty[ar.stage], ar.phase ^ 1u, PAIR))) break;
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
                     bool good = !GATHER || waited(&full_a[ring.stage], ring.phase, false);
@@ -1518,7 +1522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t row_bytes = static_cast<uint32_t>(p.nw_W * p.nw_cin * 2);
                 uint32_t slot = 0, slot_phase = 0, issued = 0;
                 for (int tile = t_first; tile < total_tiles; tile += t_step, ++issued) {
-                    const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                    const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                     if (!wait_bar(&stg_empty[slot], slot_phase ^ 1u, wc, kRoleTma)) break;
                     const int rows = min(p.win_rows, p.win_groups - u.m0);
                     uint32_t copies = 0;
@@ -1561,7 +1565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t issued = 0;
                     bool ok = true;
                     for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                        const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                        const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                         for (int kb = u.kb0; ok && kb < u.kb1; ++kb)
                             for (int t = 0; t < taps; ++t, ++issued, rb.next(SB)) {
                                 if (!wait_bar(&empty_b[rb.stage], rb.phase ^ 1u, wc, kRoleTma)) {
@@ -1592,11 +1596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // that barrier, so CTA 0's drain below covers the peer's copies too
                 // (neither CTA exits before the final cluster barrier).
                 for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                    const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                    const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                     const int rows = max(0, min(p.win_rows, p.win_groups - u.m0));
                     int rows_peer = 0;
                     if (PAIR) {
-                        const Unit v = unit_of<BN, PAIR>(p, tile, 1u, skr);
+                        const Unit v = unit_of<BN, PAIR, SKM>(p, tile, 1u, skr);
                         rows_peer = max(0, min(p.win_rows, p.win_groups - v.m0));
                     }
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
@@ -1655,7 +1659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t issued = 0;
                 bool ok = true;
                 for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
-                    const Unit u = unit_of<BN, PAIR>(p, tile, rank, skr);
+                    const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
                         if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleTma)) {
                             ok = false;
@@ -1831,9 +1835,10 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
     IgemmParams q = p;  // this launch's copy: stream-K records its grid in it
     if (p.sk) {
         // stream-K shares out every (unit, K block) iteration: as many CTAs (pairs)
-        // as fit, each with at least one iteration; no split, no column-resident
-        // weights (a CTA's iterations cross column tiles), no plane mode
-        if (kPlane || p.splits != 1 || (p.bres && p.n_tiles > 1) || p.sk_iters < 1 ||
+        // as fit, each with at least one iteration; window kernels only, no split,
+        // no column-resident weights (a CTA's iterations cross column tiles)
+        constexpr bool kWin = AMODE == kAWindow || AMODE == kAWindowPair;
+        if (!kWin || p.splits != 1 || (p.bres && p.n_tiles > 1) || p.sk_iters < 1 ||
             p.sk_iters != static_cast<long long>(p.m_tiles) * p.n_tiles * p.num_kb)
             return cudaErrorInvalidValue;
     }
