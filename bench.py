@@ -100,7 +100,7 @@ def shape_numbers(g, c: workloads.ConvShape):
                 im2win_bytes=g.im2win_bytes(c.N, c.C_in, c.H, c.W, c.KH, c.KW, c.stride, c.pad,
                                             c.dilation),
                 path={1: "gather", 2: "dense", 3: "stem", 4: "window", 5: "plane", 6: "im2win",
-                      7: "stemwin"}.get(
+                      7: "stemwin", 8: "winfold"}.get(
                     g.select_path(c.N, c.C_in, c.H, c.W, c.C_out, c.KH, c.KW, c.stride, c.pad,
                                   c.dilation), "?"))
 
@@ -529,6 +529,8 @@ def ablation_rows():
                      st, 0, 0))
     for st in (2, 4, 0):
         rows.append(("sweep_3x3_32c_150", "stages<=%d" % st if st else "default", 0, st, 0, 0))
+    # taps folded into the MMA's columns (default) against the gather path's N=32 MMAs
+    rows.append(("sweep_3x3_32c_150", "gather path", 0, 0, 1, 0))
     for bn in (64, 128, 256):
         rows.append(("sweep_3x3_256c_28", "bn=%d" % bn, bn, 0, 0, 0))
         rows.append(("strided_3x3_s2_128to256_56", "bn=%d" % bn, bn, 0, 0, 0))

@@ -95,7 +95,7 @@ typedef enum convgb_path {
                                  one contiguous run of KW columns, loaded by TMA.  Workspace:
                                  the re-laid-out input (less than half of im2col, else the
                                  path does not apply) and the re-packed weights. */
-    CONVGB_PATH_STEMWIN = 7   /* C_in = 3, stride 1, 2 or 4, undilated, W_out + ceil(KW/s) - 1
+    CONVGB_PATH_STEMWIN = 7,  /* C_in = 3, stride 1, 2 or 4, undilated, W_out + ceil(KW/s) - 1
                                  <= 128, at most 16 MMA steps of 16 per stage (KW*KC <= 256,
                                  KC = 64/s), C_in*W*2 and C_out*KH*KW*C_in*2 multiples of 16,
                                  C_out <= 256: the window order of "Im2win" (Abstract) built
@@ -104,6 +104,17 @@ typedef enum convgb_path {
                                  tensor core reads every K block of the window from the same
                                  rows at shifted starts.  No workspace: nothing goes through
                                  HBM but x, w and y. */
+    CONVGB_PATH_WINFOLD = 8   /* C_in = 32, stride 1, C_out a multiple of 32, KW <= 5,
+                                 KH <= 7, KW*C_out <= 256, (KW-1)*d <= 24: the window order
+                                 of "Im2win" (Abstract) with the KW taps folded into the
+                                 tensor core's columns.  Segments of 32 consecutive input
+                                 columns of an output row's KH input rows are staged by TMA
+                                 (zero-filled outside the image); one MMA chain over K =
+                                 KH*32 gives, per input column, each tap's partial sums
+                                 for all C_out (KW*C_out columns), and the epilogue adds
+                                 tap kw's share from the column kw*d to the right.  A
+                                 segment yields 32 - (KW-1)*d output pixels.  No
+                                 workspace. */
 } convgb_path;
 
 /* Short English text for a status code; never NULL. */
@@ -168,6 +179,11 @@ typedef struct convgb_plan {
     int epilogue_c32;     /* 1: 32-column staging chunks instead of 64 */
     int stream_k;         /* 1: each CTA (pair) takes an equal share of all (tile, K block)
                              steps; tiles split between CTAs meet in fp32 partial sums */
+    int segment_outputs;  /* CONVGB_PATH_WINFOLD: output pixels per segment, G (0 on other
+                             paths).  Each output row is cut into ceil(W_out / G)
+                             segments of G pixels (the last one shorter); segments are
+                             numbered row by row ((n, ho) order) and tile t holds
+                             segments 4t .. 4t+3, so tile_rows is 0 */
 } convgb_plan;
 
 /* Fills *plan with what conv2d_fwd_path(path, ...) would launch for this shape

@@ -20,7 +20,8 @@ __all__ = [
     "output_dims", "select_path", "workspace_size", "im2col_bytes", "im2win_bytes",
     "indirection_buffer_bytes", "check_device_errors", "set_wait_timeout_ns",
     "selftest_wait_timeout", "ConvgbError", "PATH_AUTO", "PATH_GATHER", "PATH_DENSE",
-    "PATH_STEM", "PATH_WINDOW", "PATH_PLANE", "PATH_IM2WIN", "PATH_STEMWIN", "EXPORTED_SYMBOLS",
+    "PATH_STEM", "PATH_WINDOW", "PATH_PLANE", "PATH_IM2WIN", "PATH_STEMWIN", "PATH_WINFOLD",
+    "EXPORTED_SYMBOLS",
     "library_path",
     "conv2d_fwd_host", "conv2d_fwd_host_scratch_size", "plan_info", "set_tuning", "Plan",
 ]
@@ -28,6 +29,7 @@ __all__ = [
 PATH_AUTO, PATH_GATHER, PATH_DENSE, PATH_STEM, PATH_WINDOW, PATH_PLANE, PATH_IM2WIN = (
     0, 1, 2, 3, 4, 5, 6)
 PATH_STEMWIN = 7
+PATH_WINFOLD = 8
 _BF16, _F32 = 0, 1
 OK, ERR_INTERNAL = 0, 6
 
@@ -53,7 +55,7 @@ class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "path", "a_mode", "bn", "m_tiles", "tile_rows", "n_tiles", "splits", "k_blocks", "stages",
         "weights_resident", "cta_pair", "tma_store", "epilogue_tiles", "epilogue_c32",
-        "stream_k")]
+        "stream_k", "segment_outputs")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

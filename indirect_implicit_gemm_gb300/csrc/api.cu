@@ -204,8 +204,37 @@ StemWinGeom stemwin_geom(const ConvShape& c)
     return g;
 }
 
+// Folded-window geometry (C_in = 32, stride 1).  A segment is 32 consecutive
+// input columns of one output row's KH input rows; with the KW taps folded into
+// the MMA's columns it yields G = 32 - (KW-1)*d output pixels (the rest of its
+// rows only feed its neighbours' sums).  spr segments cover an output row, four
+// make a tile.  The MMA is KW*C_out columns wide and the weights of all KH
+// blocks stay resident.
+struct FoldGeom {
+    bool ok = false;
+    int G = 0, spr = 0, n_mma = 0, b_bytes = 0;
+    long long segs = 0;
+};
+FoldGeom fold_geom(const ConvShape& c)
+{
+    FoldGeom f;
+    if (c.s != 1 || c.C_in != 32 || c.C_out % 32 != 0) return f;
+    if (c.KW > kFoldMaxKW || c.KH > kFoldMaxKH) return f;
+    f.G = 32 - (c.KW - 1) * c.d;
+    if (f.G < 8) return f;
+    f.n_mma = c.KW * c.C_out;
+    if (f.n_mma > 256 || f.n_mma % 16 != 0) return f;
+    f.spr = (c.W_out + f.G - 1) / f.G;
+    f.segs = (long long)c.N * c.H_out * f.spr;
+    if (f.segs >= (1LL << 31) - 4) return f;
+    f.b_bytes = (c.KH * f.n_mma * 64 + 1023) / 1024 * 1024;
+    f.ok = true;
+    return f;
+}
+
 struct GemmPlan;
 GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32 = 0);
+bool fold_applies(const ConvShape& c);
 bool stemwin_applies(const ConvShape& c);
 bool window_applies(const ConvShape& c);
 bool plane_applies(const ConvShape& c);
@@ -222,6 +251,7 @@ bool path_supports(int path, const ConvShape& c)
         return c.C_in % 8 == 0 && (is_pointwise(c) || is_full_spatial(c) || strided_rows(c) > 0);
     case CONVGB_PATH_STEM: return c.C_in % 8 != 0;
     case CONVGB_PATH_STEMWIN: return stemwin_applies(c);
+    case CONVGB_PATH_WINFOLD: return fold_applies(c);
     default: return false;
     }
 }
@@ -234,6 +264,13 @@ int select_path(const ConvShape& c)
                : im2win_applies(c) ? CONVGB_PATH_IM2WIN
                                    : CONVGB_PATH_STEM;
     if (path_supports(CONVGB_PATH_WINDOW, c)) return CONVGB_PATH_WINDOW;
+    // The folded window when its segments are mostly output pixels: with fewer
+    // than 12 real pixels per 32-row segment the gather path's full 128-row
+    // tiles of narrow MMAs cost less.
+    if (fold_applies(c)) {
+        const FoldGeom f = fold_geom(c);
+        if (c.W_out >= 12 * f.spr) return CONVGB_PATH_WINFOLD;
+    }
     return CONVGB_PATH_GATHER;
 }
 
@@ -334,6 +371,39 @@ bool encode_strided(CUtensorMap* m, const void* x, const ConvShape& c, int R)
     return r == CUDA_SUCCESS;
 }
 
+// Folded window: x [N][H][W][32] as a 4-D tensor, box = 32 channels x 32
+// pixels of one row (one segment's kh block), 64-byte swizzle.
+bool encode_fold_x(CUtensorMap* m, const void* x, const ConvShape& c)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {32u, (cuuint64_t)c.W, (cuuint64_t)c.H, (cuuint64_t)c.N};
+    cuuint64_t strides[3] = {64u, (cuuint64_t)c.W * 64, (cuuint64_t)c.H * c.W * 64};
+    cuuint32_t box[4] = {32u, 32u, 1u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Folded window: w [C_out][KH][KW][32] as a 4-D tensor (32 channels, kw, kh,
+// co), box = 32 channels x all C_out for one (kh, kw): the C_out rows of tap
+// kw in weight block kh, 64-byte swizzle.
+bool encode_fold_w(CUtensorMap* m, const void* w, const ConvShape& c)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {32u, (cuuint64_t)c.KW, (cuuint64_t)c.KH, (cuuint64_t)c.C_out};
+    cuuint64_t strides[3] = {64u, (cuuint64_t)c.KW * 64, (cuuint64_t)c.KH * c.KW * 64};
+    cuuint32_t box[4] = {32u, 1u, 1u, (cuuint32_t)c.C_out};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int pick_bn(int C_out)
 {
     const int forced = g_tune_bn.load(std::memory_order_relaxed);
@@ -397,6 +467,7 @@ int choose_splits(long long tiles, int num_kb, long long partial_bytes, long lon
 // aligned, no split) and the ring still has two stages with its staging tile.
 void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
 {
+    if (g.amode == kAWinFold) return;  // stores straight from the shuffle sums
     if (y_f32 || c.C_out % 8 != 0 || g.splits != 1 || g.sk || g.bn < 64 || g.stages < 2) return;
     const int kb_res = g.bres ? (int)((g.K + 63) / 64) : g.num_kb;
     const int bnb = g.pair ? g.bn / 2 : g.bn;
@@ -599,6 +670,11 @@ GemmPlan plan_plane(const ConvShape& c, int y_f32)
 
 bool plane_applies(const ConvShape& c) { return plan_plane(c, 0).stages >= 2; }
 
+bool fold_applies(const ConvShape& c)
+{
+    return fold_geom(c).ok && plan_gemm_ring(CONVGB_PATH_WINFOLD, c).stages >= 2;
+}
+
 bool stemwin_applies(const ConvShape& c)
 {
     if (!stemwin_geom(c).ok) return false;
@@ -677,6 +753,25 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
             igemm_pick_stages(g.bn, 1, g.num_kb, g.a_stage_bytes, 1, kEpiStageBytes) >= 4)
             g.bres = 1;
         g.stages = igemm_pick_stages(g.bn, g.bres, g.num_kb, g.a_stage_bytes, 1);
+        return g;
+    }
+    if (path == CONVGB_PATH_WINFOLD) {
+        // One A stage per tile: KH blocks of four 32-row segments.  Accumulator
+        // slots of 128 columns (256 when the MMA is wider).
+        const FoldGeom f = fold_geom(c);
+        g.amode = kAWinFold;
+        if (!f.ok) return g;  // stages == 0: not applicable
+        g.M = c.M;
+        g.K = (long long)c.KH * 32;
+        g.num_kb = 1;
+        g.m_step = 1;
+        g.m_tiles = (int)((f.segs + 3) / 4);
+        g.bn = f.n_mma <= 128 ? 128 : 256;
+        g.n_tiles = 1;
+        g.bres = 1;
+        g.a_stage_bytes = c.KH * kFoldKhBytes;
+        for (int st = 8; st >= 2 && !g.stages; --st)
+            if (fold_smem_bytes(f.b_bytes, st, g.a_stage_bytes) <= smem_limit()) g.stages = st;
         return g;
     }
     if (path == CONVGB_PATH_STEMWIN) {
@@ -896,9 +991,13 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     if (g.K % 8 != 0) return CONVGB_ERR_UNSUPPORTED;  // TMA row pitch must be 16-byte aligned
     memset(out, 0, sizeof *out);
     out->plan = g;
-    // (the staged-window stem packs its weights in the kernel: no weight map)
-    if (!is_stemwin(g.amode) &&
+    // (the staged-window stem packs its weights in the kernel: no weight map;
+    // the folded window reads them through its own 4-D map)
+    if (!is_stemwin(g.amode) && g.amode != kAWinFold &&
         !encode_kmajor(&out->tb, a.w, a.C_out, g.K, g.pair ? g.bn / 2 : g.bn))
+        return CONVGB_ERR_CUDA;
+    if (g.amode == kAWinFold &&
+        (!encode_fold_x(&out->ta, a.x, *a.shape) || !encode_fold_w(&out->tb, a.w, *a.shape)))
         return CONVGB_ERR_CUDA;
     if (g.amode == kADense && !encode_kmajor(&out->ta, a.a_dense, g.M, g.K, 128))
         return CONVGB_ERR_CUDA;
@@ -1026,6 +1125,21 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.ho_div = FastDiv((uint32_t)c.H_out);
         p.st_s = c.s;
     }
+    if (g.amode == kAWinFold) {
+        const ConvShape& c = *a.shape;
+        const FoldGeom f = fold_geom(c);
+        p.win_wout = c.W_out;
+        p.win_kw = c.KW;
+        p.win_d = c.d;
+        p.win_pad = c.p;
+        p.x_KH = c.KH;
+        p.ho_div = FastDiv((uint32_t)c.H_out);
+        p.fold_g = f.G;
+        p.fold_segs = (int)f.segs;
+        p.fold_n = f.n_mma;
+        p.fold_bbytes = f.b_bytes;
+        p.fold_spr_div = FastDiv((uint32_t)f.spr);
+    }
     if (window) {
         const ConvShape& c = *a.shape;
         p.win_wv = g.win_wv;
@@ -1064,6 +1178,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     if (g.stages < 2) return CONVGB_ERR_UNSUPPORTED;
     p.partial = a.partial;
     p.y_f32 = a.y_f32;
+    p.y_al32 = (reinterpret_cast<uintptr_t>(a.y) & 31u) == 0 ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     p.err = err;
     if ((g.splits > 1 || g.sk) && a.partial == nullptr) return CONVGB_ERR_WORKSPACE;
@@ -1099,7 +1214,7 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
     if (path == CONVGB_PATH_AUTO) path = select_path(c);
     if (path != CONVGB_PATH_GATHER && path != CONVGB_PATH_DENSE && path != CONVGB_PATH_STEM &&
         path != CONVGB_PATH_WINDOW && path != CONVGB_PATH_PLANE && path != CONVGB_PATH_IM2WIN &&
-        path != CONVGB_PATH_STEMWIN)
+        path != CONVGB_PATH_STEMWIN && path != CONVGB_PATH_WINFOLD)
         return CONVGB_ERR_INVALID_ARG;
     if (!path_supports(path, c)) return CONVGB_ERR_UNSUPPORTED;
     WsLayout L = workspace_layout(path, c);
@@ -1127,7 +1242,7 @@ convgb_status conv_impl(int path, const void* x, const void* w, const void* bias
         a.a_dense = x;
         a.shape = &c;
     } else if (path == CONVGB_PATH_WINDOW || path == CONVGB_PATH_PLANE ||
-               path == CONVGB_PATH_STEMWIN) {
+               path == CONVGB_PATH_STEMWIN || path == CONVGB_PATH_WINFOLD) {
         a.x = static_cast<const uint16_t*>(x);
         a.C_in = C_in;
         a.shape = &c;
@@ -1460,7 +1575,7 @@ convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_ou
     out->a_mode = g.amode;
     out->bn = g.bn;
     out->m_tiles = g.m_tiles;
-    out->tile_rows = plane ? 0 : rowtiles ? g.m_step * c.W_out : 128;
+    out->tile_rows = (plane || g.amode == kAWinFold) ? 0 : rowtiles ? g.m_step * c.W_out : 128;
     out->n_tiles = g.n_tiles;
     out->splits = g.splits;
     out->k_blocks = g.num_kb;
@@ -1471,6 +1586,7 @@ convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_ou
     out->epilogue_tiles = g.tma_store ? g.epi_bufs : 0;
     out->epilogue_c32 = g.epi_c32;
     out->stream_k = g.sk;
+    out->segment_outputs = g.amode == kAWinFold ? fold_geom(c).G : 0;
     return CONVGB_OK;
 }
 
@@ -1481,6 +1597,6 @@ void convgb_set_tuning(int bn, int max_stages, int stream_k)
     g_tune_stream_k.store(stream_k == 1 ? 1 : 0);
 }
 
-int convgb_version(void) { return 101; }
+int convgb_version(void) { return 102; }
 
 }  // extern "C"

@@ -181,7 +181,8 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, int m, int co0
     const long long row = static_cast<long long>(m) * p.C_out + co0;
     if (p.y_f32) {
         float* out = static_cast<float*>(p.y) + row;
-        if (ncols == 32 && (p.C_out & 7) == 0) {
+        // 256-bit stores need 32-byte addresses: y itself on a 32-byte boundary
+        if (ncols == 32 && (p.C_out & 7) == 0 && p.y_al32) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 ptx::st_global_v8(out + 8 * q, __float_as_uint(v[8 * q]),
@@ -201,7 +202,7 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, int m, int co0
         }
     } else {
         uint16_t* out = static_cast<uint16_t*>(p.y) + row;
-        if (ncols == 32 && (p.C_out & 15) == 0) {
+        if (ncols == 32 && (p.C_out & 15) == 0 && p.y_al32) {
             // whole 32-byte sectors: two 256-bit stores
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -423,11 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool PLANE = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     constexpr bool IM2WIN = AMODE == kAIm2win;
     constexpr bool STRIDED = AMODE == kAStrided;
+    constexpr bool FOLD = AMODE == kAWinFold;
     constexpr bool ROWTILES = WINDOW || STAGEDROWS || IM2WIN || STRIDED;  // whole output rows
     // Modes whose gather warps have nothing to gather run the epilogue on eight
     // warps: each thread converts 32 of a 64-column chunk's columns instead of
     // all 64 (the epilogue is latency-bound with one warp per scheduler).
-    constexpr bool EPI8 = WINDOW || AMODE == kADense || IM2WIN || STRIDED;
+    constexpr bool EPI8 = WINDOW || AMODE == kADense || IM2WIN || STRIDED || FOLD;
     constexpr int kEpiN = EPI8 ? 2 * kEpiThreads : kEpiThreads;
     const uint32_t S = static_cast<uint32_t>(p.stages);
     const uint32_t AST = static_cast<uint32_t>(p.a_stage_bytes);
@@ -459,7 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t NACC = PLANE ? static_cast<uint32_t>(p.pl_nacc) : static_cast<uint32_t>(C::kAcc);
     const uint32_t ACCW = PLANE ? static_cast<uint32_t>(p.pl_u * BN) : static_cast<uint32_t>(BN);
     constexpr uint32_t kTmemAlloc = PLANE ? 512u : static_cast<uint32_t>(C::kTmemCols);
-    uint8_t* sA = data + b_blocks * BB;
+    // (the folded window's resident weights: KH blocks of KW*C_out 64-byte rows)
+    uint8_t* sA = data + (FOLD ? static_cast<uint32_t>(p.fold_bbytes) : b_blocks * BB);
     uint8_t* sStg = sA + S * AST;  // narrow window: nw_slots slots of staged input rows
     const uint32_t NS = STAGEDROWS ? static_cast<uint32_t>(p.nw_slots) : 1u;
     // TMA-store epilogue: a 128 x 64 bf16 staging tile (128-byte swizzle) and the
@@ -522,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_barrier_init();
     }
     if (warp == kTmaWarp && lane == 0) {
-        if (AMODE == kADense || TMAGATHER || WINDOW || PLANE || IM2WIN || STRIDED)
+        if (AMODE == kADense || TMAGATHER || WINDOW || PLANE || IM2WIN || STRIDED || FOLD)
             ptx::prefetch_tensormap(&tmap_a);
         if (!STEMWIN) ptx::prefetch_tensormap(&tmap_b);
     }
@@ -622,6 +625,79 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ready) break;
             ptx::tc_fence_after();
+            if (FOLD) {
+                // Lane quarter `quad` holds segment 4*m0 + quad: accumulator row
+                // lane is input column w0 + lane, and column block kw of it (KW*C_out
+                // columns in all) is tap kw's share of output pixel lane - kw*d.  So
+                // output pixel lane sums block kw of rows lane + kw*d: a shuffle down
+                // by kw*d.  Lanes past fold_g, and pixels past the row's end, read
+                // rows beyond the segment and are not stored.  Warp w converts the
+                // channel half w / 4.
+                const int g = u.m0 * 4 + quad;
+                uint32_t row = 0, k = 0;
+                if (g < p.fold_segs) p.fold_spr_div.divmod(static_cast<uint32_t>(g), row, k);
+                const int wo = static_cast<int>(k) * p.fold_g + lane;
+                const bool live = g < p.fold_segs && lane < p.fold_g && wo < p.win_wout;
+                const long long m = static_cast<long long>(row) * p.win_wout + wo;
+                const int cw = p.C_out >> 1;
+                const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACCW;
+#pragma unroll 1
+                for (int c16 = 0; c16 < cw; c16 += 16) {
+                    const int co0 = half * cw + c16;
+                    uint32_t v[kFoldMaxKW][16];
+#pragma unroll
+                    for (int kw = 0; kw < kFoldMaxKW; ++kw)
+                        if (kw < p.win_kw)
+                            ptx::tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(kw * p.C_out + co0),
+                                                    v[kw]);
+                    ptx::tmem_ld_wait();
+                    if (c16 + 16 >= cw) release_acc(acc);
+                    float o[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(v[0][i]);
+#pragma unroll
+                    for (int kw = 1; kw < kFoldMaxKW; ++kw)
+                        if (kw < p.win_kw) {
+                            const int sh = kw * p.win_d;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                o[i] += __shfl_down_sync(0xffffffffu, __uint_as_float(v[kw][i]), sh);
+                        }
+                    if (!live) continue;
+                    if (p.bias != nullptr) {
+                        const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + co0);
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const uint4 b = __ldg(b4 + q);
+                            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                o[8 * q + 2 * e] += bf16_bits_to_float(static_cast<uint16_t>(bw[e] & 0xFFFFu));
+                                o[8 * q + 2 * e + 1] += bf16_bits_to_float(static_cast<uint16_t>(bw[e] >> 16));
+                            }
+                        }
+                    }
+                    const long long at = m * p.C_out + co0;
+                    if (p.y_f32) {
+                        float4* out = reinterpret_cast<float4*>(static_cast<float*>(p.y) + at);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            out[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    } else {
+                        uint16_t* out = static_cast<uint16_t*>(p.y) + at;
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) pk[q] = pack_bf16x2(o[2 * q], o[2 * q + 1]);
+                        if (p.y_al32) {
+                            ptx::st_global_v8(out, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+                        } else {
+                            reinterpret_cast<uint4*>(out)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            reinterpret_cast<uint4*>(out)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                        }
+                    }
+                }
+                continue;
+            }
             if (p.tma_store && u.n0 != bias_n0) {  // new column tile: stage its bias
                 ptx::named_barrier_sync(1, kEpiN);
                 for (int i = et; i < BN; i += kEpiN)
@@ -1334,9 +1410,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // with its outcome (the same sequence: weights, then per tile the
             // accumulator and each K block).
             // (in a pair only CTA 0 issues: each MMA covers both CTAs' 128 rows)
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
-            const uint64_t a_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
-            const uint64_t b_desc0 = ptx::sdesc_k_major_sw128(ptx::smem_addr(sB));
+            // (the folded window: MMA width KW*C_out, 64-byte rows of 32 channels)
+            const uint32_t idesc = FOLD ? ptx::idesc_bf16_f32(BM, p.fold_n)
+                                        : ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
+            const uint64_t a_desc0 = FOLD ? ptx::sdesc_k_major_sw64(ptx::smem_addr(sA))
+                                          : ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
+            const uint64_t b_desc0 = FOLD ? ptx::sdesc_k_major_sw64(ptx::smem_addr(sB))
+                                          : ptx::sdesc_k_major_sw128(ptx::smem_addr(sB));
             const uint32_t a_slot_step = AST >> 4;
             constexpr uint32_t b_blk_step = BB >> 4;
             const uint32_t col_step = static_cast<uint32_t>(p.win_d * 8);  // window: kw + 1
@@ -1419,6 +1499,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     mma_issue<PAIR>(d_tmem, ad + 8 * (q >> 2) + 2 * (q & 3),
                                                     bd0 + (q >> 2) * b_blk_step + 2 * (q & 3), idesc,
                                                     q != 0 ? 1u : acc0);
+                        } else if (FOLD) {
+                            // The stage holds one 128-row block per kh (four segments of
+                            // 32 input columns x 32 channels); weight block kh is KW*C_out
+                            // rows (kw, co).  Two 16-channel steps per kh.
+                            const uint32_t b_kh_step = static_cast<uint32_t>(p.fold_n * 64) >> 4;
+#pragma unroll
+                            for (int kh = 0; kh < kFoldMaxKH; ++kh)
+                                if (kh < p.x_KH) {
+#pragma unroll
+                                    for (int kk = 0; kk < 2; ++kk)
+                                        mma_issue<PAIR>(d_tmem,
+                                                        ad + static_cast<uint32_t>(kh) * (kFoldKhBytes >> 4) + 2 * kk,
+                                                        b_desc0 + static_cast<uint32_t>(kh) * b_kh_step + 2 * kk,
+                                                        idesc, (kh != 0 || kk != 0) ? 1u : 0u);
+                                }
                         } else {
                             const uint64_t bd =
                                 b_desc0 + (p.bres ? static_cast<uint32_t>(kb) : ring.stage) * b_blk_step;
@@ -1492,6 +1587,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // raw weights into the A stages, packed there by the epilogue warps
                 ptx::mbar_arrive_expect_tx(bres_full, static_cast<uint32_t>(p.sw_wbytes));
                 ptx::bulk_copy_g2s(sA, p.w, static_cast<uint32_t>(p.sw_wbytes), bres_full);
+            } else if (FOLD) {
+                // Weight block kh = rows (kw, co) of w[co][kh][kw][0..31]: one box of
+                // C_out rows per (kh, kw) from w viewed as [C_out][KH][KW][32].
+                ptx::mbar_arrive_expect_tx(
+                    bres_full, static_cast<uint32_t>(p.x_KH * p.fold_n) * 64u);
+                for (int kh = 0; kh < p.x_KH; ++kh)
+                    for (int kw = 0; kw < p.win_kw; ++kw)
+                        ptx::tma_load_4d(sB + (kh * p.fold_n + kw * p.C_out) * 64, &tmap_b, bres_full,
+                                         0, kw, kh, 0);
             } else if (p.bres) {
                 // Weights resident: every K block of the one column tile, once (in
                 // a pair each CTA holds half of the columns; CTA 0's barrier counts
@@ -1653,6 +1757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t a_tx =
                     GATHER                ? 0u
                     : (IM2WIN || STRIDED) ? static_cast<uint32_t>(p.win_rows * p.win_wout) * 128u
+                    : FOLD                ? AST
                                           : static_cast<uint32_t>(kABytes);
                 const uint32_t kTx = (p.bres ? 0u : static_cast<uint32_t>(BB)) + a_tx;
                 Ring ring;
@@ -1668,7 +1773,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (rank == 0)
                             ptx::mbar_arrive_expect_tx(&full_b[ring.stage],
                                                        kTx * (PAIR ? 2u : 1u));
-                        if (IM2WIN) {
+                        if (FOLD) {
+                            // Segments 4*m0 .. 4*m0 + 3 (past the last one, the last
+                            // again, whose outputs the epilogue discards): per kh, 32
+                            // input columns from k*fold_g - p of input row ho - p + kh*d,
+                            // into rows 32*q .. of the stage's kh block.  TMA zero-fills
+                            // columns and rows outside the image.
+                            for (int q = 0; q < 4; ++q) {
+                                const int g = min(u.m0 * 4 + q, p.fold_segs - 1);
+                                uint32_t row, k, n, ho;
+                                p.fold_spr_div.divmod(static_cast<uint32_t>(g), row, k);
+                                p.ho_div.divmod(row, n, ho);
+                                const int w0 = static_cast<int>(k) * p.fold_g - p.win_pad;
+                                for (int kh = 0; kh < p.x_KH; ++kh)
+                                    ptx::tma_load_4d(sA + ring.stage * AST + kh * kFoldKhBytes + q * 2048,
+                                                     &tmap_a, &full_b[ring.stage], 0, w0,
+                                                     static_cast<int>(ho) - p.win_pad + kh * p.win_d,
+                                                     static_cast<int>(n));
+                            }
+                        } else if (IM2WIN) {
                             ptx::tma_load_3d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, 0, u.m0);
                         } else if (STRIDED) {
@@ -1791,12 +1914,13 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
                                    : 0);
     constexpr bool kPlane = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     constexpr bool kPairMode = AMODE == kAWindowPair || AMODE == kATmaGatherPair;
+    constexpr bool kFold = AMODE == kAWinFold;
     const int smem =
-        kPlane
-            ? plane_smem_bytes(BN, p.stages, p.a_stage_bytes, p.bres ? p.kb_total : p.b_stages,
-                               extra)
-            : igemm_smem_bytes(kPairMode ? BN / 2 : BN, p.stages, p.bres, p.kb_total,
-                               p.a_stage_bytes, p.b_per_stage, extra);
+        kPlane ? plane_smem_bytes(BN, p.stages, p.a_stage_bytes, p.bres ? p.kb_total : p.b_stages,
+                                  extra)
+        : kFold ? fold_smem_bytes(p.fold_bbytes, p.stages, p.a_stage_bytes)
+                : igemm_smem_bytes(kPairMode ? BN / 2 : BN, p.stages, p.bres, p.kb_total,
+                                   p.a_stage_bytes, p.b_per_stage, extra);
     if (p.stages < 2 || p.stages > kMaxStages || smem > kSmemLimit) return cudaErrorInvalidValue;
     // gather warps taking turns: at most one phase ahead needs kGatherWarps stages
     static_assert(kMinGatherTurnStages == kGatherWarps, "turn-taking ring depth");
@@ -1822,6 +1946,22 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
             p.kb_total != p.num_kb * p.sw_nkb || p.sw_last < 1 || p.sw_last > 4 ||
             p.sw_steps != (p.sw_nkb - 1) * 4 + p.sw_last || p.sw_steps > kStemWinMaxSteps)
             return cudaErrorInvalidValue;
+    }
+    if (kFold) {
+        // the folded window's shared-memory layout, its unrolled loops and its
+        // epilogue's register arrays: 32 channels per 64-byte row, KW*C_out MMA
+        // columns (a multiple of 16 that fits one BN-column accumulator slot),
+        // one K block per tile, weights resident, no split, direct stores
+        const bool ok = (BN == 128 || BN == 256) && p.C_in == 32 && p.C_out % 32 == 0 &&
+                        p.fold_n == p.win_kw * p.C_out && p.fold_n % 16 == 0 && p.fold_n >= 16 &&
+                        p.fold_n <= BN && p.win_kw >= 1 && p.win_kw <= kFoldMaxKW &&
+                        p.x_KH >= 1 && p.x_KH <= kFoldMaxKH && p.win_d >= 1 &&
+                        p.fold_g == 32 - (p.win_kw - 1) * p.win_d && p.fold_g >= 1 &&
+                        p.a_stage_bytes == p.x_KH * kFoldKhBytes && p.num_kb == 1 &&
+                        p.fold_bbytes >= p.x_KH * p.fold_n * 64 && p.fold_bbytes % 1024 == 0 &&
+                        p.bres == 1 && p.n_tiles == 1 && p.splits == 1 && !p.sk && !p.tma_store &&
+                        p.fold_segs >= 1 && p.m_tiles == (p.fold_segs + 3) / 4 && p.m_step == 1;
+        if (!ok) return cudaErrorInvalidValue;
     }
     if (kPlane &&
         ((!p.bres && (p.b_stages < 2 || p.b_stages > kMaxStages)) || p.pl_u < 1 || p.pl_u > 2 ||
@@ -1941,6 +2081,11 @@ int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per
 
 int window_stage_rows(int kw, int d) { return (BM + (kw - 1) * d + 7) / 8 * 8; }
 
+int fold_smem_bytes(int b_bytes, int stages, int a_stage_bytes)
+{
+    return kHeaderBytes + 1024 + b_bytes + stages * a_stage_bytes;
+}
+
 int plane_smem_bytes(int bn, int a_stages, int a_stage_bytes, int b_blocks, int extra_bytes)
 {
     return kHeaderBytes + 1024 + b_blocks * bn * BK * 2 + a_stages * a_stage_bytes + extra_bytes;
@@ -1968,6 +2113,11 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kAStemWin: return launch_mode<kAStemWin>(bn, ta, tb, ty, p, st);
     case kAStemWin1: return launch_mode<kAStemWin1>(bn, ta, tb, ty, p, st);
     case kAStemWin4: return launch_mode<kAStemWin4>(bn, ta, tb, ty, p, st);
+    // (accumulator slots of 128 or 256 columns: MMA widths up to 128 or 256)
+    case kAWinFold:
+        return bn == 128   ? launch_bn<128, kAWinFold>(ta, tb, ty, p, st)
+               : bn == 256 ? launch_bn<256, kAWinFold>(ta, tb, ty, p, st)
+                           : cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
     }
 }

@@ -98,6 +98,12 @@ struct IgemmParams {
     int pl_nacc;             // accumulators in tensor memory (each pl_u*BN columns)
     int b_stages;            // streamed weights: B ring slots of one 64-column block
     FastDiv hp_div;          // divides a virtual row index by H + 2p
+    // folded window (kAWinFold): fold_g output pixels per 32-column segment,
+    // fold_segs segments in all (fold_spr_div divides by the segments of an output
+    // row), MMA width fold_n = KW * C_out, resident weight bytes fold_bbytes
+    int fold_g, fold_segs, fold_n, fold_bbytes;
+    FastDiv fold_spr_div;
+    int y_al32;              // 1: y starts on a 32-byte boundary (256-bit stores allowed)
     int tma_store;           // 1: epilogue stages 64-column chunks in shared memory and
                              //    stores them with TMA (bf16 y, C_out % 8 == 0, no split)
     int epi_c32;             // TMA-store epilogue: 1 = 32-column chunks (8 KB staging tiles)
@@ -161,7 +167,19 @@ enum AMode : int {
                       // strides in one kernel the 7x7 stride-2 stem ran 100 us, not 65)
     kAStemWin1 = 14,
     kAStemWin4 = 15,
+    kAWinFold = 16,   // C_in = 32, stride 1: the KW taps folded into the MMA's columns.  A row
+                      // r of a tile is input column w0 + (r % 32) of one 32-column segment
+                      // (four segments per tile, one per TMEM lane quarter) with K = (kh, ci);
+                      // B row (kw, co) holds w[co][kh][kw][ci]; the epilogue sums column
+                      // block kw of row r + kw*d into output pixel r (warp shuffles), so a
+                      // segment yields 32 - (KW-1)*d output pixels
 };
+// The folded window's limits: kernel width (registers of the epilogue's shuffle
+// sum), kernel height (the unrolled MMA sequence), and bytes of one kh block of
+// an A stage (128 rows of 32 channels).
+constexpr int kFoldMaxKW = 5;
+constexpr int kFoldMaxKH = 7;
+constexpr int kFoldKhBytes = 128 * 64;
 // The staged-window stem's A mode for a stride (1, 2 or 4).
 constexpr int stemwin_amode(int s) { return s == 1 ? kAStemWin1 : s == 4 ? kAStemWin4 : kAStemWin; }
 constexpr bool is_stemwin(int amode)
@@ -180,6 +198,9 @@ int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per
                       int extra_bytes = 0);
 // Rows of an A ring slot in window mode (128 plus the tap spill, rounded to 8).
 int window_stage_rows(int kw, int d);
+// Dynamic shared memory of a folded-window CTA: resident weights of b_bytes
+// (a multiple of 1024) and `stages` A stages.
+int fold_smem_bytes(int b_bytes, int stages, int a_stage_bytes);
 // Dynamic shared memory of a plane-mode CTA: a_stages A slots, b_blocks weight
 // blocks (resident or ring), plus extra bytes.
 int plane_smem_bytes(int bn, int a_stages, int a_stage_bytes, int b_blocks, int extra_bytes);

@@ -356,6 +356,21 @@ __device__ __forceinline__ uint64_t sdesc_k_major_sw128(uint32_t saddr)
     return d;
 }
 
+// The same for a K-major operand in the 64-byte swizzle layout: rows of 64
+// bytes (32 bf16), 16-byte chunk c of row r at r*64 + ((c ^ ((r >> 1) & 3)) * 16),
+// 8-row groups 512 bytes apart; the tile starts on a 512-byte boundary, and
+// the second 16-element K step starts 32 bytes into the row.
+__device__ __forceinline__ uint64_t sdesc_k_major_sw64(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address >> 4, bits 0-13
+    d |= static_cast<uint64_t>(1u) << 16;                  // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(512u >> 4) << 32;           // stride byte offset: 8 rows
+    d |= static_cast<uint64_t>(1u) << 46;                  // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(4u) << 61;                  // 64-byte swizzle
+    return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n)
 {

@@ -115,6 +115,13 @@ def expected_path(c):
     wv = oracle.output_size(c.W, c.KW, c.stride, c.pad, c.dilation) + (c.KW - 1) * c.dilation
     if c.stride == 1 and c.C_in % 64 == 0 and wv <= 128 and (c.KW - 1) * c.dilation <= 8:
         return 4  # window
+    # taps folded into the MMA's columns: 32 input channels, segments of
+    # G = 32 - (KW-1)d output pixels, at least 12 of them per segment on average
+    G = 32 - (c.KW - 1) * c.dilation
+    Wo = oracle.output_size(c.W, c.KW, c.stride, c.pad, c.dilation)
+    if (c.stride == 1 and c.C_in == 32 and c.C_out % 32 == 0 and c.KW <= 5 and c.KH <= 7 and
+            G >= 8 and c.KW * c.C_out <= 256 and Wo >= 12 * -(-Wo // G)):
+        return 8
     return 1  # indirection-buffer gather
 
 
@@ -126,6 +133,23 @@ def test_path_selection(lib, cfg, path):
     got = lib.select_path(cfg.N, cfg.C_in, cfg.H, cfg.W, cfg.C_out, cfg.KH, cfg.KW, cfg.stride,
                           cfg.pad, cfg.dilation)
     assert got == path
+
+
+def test_winfold_selection_and_plan(lib):
+    # 32 -> 32 3x3 at 150x150: segments of 30 output pixels, five per output row
+    pl = lib.plan_info(128, 32, 150, 150, 32, 3, 3, 1, 1, 1)
+    assert (pl["path"], pl["a_mode"], pl["segment_outputs"], pl["tile_rows"]) == (8, 16, 30, 0)
+    assert pl["m_tiles"] == (128 * 150 * 5 + 3) // 4 and pl["k_blocks"] == 1
+    assert pl["weights_resident"] == 1 and pl["splits"] == 1 and pl["tma_store"] == 0
+    assert lib.workspace_size(128, 32, 150, 150, 32, 3, 3, 1, 1, 1) == 0
+    # narrow rows (8 output pixels per 32-row segment) stay on the gather path
+    assert lib.select_path(4, 32, 8, 8, 32, 3, 3, 1, 1, 1) == 1
+    # C_out not a multiple of 32, stride 2, or KW*C_out past 256: not folded
+    assert lib.select_path(4, 32, 40, 40, 48, 3, 3, 1, 1, 1) == 1
+    assert lib.select_path(4, 32, 40, 40, 32, 3, 3, 2, 1, 1) == 1
+    assert lib.select_path(4, 32, 40, 40, 128, 3, 3, 1, 1, 1) == 1
+    with pytest.raises(lib.ConvgbError):
+        lib.plan_info(4, 32, 40, 40, 128, 3, 3, 1, 1, 1, path=lib.PATH_WINFOLD)
 
 
 def test_dense_path_needs_no_workspace(lib):

@@ -39,8 +39,29 @@ def border_points(shape, Ho, Wo):
     return np.array(pts, dtype=np.int64)
 
 
+def fold_tile_points(shape, plan, Ho, Wo, rng, per_tile=PER_TILE):
+    """Folded-window plans: tile t holds segments 4t .. 4t+3, segment g being the
+    G = segment_outputs output pixels from k*G of output row g // spr (spr
+    segments per row, the last one shorter).  per_tile / 4 (at least one)
+    random outputs in every segment, so every tile gets per_tile of them."""
+    G = plan["segment_outputs"]
+    spr = -(-Wo // G)
+    segs = shape.N * Ho * spr
+    assert plan["m_tiles"] == -(-segs // 4), plan
+    per_seg = max(1, per_tile // 4)
+    g = np.repeat(np.arange(segs, dtype=np.int64), per_seg)
+    row, k = np.divmod(g, spr)
+    span = np.minimum(Wo, (k + 1) * G) - k * G
+    wo = k * G + (rng.random(len(g)) * span).astype(np.int64)
+    n, ho = np.divmod(row, Ho)
+    co = rng.integers(0, shape.C_out, len(g))
+    return np.stack([n, co, ho, wo], axis=1)
+
+
 def tile_points(shape, plan, Ho, Wo, rng, per_tile=PER_TILE):
     """per_tile random outputs inside every (row tile, column tile) of the plan."""
+    if plan.get("segment_outputs", 0):
+        return fold_tile_points(shape, plan, Ho, Wo, rng, per_tile)
     M = shape.N * Ho * Wo
     tr = plan["tile_rows"]
     assert tr > 0, "the plan's tiles are not ranges of M"
@@ -143,6 +164,13 @@ def test_full_size_plane_path_sampled(gpu_lib, shape):
     err = np.abs(got - ref)
     assert not (err > TOL_ELEM * mag).any(), shape.name
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= TOL_REL_L2
+
+
+@pytest.mark.parametrize("shape", [c for c in FULL if c.C_in == 32], ids=lambda s: s.name)
+def test_full_size_gather_path_for_32_channels_sampled(gpu_lib, shape):
+    """The gather path, which conv2d_fwd no longer picks for 32-channel layers
+    the folded window takes, at full size."""
+    check_per_tile(gpu_lib, shape, gpu_lib.PATH_GATHER)
 
 
 @pytest.mark.parametrize("shape", [c for c in FULL if c.C_in % 8 != 0], ids=lambda s: s.name)

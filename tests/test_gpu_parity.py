@@ -218,11 +218,70 @@ def test_stem_path_explicit_matches_oracle(gpu_lib, shape):
     check(got, ref, mag, shape.name)
 
 
+# Folded window (C_in = 32, stride 1): KW taps folded into the MMA's columns,
+# the epilogue's shuffle sum across rows.  Ragged segments (W_out not a multiple
+# of G), 64 output channels (192-column MMA), dilation 2 (G = 28), 5x5 and 7x5
+# kernels (160-column MMA, KH up to 7), one kernel row, one kernel column with
+# padding, and no padding.
+FOLD_SHAPES = [
+    S("winfold_3x3_c32_ragged", N=2, C_in=32, H=9, W=37, C_out=32, seed=100),
+    S("winfold_3x3_cout64", N=2, C_in=32, H=11, W=45, C_out=64, seed=101),
+    S("winfold_3x3_d2", N=2, C_in=32, H=12, W=33, C_out=32, pad=2, dilation=2, seed=102),
+    S("winfold_5x5_cout32", N=1, C_in=32, H=14, W=50, C_out=32, KH=5, KW=5, pad=2, seed=103),
+    S("winfold_1x3", N=2, C_in=32, H=5, W=64, C_out=32, KH=1, KW=3, pad=1, seed=104),
+    S("winfold_3x1_cout96", N=2, C_in=32, H=12, W=40, C_out=96, KH=3, KW=1, pad=1, seed=105),
+    S("winfold_7x5", N=1, C_in=32, H=16, W=40, C_out=32, KH=7, KW=5, pad=3, seed=106),
+    S("winfold_p0", N=3, C_in=32, H=8, W=70, C_out=32, pad=0, seed=107),
+]
+
+
+@pytest.mark.parametrize("shape", FOLD_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_winfold_path_matches_oracle(gpu_lib, shape, out_dtype):
+    plan = gpu_lib.plan_info(shape.N, shape.C_in, shape.H, shape.W, shape.C_out, shape.KH,
+                             shape.KW, shape.stride, shape.pad, shape.dilation,
+                             path=gpu_lib.PATH_WINFOLD)
+    assert plan["a_mode"] == 16 and plan["stages"] >= 2, plan
+    assert plan["segment_outputs"] == 32 - (shape.KW - 1) * shape.dilation, plan
+    got, ref, mag = run_full(gpu_lib, shape, path=gpu_lib.PATH_WINFOLD, out_dtype=out_dtype)
+    check(got, ref, mag, shape.name)
+
+
+@pytest.mark.parametrize("shape", FOLD_SHAPES[:2], ids=lambda s: s.name)
+def test_winfold_without_bias(gpu_lib, shape):
+    got, ref, mag = run_full(gpu_lib, shape, path=gpu_lib.PATH_WINFOLD, with_bias=False)
+    check(got, ref, mag, shape.name)
+
+
+def test_winfold_unaligned_output(gpu_lib):
+    # y 16 bytes past a 32-byte boundary: the epilogue must not use 256-bit stores
+    shape = FOLD_SHAPES[0]
+    x, w, b = workloads.make_inputs(shape)
+    Ho = oracle.output_size(shape.H, shape.KH, shape.stride, shape.pad, shape.dilation)
+    Wo = oracle.output_size(shape.W, shape.KW, shape.stride, shape.pad, shape.dilation)
+    n = shape.N * Ho * Wo * shape.C_out
+    buf = torch.full((n + 16,), float("nan"), dtype=torch.bfloat16, device=dev())
+    assert buf.data_ptr() % 32 == 0
+    y = buf[8:8 + n].view(shape.N, Ho, Wo, shape.C_out)
+    gpu_lib.conv2d_fwd_path(gpu_lib.PATH_WINFOLD, x.to(dev()), w.to(dev()), b.to(dev()),
+                            shape.stride, shape.pad, shape.dilation, y=y)
+    st, code = gpu_lib.check_device_errors()
+    assert st == 0, "device error word %#x" % code
+    ref, mag = oracle.conv2d_direct(workloads.bits(x), workloads.bits(w), workloads.bits(b),
+                                    shape.stride, shape.pad, shape.dilation)
+    check(y.float().cpu().numpy(), ref, mag, shape.name)
+    assert torch.isnan(buf[:8].float()).all() and torch.isnan(buf[8 + n:].float()).all()
+
+
 # One shape per A-operand mode whose grid hands every persistent CTA at least
 # six work units (accumulator slots reused, the ring wrapped many times, pair
 # tails at scale), with small K so the oracle checks every element in seconds.
 MULTI_TILE = [
-    (S("multi_gather_c32", N=130, C_in=32, H=30, W=30, C_out=32, seed=70), 0, 1),
+    (S("multi_gather_c32", N=130, C_in=32, H=30, W=30, C_out=32, seed=70), 1, 1),
+    # folded window: one segment per output row (G = 30 = W_out), then two per
+    # row with 64 output channels (192-column MMAs, two 256-column accumulators)
+    (S("multi_winfold_c32", N=130, C_in=32, H=30, W=30, C_out=32, seed=83), 0, 16),
+    (S("multi_winfold_c32_cout64", N=64, C_in=32, H=30, W=40, C_out=64, seed=84), 8, 16),
     (S("multi_tmagather_c64_s2", N=519, C_in=64, H=30, W=30, C_out=64, stride=2, seed=71), 0, 3),
     (S("multi_tmagather_pair_1x1_p1_s2", N=456, C_in=64, H=30, W=30, C_out=256, KH=1, KW=1,
        stride=2, pad=1, seed=72), 0, 12),
