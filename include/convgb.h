@@ -104,17 +104,18 @@ typedef enum convgb_path {
                                  tensor core reads every K block of the window from the same
                                  rows at shifted starts.  No workspace: nothing goes through
                                  HBM but x, w and y. */
-    CONVGB_PATH_WINFOLD = 8   /* C_in = 32, stride 1, C_out a multiple of 32, KW <= 5,
-                                 KH <= 7, KW*C_out <= 256, (KW-1)*d <= 24: the window order
-                                 of "Im2win" (Abstract) with the KW taps folded into the
-                                 tensor core's columns.  Segments of 32 consecutive input
-                                 columns of an output row's KH input rows are staged by TMA
-                                 (zero-filled outside the image); one MMA chain over K =
-                                 KH*32 gives, per input column, each tap's partial sums
-                                 for all C_out (KW*C_out columns), and the epilogue adds
-                                 tap kw's share from the column kw*d to the right.  A
-                                 segment yields 32 - (KW-1)*d output pixels.  No
-                                 workspace. */
+    CONVGB_PATH_WINFOLD = 8   /* C_in = 32, stride 1, W >= 32, C_out a multiple of 32,
+                                 KW <= 5, KH <= 7, KW*C_out <= 256, (KW-1)*d <= 24, d <= 8:
+                                 the window order of "Im2win" (Abstract) with the KW taps
+                                 folded into the tensor core's columns.  Segments of 32
+                                 consecutive input columns (inside the row) of an output
+                                 row's KH input rows are staged by one TMA box each (rows
+                                 outside the image read as zero); one MMA chain over K =
+                                 KH*32 gives, per input column, each tap's partial sums for
+                                 all C_out (KW*C_out columns), and the epilogue adds, for
+                                 each output pixel, tap kw's share from the column it reads
+                                 (taps in the padding are left out).  A segment yields
+                                 32 - (KW-1)*d output pixels.  No workspace. */
 } convgb_path;
 
 /* Short English text for a status code; never NULL. */

@@ -220,6 +220,9 @@ FoldGeom fold_geom(const ConvShape& c)
     FoldGeom f;
     if (c.s != 1 || c.C_in != 32 || c.C_out % 32 != 0) return f;
     if (c.KW > kFoldMaxKW || c.KH > kFoldMaxKH) return f;
+    // segments are 32 columns inside the row; the row box spans (KH-1)*d + 1 rows
+    // with a row step d (a TMA element stride, at most 8)
+    if (c.W < 32 || c.d > 8 || (c.KH - 1) * c.d + 1 > 256) return f;
     f.G = 32 - (c.KW - 1) * c.d;
     if (f.G < 8) return f;
     f.n_mma = c.KW * c.C_out;
@@ -371,17 +374,22 @@ bool encode_strided(CUtensorMap* m, const void* x, const ConvShape& c, int R)
     return r == CUDA_SUCCESS;
 }
 
-// Folded window: x [N][H][W][32] as a 4-D tensor, box = 32 channels x 32
-// pixels of one row (one segment's kh block), 64-byte swizzle.
+// Folded window: x [N][H][W][32] as a 5-D tensor (channel, column, row, group
+// of eight columns, image), the group dimension 512 bytes (eight pixels) apart
+// and overlapping the column dimension.  A box of 32 channels x 8 columns x the
+// KH rows (every d-th) x 4 groups is one segment: 32 consecutive columns of its
+// KH input rows, stored group by group with each group's KH rows in turn
+// (64-byte swizzle).  The segments' columns always lie inside the row, so the
+// column bounds never apply; rows outside the image read as zero.
 bool encode_fold_x(CUtensorMap* m, const void* x, const ConvShape& c)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[4] = {32u, (cuuint64_t)c.W, (cuuint64_t)c.H, (cuuint64_t)c.N};
-    cuuint64_t strides[3] = {64u, (cuuint64_t)c.W * 64, (cuuint64_t)c.H * c.W * 64};
-    cuuint32_t box[4] = {32u, 32u, 1u, 1u};
-    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
+    cuuint64_t dims[5] = {32u, (cuuint64_t)c.W, (cuuint64_t)c.H, 4u, (cuuint64_t)c.N};
+    cuuint64_t strides[4] = {64u, (cuuint64_t)c.W * 64, 512u, (cuuint64_t)c.H * c.W * 64};
+    cuuint32_t box[5] = {32u, 8u, (cuuint32_t)((c.KH - 1) * c.d + 1), 4u, 1u};
+    cuuint32_t estr[5] = {1u, 1u, (cuuint32_t)c.d, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(x), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -1133,6 +1141,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.win_d = c.d;
         p.win_pad = c.p;
         p.x_KH = c.KH;
+        p.x_W = c.W;
         p.ho_div = FastDiv((uint32_t)c.H_out);
         p.fold_g = f.G;
         p.fold_segs = (int)f.segs;

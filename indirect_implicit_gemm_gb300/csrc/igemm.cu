@@ -470,6 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sEpi = sStg + (STAGEDROWS ? NS * p.nw_slot_bytes : 0);
     const int epi_tile = p.epi_c32 ? kEpiNarrowTileBytes : kEpiTileBytes;  // staging tile bytes
     float* sBias = reinterpret_cast<float*>(sEpi + p.epi_bufs * epi_tile);
+    // folded window: the bias as fp32 right after the A stages (1 KB)
+    float* sBiasF = reinterpret_cast<float*>(sA + S * AST);
     uint32_t* sVote = reinterpret_cast<uint32_t*>(abort_flag + 1);  // up to 8 epilogue-warp votes
     volatile uint32_t* sTilesDone = sVote + 8;  // tiles the epilogue has finished (plane prefetch)
     // wait warp -> MMA warp: 1 if the awaited barrier completed, 0 to unwind; two
@@ -604,6 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::named_barrier_sync(1, kEpiN);
             if (et == 0) ptx::mbar_arrive(wpack);
         }
+        if (FOLD) {
+            // the bias as fp32, once: every tile has the same C_out columns
+            for (int i = et; i < p.C_out; i += kEpiN)
+                sBiasF[i] = p.bias != nullptr ? bf16_bits_to_float(p.bias[i]) : 0.f;
+            ptx::named_barrier_sync(1, kEpiN);
+        }
         const int wrow = (ROWTILES || PLANE) ? r / p.win_wv : 0;
         const int wcol = (ROWTILES || PLANE) ? r - wrow * p.win_wv : 0;
         uint32_t lt = 0;
@@ -626,18 +634,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ready) break;
             ptx::tc_fence_after();
             if (FOLD) {
-                // Lane quarter `quad` holds segment 4*m0 + quad: accumulator row
-                // lane is input column w0 + lane, and column block kw of it (KW*C_out
-                // columns in all) is tap kw's share of output pixel lane - kw*d.  So
-                // output pixel lane sums block kw of rows lane + kw*d: a shuffle down
-                // by kw*d.  Lanes past fold_g, and pixels past the row's end, read
-                // rows beyond the segment and are not stored.  Warp w converts the
-                // channel half w / 4.
+                // Lane quarter `quad` holds segment 4*m0 + quad: accumulator row r
+                // is input column c0 + r, and its column block kw (KW*C_out columns
+                // in all) is tap kw's share of the output pixel that reads column
+                // c0 + r through tap kw.  The segment owns output pixels k*G ..
+                // k*G + G - 1 of its row; lane l computes pixel wo = k*G + l as the
+                // sum over the taps whose column wo - p + kw*d lies in the image of
+                // block kw of row wo - p + kw*d - c0 (a shuffle; taps outside the
+                // image are the zero padding and are left out).  Warp w converts
+                // the channel half w / 4.
                 const int g = u.m0 * 4 + quad;
                 uint32_t row = 0, k = 0;
                 if (g < p.fold_segs) p.fold_spr_div.divmod(static_cast<uint32_t>(g), row, k);
                 const int wo = static_cast<int>(k) * p.fold_g + lane;
                 const bool live = g < p.fold_segs && lane < p.fold_g && wo < p.win_wout;
+                const int c0 = min(max(static_cast<int>(k) * p.fold_g - p.win_pad, 0), p.x_W - 32);
+                const int col0 = wo - p.win_pad;  // column of tap 0
+                uint32_t taps = 0;                // taps whose column lies in the image
+#pragma unroll
+                for (int kw = 0; kw < kFoldMaxKW; ++kw) {
+                    const int col = col0 + kw * p.win_d;
+                    if (kw < p.win_kw && col >= 0 && col < p.x_W) taps |= 1u << kw;
+                }
+                // a segment that starts at k*G - p lies inside the row with every
+                // tap of its pixels (warp-uniform)
+                const bool interior = c0 == static_cast<int>(k) * p.fold_g - p.win_pad;
                 const long long m = static_cast<long long>(row) * p.win_wout + wo;
                 const int cw = p.C_out >> 1;
                 const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACCW;
@@ -653,28 +674,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_wait();
                     if (c16 + 16 >= cw) release_acc(acc);
                     float o[16];
+                    if (interior) {
+                        // every tap of every pixel in the image, tap kw kw*d rows on
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(v[0][i]);
+                        for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(v[0][i]);
 #pragma unroll
-                    for (int kw = 1; kw < kFoldMaxKW; ++kw)
-                        if (kw < p.win_kw) {
-                            const int sh = kw * p.win_d;
+                        for (int kw = 1; kw < kFoldMaxKW; ++kw)
+                            if (kw < p.win_kw) {
+                                const int sh = kw * p.win_d;
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                o[i] += __shfl_down_sync(0xffffffffu, __uint_as_float(v[kw][i]), sh);
-                        }
-                    if (!live) continue;
-                    if (p.bias != nullptr) {
-                        const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + co0);
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const uint4 b = __ldg(b4 + q);
-                            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                o[8 * q + 2 * e] += bf16_bits_to_float(static_cast<uint16_t>(bw[e] & 0xFFFFu));
-                                o[8 * q + 2 * e + 1] += bf16_bits_to_float(static_cast<uint16_t>(bw[e] >> 16));
+                                for (int i = 0; i < 16; ++i)
+                                    o[i] += __shfl_down_sync(0xffffffffu, __uint_as_float(v[kw][i]), sh);
                             }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] = 0.f;
+#pragma unroll
+                        for (int kw = 0; kw < kFoldMaxKW; ++kw)
+                            if (kw < p.win_kw) {
+                                // source row, kept in the warp for taps that are left out
+                                const int src = (col0 + kw * p.win_d - c0) & 31;
+                                const bool use = (taps >> kw) & 1u;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    const float t =
+                                        __shfl_sync(0xffffffffu, __uint_as_float(v[kw][i]), src);
+                                    o[i] += use ? t : 0.f;
+                                }
+                            }
+                    }
+                    if (!live) continue;
+                    {
+                        const float4* bs = reinterpret_cast<const float4*>(sBiasF + co0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 bq = bs[q];
+                            o[4 * q] += bq.x;
+                            o[4 * q + 1] += bq.y;
+                            o[4 * q + 2] += bq.z;
+                            o[4 * q + 3] += bq.w;
                         }
                     }
                     const long long at = m * p.C_out + co0;
@@ -1413,8 +1451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (the folded window: MMA width KW*C_out, 64-byte rows of 32 channels)
             const uint32_t idesc = FOLD ? ptx::idesc_bf16_f32(BM, p.fold_n)
                                         : ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
-            const uint64_t a_desc0 = FOLD ? ptx::sdesc_k_major_sw64(ptx::smem_addr(sA))
-                                          : ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
+            const uint64_t a_desc0 =
+                FOLD ? ptx::sdesc_k_major_sw64(ptx::smem_addr(sA), static_cast<uint32_t>(p.x_KH) * 512u)
+                     : ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
             const uint64_t b_desc0 = FOLD ? ptx::sdesc_k_major_sw64(ptx::smem_addr(sB))
                                           : ptx::sdesc_k_major_sw128(ptx::smem_addr(sB));
             const uint32_t a_slot_step = AST >> 4;
@@ -1500,8 +1539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     bd0 + (q >> 2) * b_blk_step + 2 * (q & 3), idesc,
                                                     q != 0 ? 1u : acc0);
                         } else if (FOLD) {
-                            // The stage holds one 128-row block per kh (four segments of
-                            // 32 input columns x 32 channels); weight block kh is KW*C_out
+                            // Rows of kh: 16 groups of eight (four per segment), KH * 512
+                            // bytes apart from kh * 512 on; weight block kh is KW*C_out
                             // rows (kw, co).  Two 16-channel steps per kh.
                             const uint32_t b_kh_step = static_cast<uint32_t>(p.fold_n * 64) >> 4;
 #pragma unroll
@@ -1510,7 +1549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                     for (int kk = 0; kk < 2; ++kk)
                                         mma_issue<PAIR>(d_tmem,
-                                                        ad + static_cast<uint32_t>(kh) * (kFoldKhBytes >> 4) + 2 * kk,
+                                                        ad + static_cast<uint32_t>(kh) * (512u >> 4) + 2 * kk,
                                                         b_desc0 + static_cast<uint32_t>(kh) * b_kh_step + 2 * kk,
                                                         idesc, (kh != 0 || kk != 0) ? 1u : 0u);
                                 }
@@ -1775,21 +1814,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                        kTx * (PAIR ? 2u : 1u));
                         if (FOLD) {
                             // Segments 4*m0 .. 4*m0 + 3 (past the last one, the last
-                            // again, whose outputs the epilogue discards): per kh, 32
-                            // input columns from k*fold_g - p of input row ho - p + kh*d,
-                            // into rows 32*q .. of the stage's kh block.  TMA zero-fills
-                            // columns and rows outside the image.
+                            // again, whose outputs the epilogue discards): one box per
+                            // segment, its 32 input columns from c0 of the KH input rows
+                            // ho - p + kh*d, laid out as four groups of eight columns,
+                            // each group holding its KH rows in turn.  Segment q lands at
+                            // q * KH * 2048, so the rows of one kh are 8-row groups
+                            // KH * 512 bytes apart.  TMA zero-fills rows outside the
+                            // image; the columns all lie inside it.
                             for (int q = 0; q < 4; ++q) {
                                 const int g = min(u.m0 * 4 + q, p.fold_segs - 1);
                                 uint32_t row, k, n, ho;
                                 p.fold_spr_div.divmod(static_cast<uint32_t>(g), row, k);
                                 p.ho_div.divmod(row, n, ho);
-                                const int w0 = static_cast<int>(k) * p.fold_g - p.win_pad;
-                                for (int kh = 0; kh < p.x_KH; ++kh)
-                                    ptx::tma_load_4d(sA + ring.stage * AST + kh * kFoldKhBytes + q * 2048,
-                                                     &tmap_a, &full_b[ring.stage], 0, w0,
-                                                     static_cast<int>(ho) - p.win_pad + kh * p.win_d,
-                                                     static_cast<int>(n));
+                                const int c0 =
+                                    min(max(static_cast<int>(k) * p.fold_g - p.win_pad, 0), p.x_W - 32);
+                                ptx::tma_load_5d(sA + ring.stage * AST + q * p.x_KH * 2048, &tmap_a,
+                                                 &full_b[ring.stage], 0, c0,
+                                                 static_cast<int>(ho) - p.win_pad, 0,
+                                                 static_cast<int>(n));
                             }
                         } else if (IM2WIN) {
                             ptx::tma_load_3d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
@@ -1953,9 +1995,10 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         // columns (a multiple of 16 that fits one BN-column accumulator slot),
         // one K block per tile, weights resident, no split, direct stores
         const bool ok = (BN == 128 || BN == 256) && p.C_in == 32 && p.C_out % 32 == 0 &&
+                        p.C_out * 4 <= kFoldBiasBytes &&
                         p.fold_n == p.win_kw * p.C_out && p.fold_n % 16 == 0 && p.fold_n >= 16 &&
                         p.fold_n <= BN && p.win_kw >= 1 && p.win_kw <= kFoldMaxKW &&
-                        p.x_KH >= 1 && p.x_KH <= kFoldMaxKH && p.win_d >= 1 &&
+                        p.x_KH >= 1 && p.x_KH <= kFoldMaxKH && p.win_d >= 1 && p.x_W >= 32 &&
                         p.fold_g == 32 - (p.win_kw - 1) * p.win_d && p.fold_g >= 1 &&
                         p.a_stage_bytes == p.x_KH * kFoldKhBytes && p.num_kb == 1 &&
                         p.fold_bbytes >= p.x_KH * p.fold_n * 64 && p.fold_bbytes % 1024 == 0 &&
@@ -2083,7 +2126,7 @@ int window_stage_rows(int kw, int d) { return (BM + (kw - 1) * d + 7) / 8 * 8; }
 
 int fold_smem_bytes(int b_bytes, int stages, int a_stage_bytes)
 {
-    return kHeaderBytes + 1024 + b_bytes + stages * a_stage_bytes;
+    return kHeaderBytes + 1024 + b_bytes + stages * a_stage_bytes + kFoldBiasBytes;
 }
 
 int plane_smem_bytes(int bn, int a_stages, int a_stage_bytes, int b_blocks, int extra_bytes)

@@ -168,18 +168,21 @@ enum AMode : int {
     kAStemWin1 = 14,
     kAStemWin4 = 15,
     kAWinFold = 16,   // C_in = 32, stride 1: the KW taps folded into the MMA's columns.  A row
-                      // r of a tile is input column w0 + (r % 32) of one 32-column segment
-                      // (four segments per tile, one per TMEM lane quarter) with K = (kh, ci);
-                      // B row (kw, co) holds w[co][kh][kw][ci]; the epilogue sums column
-                      // block kw of row r + kw*d into output pixel r (warp shuffles), so a
-                      // segment yields 32 - (KW-1)*d output pixels
+                      // r of a tile is input column c0 + (r % 32) of one 32-column segment
+                      // inside the image row (four segments per tile, one per TMEM lane
+                      // quarter, each loaded by one TMA box) with K = (kh, ci); B row
+                      // (kw, co) holds w[co][kh][kw][ci]; the epilogue sums, for each output
+                      // pixel, column block kw of the row holding its tap-kw column (warp
+                      // shuffles; taps in the padding are left out), so a segment yields
+                      // 32 - (KW-1)*d output pixels
 };
 // The folded window's limits: kernel width (registers of the epilogue's shuffle
-// sum), kernel height (the unrolled MMA sequence), and bytes of one kh block of
+// sum), kernel height (the unrolled MMA sequence), and bytes of one kh plane of
 // an A stage (128 rows of 32 channels).
 constexpr int kFoldMaxKW = 5;
 constexpr int kFoldMaxKH = 7;
 constexpr int kFoldKhBytes = 128 * 64;
+constexpr int kFoldBiasBytes = 1024;  // the bias as fp32, after the A stages
 // The staged-window stem's A mode for a stride (1, 2 or 4).
 constexpr int stemwin_amode(int s) { return s == 1 ? kAStemWin1 : s == 4 ? kAStemWin4 : kAStemWin; }
 constexpr bool is_stemwin(int amode)
@@ -199,7 +202,7 @@ int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per
 // Rows of an A ring slot in window mode (128 plus the tap spill, rounded to 8).
 int window_stage_rows(int kw, int d);
 // Dynamic shared memory of a folded-window CTA: resident weights of b_bytes
-// (a multiple of 1024) and `stages` A stages.
+// (a multiple of 1024), `stages` A stages and the fp32 bias.
 int fold_smem_bytes(int b_bytes, int stages, int a_stage_bytes);
 // Dynamic shared memory of a plane-mode CTA: a_stages A slots, b_blocks weight
 // blocks (resident or ring), plus extra bytes.

@@ -133,6 +133,18 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// 5-D tiled bulk tensor load (c0 innermost), as tma_load_4d.
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3, int c4)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3), "r"(c4)
+        : "memory");
+}
+
 // Four rows of a 2-D tensor, chosen by row index, each `box` columns wide from
 // column c0, into four consecutive shared-memory rows at `dst` (tile::gather4;
 // the tensor map's box is one row high).  Rows outside the tensor read as zero.
@@ -360,12 +372,14 @@ __device__ __forceinline__ uint64_t sdesc_k_major_sw128(uint32_t saddr)
 // bytes (32 bf16), 16-byte chunk c of row r at r*64 + ((c ^ ((r >> 1) & 3)) * 16),
 // 8-row groups 512 bytes apart; the tile starts on a 512-byte boundary, and
 // the second 16-element K step starts 32 bytes into the row.
-__device__ __forceinline__ uint64_t sdesc_k_major_sw64(uint32_t saddr)
+// `sbo`: bytes from one 8-row group to the next (512 when the rows are dense; a
+// multiple of 512 when the groups of several planes are interleaved).
+__device__ __forceinline__ uint64_t sdesc_k_major_sw64(uint32_t saddr, uint32_t sbo = 512u)
 {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address >> 4, bits 0-13
     d |= static_cast<uint64_t>(1u) << 16;                  // leading byte offset (unused here)
-    d |= static_cast<uint64_t>(512u >> 4) << 32;           // stride byte offset: 8 rows
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;  // stride byte offset
     d |= static_cast<uint64_t>(1u) << 46;                  // descriptor version for tcgen05
     d |= static_cast<uint64_t>(4u) << 61;                  // 64-byte swizzle
     return d;

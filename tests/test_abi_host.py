@@ -120,7 +120,8 @@ def expected_path(c):
     G = 32 - (c.KW - 1) * c.dilation
     Wo = oracle.output_size(c.W, c.KW, c.stride, c.pad, c.dilation)
     if (c.stride == 1 and c.C_in == 32 and c.C_out % 32 == 0 and c.KW <= 5 and c.KH <= 7 and
-            G >= 8 and c.KW * c.C_out <= 256 and Wo >= 12 * -(-Wo // G)):
+            G >= 8 and c.KW * c.C_out <= 256 and c.W >= 32 and c.dilation <= 8 and
+            Wo >= 12 * -(-Wo // G)):
         return 8
     return 1  # indirection-buffer gather
 
@@ -142,8 +143,10 @@ def test_winfold_selection_and_plan(lib):
     assert pl["m_tiles"] == (128 * 150 * 5 + 3) // 4 and pl["k_blocks"] == 1
     assert pl["weights_resident"] == 1 and pl["splits"] == 1 and pl["tma_store"] == 0
     assert lib.workspace_size(128, 32, 150, 150, 32, 3, 3, 1, 1, 1) == 0
-    # narrow rows (8 output pixels per 32-row segment) stay on the gather path
+    # rows narrower than a 32-pixel segment stay on the gather path
     assert lib.select_path(4, 32, 8, 8, 32, 3, 3, 1, 1, 1) == 1
+    assert lib.select_path(4, 32, 31, 31, 32, 3, 3, 1, 1, 1) == 1
+    assert lib.select_path(4, 32, 32, 32, 32, 3, 3, 1, 1, 1) == 8
     # C_out not a multiple of 32, stride 2, or KW*C_out past 256: not folded
     assert lib.select_path(4, 32, 40, 40, 48, 3, 3, 1, 1, 1) == 1
     assert lib.select_path(4, 32, 40, 40, 32, 3, 3, 2, 1, 1) == 1

@@ -219,10 +219,12 @@ def test_stem_path_explicit_matches_oracle(gpu_lib, shape):
 
 
 # Folded window (C_in = 32, stride 1): KW taps folded into the MMA's columns,
-# the epilogue's shuffle sum across rows.  Ragged segments (W_out not a multiple
-# of G), 64 output channels (192-column MMA), dilation 2 (G = 28), 5x5 and 7x5
+# the epilogue's shuffle sum across rows, padding columns left out of the sum.
+# Ragged segments (W_out not a multiple of G), 64 output channels (192-column
+# MMA), dilation 2 (G = 28, a row step of 2 in the segment's box), 5x5 and 7x5
 # kernels (160-column MMA, KH up to 7), one kernel row, one kernel column with
-# padding, and no padding.
+# padding, no padding, rows exactly 32 pixels wide, and padding wider than the
+# dilated kernel's reach into the image.
 FOLD_SHAPES = [
     S("winfold_3x3_c32_ragged", N=2, C_in=32, H=9, W=37, C_out=32, seed=100),
     S("winfold_3x3_cout64", N=2, C_in=32, H=11, W=45, C_out=64, seed=101),
@@ -232,6 +234,8 @@ FOLD_SHAPES = [
     S("winfold_3x1_cout96", N=2, C_in=32, H=12, W=40, C_out=96, KH=3, KW=1, pad=1, seed=105),
     S("winfold_7x5", N=1, C_in=32, H=16, W=40, C_out=32, KH=7, KW=5, pad=3, seed=106),
     S("winfold_p0", N=3, C_in=32, H=8, W=70, C_out=32, pad=0, seed=107),
+    S("winfold_w32_p2", N=2, C_in=32, H=6, W=32, C_out=32, pad=2, seed=108),
+    S("winfold_d2_p5", N=1, C_in=32, H=9, W=40, C_out=32, pad=5, dilation=2, seed=109),
 ]
 
 
@@ -278,9 +282,10 @@ def test_winfold_unaligned_output(gpu_lib):
 # tails at scale), with small K so the oracle checks every element in seconds.
 MULTI_TILE = [
     (S("multi_gather_c32", N=130, C_in=32, H=30, W=30, C_out=32, seed=70), 1, 1),
-    # folded window: one segment per output row (G = 30 = W_out), then two per
-    # row with 64 output channels (192-column MMAs, two 256-column accumulators)
-    (S("multi_winfold_c32", N=130, C_in=32, H=30, W=30, C_out=32, seed=83), 0, 16),
+    # folded window: two segments per 32-pixel output row (the second one
+    # right-aligned in the row), then 64 output channels (192-column MMAs, two
+    # 256-column accumulators)
+    (S("multi_winfold_c32", N=130, C_in=32, H=30, W=32, C_out=32, seed=83), 0, 16),
     (S("multi_winfold_c32_cout64", N=64, C_in=32, H=30, W=40, C_out=64, seed=84), 8, 16),
     (S("multi_tmagather_c64_s2", N=519, C_in=64, H=30, W=30, C_out=64, stride=2, seed=71), 0, 3),
     (S("multi_tmagather_pair_1x1_p1_s2", N=456, C_in=64, H=30, W=30, C_out=256, KH=1, KW=1,
