@@ -181,10 +181,11 @@ typedef struct convgb_plan {
     int stream_k;         /* 1: each CTA (pair) takes an equal share of all (tile, K block)
                              steps; tiles split between CTAs meet in fp32 partial sums */
     int segment_outputs;  /* CONVGB_PATH_WINFOLD: output pixels per segment, G (0 on other
-                             paths).  Each output row is cut into ceil(W_out / G)
-                             segments of G pixels (the last one shorter); segments are
-                             numbered row by row ((n, ho) order) and tile t holds
-                             segments 4t .. 4t+3, so tile_rows is 0 */
+                             paths).  Each output row is cut into spr = ceil(W_out / G)
+                             segments of G pixels (the last one shorter) and the
+                             output rows of an image into HB = ceil(H_out / 4) blocks
+                             of four; tile t = (n*HB + hb)*spr + k holds segment k of
+                             rows 4*hb .. 4*hb + 3 of image n, so tile_rows is 0 */
 } convgb_plan;
 
 /* Fills *plan with what conv2d_fwd_path(path, ...) would launch for this shape

@@ -205,31 +205,35 @@ StemWinGeom stemwin_geom(const ConvShape& c)
 }
 
 // Folded-window geometry (C_in = 32, stride 1).  A segment is 32 consecutive
-// input columns of one output row's KH input rows; with the KW taps folded into
-// the MMA's columns it yields G = 32 - (KW-1)*d output pixels (the rest of its
-// rows only feed its neighbours' sums).  spr segments cover an output row, four
-// make a tile.  The MMA is KW*C_out columns wide and the weights of all KH
-// blocks stay resident.
+// input columns inside the image row; with the KW taps folded into the MMA's
+// columns it yields G = 32 - (KW-1)*d output pixels of an output row (the rest
+// of its columns only feed its neighbours' sums).  spr segments cover an output
+// row.  A tile is one segment of four consecutive output rows (HB = ceil(H_out
+// / 4) row blocks per image), whose R = 4 + (KH-1)*d input rows one TMA box
+// stages.  The MMA is KW*C_out columns wide and the weights of all KH blocks
+// stay resident.
 struct FoldGeom {
     bool ok = false;
-    int G = 0, spr = 0, n_mma = 0, b_bytes = 0;
-    long long segs = 0;
+    int G = 0, spr = 0, HB = 0, R = 0, n_mma = 0, b_bytes = 0;
+    long long tiles = 0;
 };
 FoldGeom fold_geom(const ConvShape& c)
 {
     FoldGeom f;
     if (c.s != 1 || c.C_in != 32 || c.C_out % 32 != 0) return f;
     if (c.KW > kFoldMaxKW || c.KH > kFoldMaxKH) return f;
-    // segments are 32 columns inside the row; the row box spans (KH-1)*d + 1 rows
-    // with a row step d (a TMA element stride, at most 8)
-    if (c.W < 32 || c.d > 8 || (c.KH - 1) * c.d + 1 > 256) return f;
+    // segments are 32 columns inside the row; a box spans R rows
+    if (c.W < 32) return f;
+    f.R = kFoldRows + (c.KH - 1) * c.d;
+    if (f.R > 256) return f;
     f.G = 32 - (c.KW - 1) * c.d;
     if (f.G < 8) return f;
     f.n_mma = c.KW * c.C_out;
     if (f.n_mma > 256 || f.n_mma % 16 != 0) return f;
     f.spr = (c.W_out + f.G - 1) / f.G;
-    f.segs = (long long)c.N * c.H_out * f.spr;
-    if (f.segs >= (1LL << 31) - 4) return f;
+    f.HB = (c.H_out + kFoldRows - 1) / kFoldRows;
+    f.tiles = (long long)c.N * f.HB * f.spr;
+    if (f.tiles >= (1LL << 31)) return f;
     f.b_bytes = (c.KH * f.n_mma * 64 + 1023) / 1024 * 1024;
     f.ok = true;
     return f;
@@ -374,22 +378,20 @@ bool encode_strided(CUtensorMap* m, const void* x, const ConvShape& c, int R)
     return r == CUDA_SUCCESS;
 }
 
-// Folded window: x [N][H][W][32] as a 5-D tensor (channel, column, row, group
-// of eight columns, image), the group dimension 512 bytes (eight pixels) apart
-// and overlapping the column dimension.  A box of 32 channels x 8 columns x the
-// KH rows (every d-th) x 4 groups is one segment: 32 consecutive columns of its
-// KH input rows, stored group by group with each group's KH rows in turn
-// (64-byte swizzle).  The segments' columns always lie inside the row, so the
-// column bounds never apply; rows outside the image read as zero.
-bool encode_fold_x(CUtensorMap* m, const void* x, const ConvShape& c)
+// Folded window: x [N][H][W][32] as a 4-D tensor; a box of 32 channels x 32
+// columns x R rows is one tile's staging: R consecutive input rows of one
+// segment (64-byte swizzle, 2 KB per row).  The segments' columns always lie
+// inside the row, so the column bounds never apply; rows outside the image read
+// as zero.
+bool encode_fold_x(CUtensorMap* m, const void* x, const ConvShape& c, int R)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[5] = {32u, (cuuint64_t)c.W, (cuuint64_t)c.H, 4u, (cuuint64_t)c.N};
-    cuuint64_t strides[4] = {64u, (cuuint64_t)c.W * 64, 512u, (cuuint64_t)c.H * c.W * 64};
-    cuuint32_t box[5] = {32u, 8u, (cuuint32_t)((c.KH - 1) * c.d + 1), 4u, 1u};
-    cuuint32_t estr[5] = {1u, 1u, (cuuint32_t)c.d, 1u, 1u};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(x), dims, strides,
+    cuuint64_t dims[4] = {32u, (cuuint64_t)c.W, (cuuint64_t)c.H, (cuuint64_t)c.N};
+    cuuint64_t strides[3] = {64u, (cuuint64_t)c.W * 64, (cuuint64_t)c.H * c.W * 64};
+    cuuint32_t box[4] = {32u, 32u, (cuuint32_t)R, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -764,8 +766,8 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         return g;
     }
     if (path == CONVGB_PATH_WINFOLD) {
-        // One A stage per tile: KH blocks of four 32-row segments.  Accumulator
-        // slots of 128 columns (256 when the MMA is wider).
+        // One A stage per tile: the R staged input rows of its segment.
+        // Accumulator slots of 128 columns (256 when the MMA is wider).
         const FoldGeom f = fold_geom(c);
         g.amode = kAWinFold;
         if (!f.ok) return g;  // stages == 0: not applicable
@@ -773,11 +775,11 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         g.K = (long long)c.KH * 32;
         g.num_kb = 1;
         g.m_step = 1;
-        g.m_tiles = (int)((f.segs + 3) / 4);
+        g.m_tiles = (int)f.tiles;
         g.bn = f.n_mma <= 128 ? 128 : 256;
         g.n_tiles = 1;
         g.bres = 1;
-        g.a_stage_bytes = c.KH * kFoldKhBytes;
+        g.a_stage_bytes = f.R * kFoldRowBytes;
         for (int st = 8; st >= 2 && !g.stages; --st)
             if (fold_smem_bytes(f.b_bytes, st, g.a_stage_bytes) <= smem_limit()) g.stages = st;
         return g;
@@ -1005,7 +1007,8 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         !encode_kmajor(&out->tb, a.w, a.C_out, g.K, g.pair ? g.bn / 2 : g.bn))
         return CONVGB_ERR_CUDA;
     if (g.amode == kAWinFold &&
-        (!encode_fold_x(&out->ta, a.x, *a.shape) || !encode_fold_w(&out->tb, a.w, *a.shape)))
+        (!encode_fold_x(&out->ta, a.x, *a.shape, fold_geom(*a.shape).R) ||
+         !encode_fold_w(&out->tb, a.w, *a.shape)))
         return CONVGB_ERR_CUDA;
     if (g.amode == kADense && !encode_kmajor(&out->ta, a.a_dense, g.M, g.K, 128))
         return CONVGB_ERR_CUDA;
@@ -1144,7 +1147,8 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.x_W = c.W;
         p.ho_div = FastDiv((uint32_t)c.H_out);
         p.fold_g = f.G;
-        p.fold_segs = (int)f.segs;
+        p.fold_hout = c.H_out;
+        p.fold_hb_div = FastDiv((uint32_t)f.HB);
         p.fold_n = f.n_mma;
         p.fold_bbytes = f.b_bytes;
         p.fold_spr_div = FastDiv((uint32_t)f.spr);

@@ -513,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t s = 0; s < SB; ++s) ptx::mbar_init(&empty_b[s], 1);
         for (uint32_t i = 0; i < NACC; ++i) {
             ptx::mbar_init(&tfull[i], 1);
-            ptx::mbar_init(&tempty[i], PAIR ? 2 * kEpiN : kEpiN);
+            // (the folded window: one warp group drains each accumulator)
+            ptx::mbar_init(&tempty[i], PAIR ? 2 * kEpiN : FOLD ? kEpiThreads : kEpiN);
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(bres_full, 1);
@@ -619,6 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int bias_n0 = -1;
         Ring ar;  // accumulator index and the parity of its current use
         for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt, ar.next(NACC)) {
+            // folded window: warps 0-3 take the even tiles, 4-7 the odd ones (measured
+            // on the 32-channel 3x3 layer at 150x150: 144 -> 124 us against both
+            // groups converting half of every tile's channels)
+            if (FOLD && (lt & 1u) != static_cast<uint32_t>(half)) continue;
             const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
             const uint32_t acc = ar.stage;
             // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds,
@@ -634,20 +639,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ready) break;
             ptx::tc_fence_after();
             if (FOLD) {
-                // Lane quarter `quad` holds segment 4*m0 + quad: accumulator row r
-                // is input column c0 + r, and its column block kw (KW*C_out columns
-                // in all) is tap kw's share of the output pixel that reads column
-                // c0 + r through tap kw.  The segment owns output pixels k*G ..
-                // k*G + G - 1 of its row; lane l computes pixel wo = k*G + l as the
-                // sum over the taps whose column wo - p + kw*d lies in the image of
-                // block kw of row wo - p + kw*d - c0 (a shuffle; taps outside the
-                // image are the zero padding and are left out).  Warp w converts
-                // the channel half w / 4.
-                const int g = u.m0 * 4 + quad;
-                uint32_t row = 0, k = 0;
-                if (g < p.fold_segs) p.fold_spr_div.divmod(static_cast<uint32_t>(g), row, k);
+                // Lane quarter `quad` holds output row ho = 4*hb + quad of the tile:
+                // accumulator row r is input column c0 + r, and its column block kw
+                // (KW*C_out columns in all) is tap kw's share of the output pixel that
+                // reads column c0 + r through tap kw.  The segment owns output pixels
+                // k*G .. k*G + G - 1 of the row; lane l computes pixel wo = k*G + l as
+                // the sum over the taps whose column wo - p + kw*d lies in the image
+                // of block kw of row wo - p + kw*d - c0 (a shuffle; taps outside the
+                // image are the zero padding and are left out).  The warp groups 0-3
+                // and 4-7 take alternate tiles, each converting all C_out channels.
+                uint32_t nhb, k, n, hb;
+                p.fold_spr_div.divmod(static_cast<uint32_t>(u.m0), nhb, k);
+                p.fold_hb_div.divmod(nhb, n, hb);
+                const int ho = static_cast<int>(hb) * kFoldRows + quad;
                 const int wo = static_cast<int>(k) * p.fold_g + lane;
-                const bool live = g < p.fold_segs && lane < p.fold_g && wo < p.win_wout;
+                const bool live = ho < p.fold_hout && lane < p.fold_g && wo < p.win_wout;
                 const int c0 = min(max(static_cast<int>(k) * p.fold_g - p.win_pad, 0), p.x_W - 32);
                 const int col0 = wo - p.win_pad;  // column of tap 0
                 uint32_t taps = 0;                // taps whose column lies in the image
@@ -659,12 +665,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // a segment that starts at k*G - p lies inside the row with every
                 // tap of its pixels (warp-uniform)
                 const bool interior = c0 == static_cast<int>(k) * p.fold_g - p.win_pad;
-                const long long m = static_cast<long long>(row) * p.win_wout + wo;
-                const int cw = p.C_out >> 1;
+                const long long m =
+                    (static_cast<long long>(n) * p.fold_hout + ho) * p.win_wout + wo;
+                const int cw = p.C_out;
                 const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACCW;
 #pragma unroll 1
                 for (int c16 = 0; c16 < cw; c16 += 16) {
-                    const int co0 = half * cw + c16;
+                    const int co0 = c16;
                     uint32_t v[kFoldMaxKW][16];
 #pragma unroll
                     for (int kw = 0; kw < kFoldMaxKW; ++kw)
@@ -1451,9 +1458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (the folded window: MMA width KW*C_out, 64-byte rows of 32 channels)
             const uint32_t idesc = FOLD ? ptx::idesc_bf16_f32(BM, p.fold_n)
                                         : ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
-            const uint64_t a_desc0 =
-                FOLD ? ptx::sdesc_k_major_sw64(ptx::smem_addr(sA), static_cast<uint32_t>(p.x_KH) * 512u)
-                     : ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
+            const uint64_t a_desc0 = FOLD ? ptx::sdesc_k_major_sw64(ptx::smem_addr(sA))
+                                          : ptx::sdesc_k_major_sw128(ptx::smem_addr(sA));
             const uint64_t b_desc0 = FOLD ? ptx::sdesc_k_major_sw64(ptx::smem_addr(sB))
                                           : ptx::sdesc_k_major_sw128(ptx::smem_addr(sB));
             const uint32_t a_slot_step = AST >> 4;
@@ -1539,9 +1545,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     bd0 + (q >> 2) * b_blk_step + 2 * (q & 3), idesc,
                                                     q != 0 ? 1u : acc0);
                         } else if (FOLD) {
-                            // Rows of kh: 16 groups of eight (four per segment), KH * 512
-                            // bytes apart from kh * 512 on; weight block kh is KW*C_out
-                            // rows (kw, co).  Two 16-channel steps per kh.
+                            // Tap row kh: the 128 rows from staged row kh*d on (lane
+                            // quarter q reads input row 4*hb - p + q + kh*d); weight
+                            // block kh is KW*C_out rows (kw, co).  Two 16-channel steps
+                            // per kh.
+                            const uint32_t a_kh_step =
+                                static_cast<uint32_t>(p.win_d * kFoldRowBytes) >> 4;
                             const uint32_t b_kh_step = static_cast<uint32_t>(p.fold_n * 64) >> 4;
 #pragma unroll
                             for (int kh = 0; kh < kFoldMaxKH; ++kh)
@@ -1549,7 +1558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                     for (int kk = 0; kk < 2; ++kk)
                                         mma_issue<PAIR>(d_tmem,
-                                                        ad + static_cast<uint32_t>(kh) * (512u >> 4) + 2 * kk,
+                                                        ad + static_cast<uint32_t>(kh) * a_kh_step + 2 * kk,
                                                         b_desc0 + static_cast<uint32_t>(kh) * b_kh_step + 2 * kk,
                                                         idesc, (kh != 0 || kk != 0) ? 1u : 0u);
                                 }
@@ -1813,26 +1822,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::mbar_arrive_expect_tx(&full_b[ring.stage],
                                                        kTx * (PAIR ? 2u : 1u));
                         if (FOLD) {
-                            // Segments 4*m0 .. 4*m0 + 3 (past the last one, the last
-                            // again, whose outputs the epilogue discards): one box per
-                            // segment, its 32 input columns from c0 of the KH input rows
-                            // ho - p + kh*d, laid out as four groups of eight columns,
-                            // each group holding its KH rows in turn.  Segment q lands at
-                            // q * KH * 2048, so the rows of one kh are 8-row groups
-                            // KH * 512 bytes apart.  TMA zero-fills rows outside the
-                            // image; the columns all lie inside it.
-                            for (int q = 0; q < 4; ++q) {
-                                const int g = min(u.m0 * 4 + q, p.fold_segs - 1);
-                                uint32_t row, k, n, ho;
-                                p.fold_spr_div.divmod(static_cast<uint32_t>(g), row, k);
-                                p.ho_div.divmod(row, n, ho);
-                                const int c0 =
-                                    min(max(static_cast<int>(k) * p.fold_g - p.win_pad, 0), p.x_W - 32);
-                                ptx::tma_load_5d(sA + ring.stage * AST + q * p.x_KH * 2048, &tmap_a,
-                                                 &full_b[ring.stage], 0, c0,
-                                                 static_cast<int>(ho) - p.win_pad, 0,
-                                                 static_cast<int>(n));
-                            }
+                            // One box: the 32 input columns from c0 of input rows
+                            // 4*hb - p .. 4*hb - p + 3 + (KH-1)*d, row after row (2 KB
+                            // each).  TMA zero-fills rows outside the image; the columns
+                            // all lie inside it.
+                            uint32_t nhb, k, n, hb;
+                            p.fold_spr_div.divmod(static_cast<uint32_t>(u.m0), nhb, k);
+                            p.fold_hb_div.divmod(nhb, n, hb);
+                            const int c0 =
+                                min(max(static_cast<int>(k) * p.fold_g - p.win_pad, 0), p.x_W - 32);
+                            ptx::tma_load_4d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage], 0,
+                                             c0, static_cast<int>(hb) * kFoldRows - p.win_pad,
+                                             static_cast<int>(n));
                         } else if (IM2WIN) {
                             ptx::tma_load_3d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, 0, u.m0);
@@ -2000,10 +2001,11 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
                         p.fold_n <= BN && p.win_kw >= 1 && p.win_kw <= kFoldMaxKW &&
                         p.x_KH >= 1 && p.x_KH <= kFoldMaxKH && p.win_d >= 1 && p.x_W >= 32 &&
                         p.fold_g == 32 - (p.win_kw - 1) * p.win_d && p.fold_g >= 1 &&
-                        p.a_stage_bytes == p.x_KH * kFoldKhBytes && p.num_kb == 1 &&
+                        p.a_stage_bytes == (kFoldRows + (p.x_KH - 1) * p.win_d) * kFoldRowBytes &&
+                        kFoldRows + (p.x_KH - 1) * p.win_d <= 256 && p.num_kb == 1 &&
                         p.fold_bbytes >= p.x_KH * p.fold_n * 64 && p.fold_bbytes % 1024 == 0 &&
                         p.bres == 1 && p.n_tiles == 1 && p.splits == 1 && !p.sk && !p.tma_store &&
-                        p.fold_segs >= 1 && p.m_tiles == (p.fold_segs + 3) / 4 && p.m_step == 1;
+                        p.fold_hout >= 1 && p.m_tiles >= 1 && p.m_step == 1;
         if (!ok) return cudaErrorInvalidValue;
     }
     if (kPlane &&

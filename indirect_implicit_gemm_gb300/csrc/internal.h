@@ -98,11 +98,13 @@ struct IgemmParams {
     int pl_nacc;             // accumulators in tensor memory (each pl_u*BN columns)
     int b_stages;            // streamed weights: B ring slots of one 64-column block
     FastDiv hp_div;          // divides a virtual row index by H + 2p
-    // folded window (kAWinFold): fold_g output pixels per 32-column segment,
-    // fold_segs segments in all (fold_spr_div divides by the segments of an output
-    // row), MMA width fold_n = KW * C_out, resident weight bytes fold_bbytes
-    int fold_g, fold_segs, fold_n, fold_bbytes;
-    FastDiv fold_spr_div;
+    // folded window (kAWinFold): a tile is column segment k (fold_g output pixels
+    // read through 32 input columns) of output rows 4*hb .. 4*hb + 3 of image n,
+    // tile = (n * HB + hb) * spr + k (fold_spr_div divides by the segments of a
+    // row, spr; fold_hb_div by the row blocks of an image, HB); MMA width fold_n =
+    // KW * C_out, resident weight bytes fold_bbytes, output height fold_hout
+    int fold_g, fold_n, fold_bbytes, fold_hout;
+    FastDiv fold_spr_div, fold_hb_div;
     int y_al32;              // 1: y starts on a 32-byte boundary (256-bit stores allowed)
     int tma_store;           // 1: epilogue stages 64-column chunks in shared memory and
                              //    stores them with TMA (bf16 y, C_out % 8 == 0, no split)
@@ -167,21 +169,23 @@ enum AMode : int {
                       // strides in one kernel the 7x7 stride-2 stem ran 100 us, not 65)
     kAStemWin1 = 14,
     kAStemWin4 = 15,
-    kAWinFold = 16,   // C_in = 32, stride 1: the KW taps folded into the MMA's columns.  A row
-                      // r of a tile is input column c0 + (r % 32) of one 32-column segment
-                      // inside the image row (four segments per tile, one per TMEM lane
-                      // quarter, each loaded by one TMA box) with K = (kh, ci); B row
-                      // (kw, co) holds w[co][kh][kw][ci]; the epilogue sums, for each output
-                      // pixel, column block kw of the row holding its tap-kw column (warp
-                      // shuffles; taps in the padding are left out), so a segment yields
-                      // 32 - (KW-1)*d output pixels
+    kAWinFold = 16,   // C_in = 32, stride 1: the KW taps folded into the MMA's columns.  A
+                      // tile is one 32-column segment (inside the image row) of four
+                      // consecutive output rows, one per TMEM lane quarter; one TMA box
+                      // stages its 4 + (KH-1)*d input rows and tap row kh reads them from
+                      // kh*d rows on.  A row r is input column c0 + (r % 32) with K = (kh,
+                      // ci); B row (kw, co) holds w[co][kh][kw][ci]; the epilogue sums, for
+                      // each output pixel, column block kw of the row holding its tap-kw
+                      // column (warp shuffles; taps in the padding are left out), so a
+                      // segment yields 32 - (KW-1)*d output pixels per row
 };
 // The folded window's limits: kernel width (registers of the epilogue's shuffle
-// sum), kernel height (the unrolled MMA sequence), and bytes of one kh plane of
-// an A stage (128 rows of 32 channels).
+// sum), kernel height (the unrolled MMA sequence); output rows per tile and bytes
+// of one staged input row segment (32 columns of 32 channels).
 constexpr int kFoldMaxKW = 5;
 constexpr int kFoldMaxKH = 7;
-constexpr int kFoldKhBytes = 128 * 64;
+constexpr int kFoldRows = 4;
+constexpr int kFoldRowBytes = 32 * 64;
 constexpr int kFoldBiasBytes = 1024;  // the bias as fp32, after the A stages
 // The staged-window stem's A mode for a stride (1, 2 or 4).
 constexpr int stemwin_amode(int s) { return s == 1 ? kAStemWin1 : s == 4 ? kAStemWin4 : kAStemWin; }

@@ -140,7 +140,7 @@ def test_winfold_selection_and_plan(lib):
     # 32 -> 32 3x3 at 150x150: segments of 30 output pixels, five per output row
     pl = lib.plan_info(128, 32, 150, 150, 32, 3, 3, 1, 1, 1)
     assert (pl["path"], pl["a_mode"], pl["segment_outputs"], pl["tile_rows"]) == (8, 16, 30, 0)
-    assert pl["m_tiles"] == (128 * 150 * 5 + 3) // 4 and pl["k_blocks"] == 1
+    assert pl["m_tiles"] == 128 * 38 * 5 and pl["k_blocks"] == 1  # 4-row blocks x segments
     assert pl["weights_resident"] == 1 and pl["splits"] == 1 and pl["tma_store"] == 0
     assert lib.workspace_size(128, 32, 150, 150, 32, 3, 3, 1, 1, 1) == 0
     # rows narrower than a 32-pixel segment stay on the gather path

@@ -40,21 +40,25 @@ def border_points(shape, Ho, Wo):
 
 
 def fold_tile_points(shape, plan, Ho, Wo, rng, per_tile=PER_TILE):
-    """Folded-window plans: tile t holds segments 4t .. 4t+3, segment g being the
-    G = segment_outputs output pixels from k*G of output row g // spr (spr
-    segments per row, the last one shorter).  per_tile / 4 (at least one)
-    random outputs in every segment, so every tile gets per_tile of them."""
+    """Folded-window plans: tile t = (n*HB + hb)*spr + k holds output pixels
+    k*G .. k*G + G - 1 (G = segment_outputs, spr segments per row, the last one
+    shorter) of output rows 4*hb .. 4*hb + 3 (HB = ceil(H_out / 4) row blocks).
+    per_tile / 4 (at least one) random outputs in each of a tile's rows."""
     G = plan["segment_outputs"]
     spr = -(-Wo // G)
-    segs = shape.N * Ho * spr
-    assert plan["m_tiles"] == -(-segs // 4), plan
-    per_seg = max(1, per_tile // 4)
-    g = np.repeat(np.arange(segs, dtype=np.int64), per_seg)
-    row, k = np.divmod(g, spr)
+    HB = -(-Ho // 4)
+    assert plan["m_tiles"] == shape.N * HB * spr, plan
+    per_row = max(1, per_tile // 4)
+    t = np.repeat(np.arange(plan["m_tiles"], dtype=np.int64), 4 * per_row)
+    q = np.tile(np.repeat(np.arange(4, dtype=np.int64), per_row), plan["m_tiles"])
+    nhb, k = np.divmod(t, spr)
+    n, hb = np.divmod(nhb, HB)
+    ho = hb * 4 + q
+    keep = ho < Ho
+    t, k, n, ho = t[keep], k[keep], n[keep], ho[keep]
     span = np.minimum(Wo, (k + 1) * G) - k * G
-    wo = k * G + (rng.random(len(g)) * span).astype(np.int64)
-    n, ho = np.divmod(row, Ho)
-    co = rng.integers(0, shape.C_out, len(g))
+    wo = k * G + (rng.random(len(t)) * span).astype(np.int64)
+    co = rng.integers(0, shape.C_out, len(t))
     return np.stack([n, co, ho, wo], axis=1)
 
 
