@@ -780,8 +780,11 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         g.n_tiles = 1;
         g.bres = 1;
         g.a_stage_bytes = f.R * kFoldRowBytes;
-        for (int st = 8; st >= 2 && !g.stages; --st)
-            if (fold_smem_bytes(f.b_bytes, st, g.a_stage_bytes) <= smem_limit()) g.stages = st;
+        // one stage per accumulator slot (four of 128 columns, two of 256): a
+        // tile's one commit frees both
+        const int st = g.bn == 128 ? 4 : 2;
+        g.stages = fold_smem_bytes(f.b_bytes, st, g.a_stage_bytes) <= smem_limit() ? st : 0;
+        g.min_stages = st;
         return g;
     }
     if (path == CONVGB_PATH_STEMWIN) {

@@ -1478,7 +1478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
                 const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 const uint32_t acc = ar.stage;
-                if (!receive()) break;  // accumulator drained by the epilogue
+                // accumulator drained by the epilogue (the folded window: handed over
+                // together with its one stage below)
+                if (!FOLD && !receive()) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 // window mode: (kh, cc) of the K block, walked instead of divided
@@ -1574,7 +1576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     mma_issue<PAIR>(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
                                                   (kb != u.kb0 || kk != 0) ? 1u : 0u);
                         }
-                        mma_commit_to<PAIR>(&empty[ring.stage]);
+                        // (the folded window's stages are its accumulators' slots: the
+                        // commit to tfull below frees the stage as well)
+                        if (!FOLD) mma_commit_to<PAIR>(&empty[ring.stage]);
                     }
                     __syncwarp();
                     if (WINDOW && ++win_cc == p.win_cc) {
@@ -1616,9 +1620,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
                 const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
-                if (!send(waited(&tempty[ar.stage], ar.phase ^ 1u, PAIR))) break;
+                // (the folded window: one hand-off per tile, the accumulator and the
+                // stage together)
+                if (!FOLD && !send(waited(&tempty[ar.stage], ar.phase ^ 1u, PAIR))) break;
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
                     bool good = !GATHER || waited(&full_a[ring.stage], ring.phase, false);
+                    if (FOLD) good = waited(&tempty[ar.stage], ar.phase ^ 1u, false);
                     if (good && (!GATHER || !p.bres))
                         good = waited(&full_b[ring.stage], ring.phase, false);
                     if (!send(good)) {
@@ -1814,7 +1821,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int tile = t_first; ok && tile < total_tiles; tile += t_step) {
                     const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                     for (int kb = u.kb0; kb < u.kb1; ++kb, ++issued, ring.next(S)) {
-                        if (!wait_bar(&empty[ring.stage], ring.phase ^ 1u, wc, kRoleTma)) {
+                        // (the folded window: stage s is accumulator slot s, free once
+                        // the tile that last used it has completed its MMAs)
+                        if (!wait_bar(FOLD ? &tfull[ring.stage] : &empty[ring.stage], ring.phase ^ 1u,
+                                      wc, kRoleTma)) {
                             ok = false;
                             break;
                         }
@@ -2005,6 +2015,7 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
                         kFoldRows + (p.x_KH - 1) * p.win_d <= 256 && p.num_kb == 1 &&
                         p.fold_bbytes >= p.x_KH * p.fold_n * 64 && p.fold_bbytes % 1024 == 0 &&
                         p.bres == 1 && p.n_tiles == 1 && p.splits == 1 && !p.sk && !p.tma_store &&
+                        p.stages == Cfg<BN>::kAcc &&
                         p.fold_hout >= 1 && p.m_tiles >= 1 && p.m_step == 1;
         if (!ok) return cudaErrorInvalidValue;
     }
