@@ -477,7 +477,7 @@ int choose_splits(long long tiles, int num_kb, long long partial_bytes, long lon
 // aligned, no split) and the ring still has two stages with its staging tile.
 void plan_epilogue(GemmPlan& g, const ConvShape& c, int y_f32)
 {
-    if (g.amode == kAWinFold) return;  // stores straight from the shuffle sums
+    if (is_fold(g.amode)) return;  // stores straight from the shuffle sums
     if (y_f32 || c.C_out % 8 != 0 || g.splits != 1 || g.sk || g.bn < 64 || g.stages < 2) return;
     const int kb_res = g.bres ? (int)((g.K + 63) / 64) : g.num_kb;
     const int bnb = g.pair ? g.bn / 2 : g.bn;
@@ -769,7 +769,7 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         // One A stage per tile: the R staged input rows of its segment.
         // Accumulator slots of 128 columns (256 when the MMA is wider).
         const FoldGeom f = fold_geom(c);
-        g.amode = kAWinFold;
+        g.amode = (c.KW <= kFold3MaxK && c.KH <= kFold3MaxK) ? kAWinFold3 : kAWinFold;
         if (!f.ok) return g;  // stages == 0: not applicable
         g.M = c.M;
         g.K = (long long)c.KH * 32;
@@ -1006,10 +1006,10 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
     out->plan = g;
     // (the staged-window stem packs its weights in the kernel: no weight map;
     // the folded window reads them through its own 4-D map)
-    if (!is_stemwin(g.amode) && g.amode != kAWinFold &&
+    if (!is_stemwin(g.amode) && !is_fold(g.amode) &&
         !encode_kmajor(&out->tb, a.w, a.C_out, g.K, g.pair ? g.bn / 2 : g.bn))
         return CONVGB_ERR_CUDA;
-    if (g.amode == kAWinFold &&
+    if (is_fold(g.amode) &&
         (!encode_fold_x(&out->ta, a.x, *a.shape, fold_geom(*a.shape).R) ||
          !encode_fold_w(&out->tb, a.w, *a.shape)))
         return CONVGB_ERR_CUDA;
@@ -1139,7 +1139,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.ho_div = FastDiv((uint32_t)c.H_out);
         p.st_s = c.s;
     }
-    if (g.amode == kAWinFold) {
+    if (is_fold(g.amode)) {
         const ConvShape& c = *a.shape;
         const FoldGeom f = fold_geom(c);
         p.win_wout = c.W_out;
@@ -1591,7 +1591,7 @@ convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_ou
     out->a_mode = g.amode;
     out->bn = g.bn;
     out->m_tiles = g.m_tiles;
-    out->tile_rows = (plane || g.amode == kAWinFold) ? 0 : rowtiles ? g.m_step * c.W_out : 128;
+    out->tile_rows = (plane || is_fold(g.amode)) ? 0 : rowtiles ? g.m_step * c.W_out : 128;
     out->n_tiles = g.n_tiles;
     out->splits = g.splits;
     out->k_blocks = g.num_kb;
@@ -1602,7 +1602,7 @@ convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_ou
     out->epilogue_tiles = g.tma_store ? g.epi_bufs : 0;
     out->epilogue_c32 = g.epi_c32;
     out->stream_k = g.sk;
-    out->segment_outputs = g.amode == kAWinFold ? fold_geom(c).G : 0;
+    out->segment_outputs = is_fold(g.amode) ? fold_geom(c).G : 0;
     return CONVGB_OK;
 }
 

@@ -424,7 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool PLANE = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     constexpr bool IM2WIN = AMODE == kAIm2win;
     constexpr bool STRIDED = AMODE == kAStrided;
-    constexpr bool FOLD = AMODE == kAWinFold;
+    constexpr bool FOLD = is_fold(AMODE);
+    // its tap loops' length (the kernel's code size matters: see kAWinFold3)
+    constexpr int FKW = AMODE == kAWinFold3 ? kFold3MaxK : kFoldMaxKW;
+    constexpr int FKH = AMODE == kAWinFold3 ? kFold3MaxK : kFoldMaxKH;
     constexpr bool ROWTILES = WINDOW || STAGEDROWS || IM2WIN || STRIDED;  // whole output rows
     // Modes whose gather warps have nothing to gather run the epilogue on eight
     // warps: each thread converts 32 of a 64-column chunk's columns instead of
@@ -658,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int col0 = wo - p.win_pad;  // column of tap 0
                 uint32_t taps = 0;                // taps whose column lies in the image
 #pragma unroll
-                for (int kw = 0; kw < kFoldMaxKW; ++kw) {
+                for (int kw = 0; kw < FKW; ++kw) {
                     const int col = col0 + kw * p.win_d;
                     if (kw < p.win_kw && col >= 0 && col < p.x_W) taps |= 1u << kw;
                 }
@@ -672,9 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int c16 = 0; c16 < cw; c16 += 16) {
                     const int co0 = c16;
-                    uint32_t v[kFoldMaxKW][16];
+                    uint32_t v[FKW][16];
 #pragma unroll
-                    for (int kw = 0; kw < kFoldMaxKW; ++kw)
+                    for (int kw = 0; kw < FKW; ++kw)
                         if (kw < p.win_kw)
                             ptx::tmem_ld_32x32b_x16(tb + static_cast<uint32_t>(kw * p.C_out + co0),
                                                     v[kw]);
@@ -686,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(v[0][i]);
 #pragma unroll
-                        for (int kw = 1; kw < kFoldMaxKW; ++kw)
+                        for (int kw = 1; kw < FKW; ++kw)
                             if (kw < p.win_kw) {
                                 const int sh = kw * p.win_d;
 #pragma unroll
@@ -697,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) o[i] = 0.f;
 #pragma unroll
-                        for (int kw = 0; kw < kFoldMaxKW; ++kw)
+                        for (int kw = 0; kw < FKW; ++kw)
                             if (kw < p.win_kw) {
                                 // source row, kept in the warp for taps that are left out
                                 const int src = (col0 + kw * p.win_d - c0) & 31;
@@ -1555,7 +1558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 static_cast<uint32_t>(p.win_d * kFoldRowBytes) >> 4;
                             const uint32_t b_kh_step = static_cast<uint32_t>(p.fold_n * 64) >> 4;
 #pragma unroll
-                            for (int kh = 0; kh < kFoldMaxKH; ++kh)
+                            for (int kh = 0; kh < FKH; ++kh)
                                 if (kh < p.x_KH) {
 #pragma unroll
                                     for (int kk = 0; kk < 2; ++kk)
@@ -1967,7 +1970,9 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
                                    : 0);
     constexpr bool kPlane = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
     constexpr bool kPairMode = AMODE == kAWindowPair || AMODE == kATmaGatherPair;
-    constexpr bool kFold = AMODE == kAWinFold;
+    constexpr bool kFold = is_fold(AMODE);
+    constexpr int kFKW = AMODE == kAWinFold3 ? kFold3MaxK : kFoldMaxKW;
+    constexpr int kFKH = AMODE == kAWinFold3 ? kFold3MaxK : kFoldMaxKH;
     const int smem =
         kPlane ? plane_smem_bytes(BN, p.stages, p.a_stage_bytes, p.bres ? p.kb_total : p.b_stages,
                                   extra)
@@ -2008,8 +2013,8 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         const bool ok = (BN == 128 || BN == 256) && p.C_in == 32 && p.C_out % 32 == 0 &&
                         p.C_out * 4 <= kFoldBiasBytes &&
                         p.fold_n == p.win_kw * p.C_out && p.fold_n % 16 == 0 && p.fold_n >= 16 &&
-                        p.fold_n <= BN && p.win_kw >= 1 && p.win_kw <= kFoldMaxKW &&
-                        p.x_KH >= 1 && p.x_KH <= kFoldMaxKH && p.win_d >= 1 && p.x_W >= 32 &&
+                        p.fold_n <= BN && p.win_kw >= 1 && p.win_kw <= kFKW &&
+                        p.x_KH >= 1 && p.x_KH <= kFKH && p.win_d >= 1 && p.x_W >= 32 &&
                         p.fold_g == 32 - (p.win_kw - 1) * p.win_d && p.fold_g >= 1 &&
                         p.a_stage_bytes == (kFoldRows + (p.x_KH - 1) * p.win_d) * kFoldRowBytes &&
                         kFoldRows + (p.x_KH - 1) * p.win_d <= 256 && p.num_kb == 1 &&
@@ -2173,6 +2178,10 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kAWinFold:
         return bn == 128   ? launch_bn<128, kAWinFold>(ta, tb, ty, p, st)
                : bn == 256 ? launch_bn<256, kAWinFold>(ta, tb, ty, p, st)
+                           : cudaErrorInvalidValue;
+    case kAWinFold3:
+        return bn == 128   ? launch_bn<128, kAWinFold3>(ta, tb, ty, p, st)
+               : bn == 256 ? launch_bn<256, kAWinFold3>(ta, tb, ty, p, st)
                            : cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
     }

@@ -139,7 +139,9 @@ def test_path_selection(lib, cfg, path):
 def test_winfold_selection_and_plan(lib):
     # 32 -> 32 3x3 at 150x150: segments of 30 output pixels, five per output row
     pl = lib.plan_info(128, 32, 150, 150, 32, 3, 3, 1, 1, 1)
-    assert (pl["path"], pl["a_mode"], pl["segment_outputs"], pl["tile_rows"]) == (8, 16, 30, 0)
+    assert (pl["path"], pl["a_mode"], pl["segment_outputs"], pl["tile_rows"]) == (8, 17, 30, 0)
+    # 5x5: the instantiation with tap loops for up to 7 x 5
+    assert lib.plan_info(128, 32, 150, 150, 32, 5, 5, 1, 2, 1)["a_mode"] == 16
     assert pl["m_tiles"] == 128 * 38 * 5 and pl["k_blocks"] == 1  # 4-row blocks x segments
     assert pl["weights_resident"] == 1 and pl["splits"] == 1 and pl["tma_store"] == 0
     assert lib.workspace_size(128, 32, 150, 150, 32, 3, 3, 1, 1, 1) == 0
