@@ -565,6 +565,10 @@ GemmPlan plan_gemm(int path, const ConvShape& c, int y_f32)
     if (path != CONVGB_PATH_PLANE) plan_stream_k(g, c);
     if (path != CONVGB_PATH_PLANE) plan_epilogue(g, c, y_f32);
     cap_stages(g);
+    // the window mode's common plan runs on the kernel built for it
+    if (g.amode == kAWindow && g.bres && g.tma_store && !g.epi_c32 && g.splits == 1 && !g.sk &&
+        c.KW == 3 && g.n_tiles == 1)
+        g.amode = kAWindowT;
     return g;
 }
 
@@ -1027,7 +1031,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         !encode_kmajor(&out->ta, a.x, a.x_rows, a.C_in, 1))
         return CONVGB_ERR_CUDA;
     const bool plane = g.amode == kAPlane || g.amode == kAPlane3 || g.amode == kAPlane3U2;
-    const bool window = g.amode == kAWindow || g.amode == kAWindowPair;
+    const bool window = is_window(g.amode);
     if (window || plane) {
         const ConvShape& c = *a.shape;
         if (!encode_window(&out->ta, a.x, c.N, c.H, c.W, c.C_in, g.win_wv)) return CONVGB_ERR_CUDA;
@@ -1584,7 +1588,7 @@ convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_ou
     if (!path_supports(path, c)) return CONVGB_ERR_UNSUPPORTED;
     const GemmPlan g = plan_gemm(path, c, y_dtype == CONVGB_F32 ? 1 : 0);
     const bool plane = g.amode == kAPlane || g.amode == kAPlane3 || g.amode == kAPlane3U2;
-    const bool rowtiles = g.amode == kAWindow || g.amode == kAWindowPair ||
+    const bool rowtiles = is_window(g.amode) ||
                           g.amode == kANarrowWin || g.amode == kAIm2win || g.amode == kAStrided ||
                           is_stemwin(g.amode);
     out->path = path;

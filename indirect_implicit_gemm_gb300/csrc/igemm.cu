@@ -418,7 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool GATHER =
         AMODE == kAGather || AMODE == kANarrow || TMAGATHER || NARROWWIN || STEMWIN;
     constexpr bool PAIR = AMODE == kAWindowPair || AMODE == kATmaGatherPair;  // CTA pair
-    constexpr bool WINDOW = AMODE == kAWindow || AMODE == kAWindowPair;
+    constexpr bool WINDOW = is_window(AMODE);
+    // the window mode's common plan, fixed at compile time (kAWindowT); other
+    // modes read it from the parameters
+    constexpr bool WT = AMODE == kAWindowT;
+    const int tma_store = WT ? 1 : p.tma_store;
+    const int epi_c32 = WT ? 0 : p.epi_c32;
+    const bool split_k = !WT && p.splits > 1;
+    const bool kw3 = WT || p.win_kw == 3;
+    const int bres = WT ? 1 : p.bres;
     // B block bytes in this CTA's shared memory (a pair splits B's columns)
     constexpr uint32_t BB = PAIR ? C::kBBytes / 2 : C::kBBytes;
     constexpr bool PLANE = AMODE == kAPlane || AMODE == kAPlane3 || AMODE == kAPlane3U2;
@@ -457,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* data = smem_raw + kHeaderBytes + ((1024u - (base & 1023u)) & 1023u);
     uint8_t* sB = data;
     const uint32_t SB = PLANE ? static_cast<uint32_t>(p.b_stages) : 1u;  // plane: B ring slots
-    const uint32_t b_blocks = p.bres ? static_cast<uint32_t>(p.kb_total)
+    const uint32_t b_blocks = bres ? static_cast<uint32_t>(p.kb_total)
                               : PLANE ? SB
                                       : S * static_cast<uint32_t>(p.b_per_stage);
     // Accumulators: plane mode keeps pl_u sub-tiles of BN columns per tile.
@@ -471,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA-store epilogue: a 128 x 64 bf16 staging tile (128-byte swizzle) and the
     // current column tile's bias in fp32.
     uint8_t* sEpi = sStg + (STAGEDROWS ? NS * p.nw_slot_bytes : 0);
-    const int epi_tile = p.epi_c32 ? kEpiNarrowTileBytes : kEpiTileBytes;  // staging tile bytes
+    const int epi_tile = epi_c32 ? kEpiNarrowTileBytes : kEpiTileBytes;  // staging tile bytes
     float* sBias = reinterpret_cast<float*>(sEpi + p.epi_bufs * epi_tile);
     // folded window: the bias as fp32 right after the A stages (1 KB)
     float* sBiasF = reinterpret_cast<float*>(sA + S * AST);
@@ -492,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // walked as segments 0, 1, ... of the units it touches; partial sums meet
     // in the fp32 buffer.
     const int cta_idx = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    constexpr bool SKM = WINDOW;  // stream-K is built into the window kernels only
+    constexpr bool SKM = WINDOW && !WT;  // stream-K is built into the window kernels only
     SkRange skr;
     if (SKM && p.sk) {
         const long long G = p.sk_ctas, W = p.sk_iters;
@@ -632,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds,
             // and with the TMA store all four warps do (they share named barriers).
             bool ready = __all_sync(0xffffffffu, wait_bar(&tfull[acc], ar.phase, wc, kRoleEpilogue));
-            if (p.tma_store) {
+            if (tma_store) {
                 if (lane == 0) sVote[warp] = ready ? 1u : 0u;
                 ptx::named_barrier_sync(1, kEpiN);
                 ready = sVote[0] && sVote[1] && sVote[2] && sVote[3] &&
@@ -746,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
-            if (p.tma_store && u.n0 != bias_n0) {  // new column tile: stage its bias
+            if (tma_store && u.n0 != bias_n0) {  // new column tile: stage its bias
                 ptx::named_barrier_sync(1, kEpiN);
                 for (int i = et; i < BN; i += kEpiN)
                     sBias[i] = (p.bias != nullptr && u.n0 + i < p.C_out)
@@ -779,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t taddr = tbase + static_cast<uint32_t>(sub * BN);
                 const bool live = m < p.M;
-                if (EPI8 && p.tma_store && p.epi_c32) {
+                if (EPI8 && tma_store && epi_c32) {
                     // Narrow staging: 32-column chunks in a 128 x 64-byte tile, 64-byte
                     // swizzle (16-byte piece q of staged row s sits at q ^ ((s >> 1) & 3));
                     // warp w converts the 16-column half w / 4 of each chunk.
@@ -835,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     continue;
                 }
-                if (p.tma_store) {
+                if (tma_store) {
 #pragma unroll 1
                     for (int c64 = 0; c64 < BN / 64; ++c64) {
                         uint32_t ra[32], rb[32];
@@ -932,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         const int co0 = u.n0 + ch * 32;
                         if (live && co0 < p.C_out) {
-                            if (p.splits > 1 || p.sk)
+                            if (split_k || p.sk)
                                 reduce_chunk(p, m, co0, ra);
                             else
                                 store_chunk(p, m, co0, ra);
@@ -949,13 +957,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (last_sub && ch + 2 >= BN / 32) release_acc(acc);
                         const int co0 = u.n0 + ch * 32;
                         if (live && co0 < p.C_out) {
-                            if (p.splits > 1 || p.sk)
+                            if (split_k || p.sk)
                                 reduce_chunk(p, m, co0, ra);
                             else
                                 store_chunk(p, m, co0, ra);
                         }
                         if (live && ch + 1 < BN / 32 && co0 + 32 < p.C_out) {
-                            if (p.splits > 1 || p.sk)
+                            if (split_k || p.sk)
                                 reduce_chunk(p, m, co0 + 32, rb);
                             else
                                 store_chunk(p, m, co0 + 32, rb);
@@ -966,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (et == 0) *sTilesDone = lt + 1;
         }
         // Every TMA store has finished before the CTA exits.
-        if (p.tma_store && et == 0) ptx::bulk_wait_all();
+        if (tma_store && et == 0) ptx::bulk_wait_all();
     } else if (warp < kEpiWarps + kGatherWarps) {
         // ------------------------------------------------------------ A gather
         if (PLANE && warp == kEpiWarps) {
@@ -1364,7 +1372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             Ring ra, rb;
             uint32_t lt = 0;
-            bool ok = !p.bres || wait_bar(bres_full, 0u, wc, kRoleMma);
+            bool ok = !bres || wait_bar(bres_full, 0u, wc, kRoleMma);
             const int taps = p.x_KH * p.win_kw;
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles;
@@ -1387,7 +1395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int t = 0; t < CT; ++t) {
                             uint64_t bd = bres_d + boff[t];
-                            if (!p.bres) {
+                            if (!bres) {
                                 if (!wait_bar(&full_b[rb.stage], rb.phase, wc, kRoleMma)) {
                                     ok = false;
                                     break;
@@ -1403,7 +1411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   ad + aoff[t] + sub * sub_step + 2 * kk,
                                                   bd + 2 * kk, idesc,
                                                   (t != 0 || kk != 0) ? 1u : first);
-                            if (!p.bres) {
+                            if (!bres) {
                                 ptx::mma_commit(&empty_b[rb.stage]);
                                 rb.next(SB);
                             }
@@ -1423,7 +1431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      static_cast<uint32_t>(kw) * col_step;
                             b_next += static_cast<uint64_t>(static_cast<uint32_t>(p.win_cc) *
                                                             b_blk_step);
-                            if (!p.bres) {
+                            if (!bres) {
                                 if (!wait_bar(&full_b[rb.stage], rb.phase, wc, kRoleMma)) {
                                     ok = false;
                                     break;
@@ -1438,7 +1446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   ad + a_cur + sub * sub_step + 2 * kk,
                                                   bd + 2 * kk, idesc,
                                                   (t != 0 || kk != 0) ? 1u : first);
-                            if (!p.bres) {
+                            if (!bres) {
                                 ptx::mma_commit(&empty_b[rb.stage]);
                                 rb.next(SB);
                             }
@@ -1510,13 +1518,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // One staged (kh, cc) block feeds every kw tap: tap kw reads
                             // the staging rows shifted down by kw*d.
                             const uint64_t bd0 =
-                                p.bres ? b_desc0 + static_cast<uint32_t>(win_kh * p.win_kw * p.win_cc +
+                                bres ? b_desc0 + static_cast<uint32_t>(win_kh * p.win_kw * p.win_cc +
                                                                          win_cc) *
                                                        b_blk_step
                                        : b_desc0 + ring.stage * p.b_per_stage * b_blk_step;
-                            const uint32_t bstep = p.bres ? p.win_cc * b_blk_step : b_blk_step;
+                            const uint32_t bstep = bres ? p.win_cc * b_blk_step : b_blk_step;
                             const uint32_t first = kb != u.kb0 ? 1u : 0u;
-                            if (p.win_kw == 3) {
+                            if (kw3) {
 #pragma unroll
                                 for (int kw = 0; kw < 3; ++kw)
 #pragma unroll
@@ -1569,7 +1577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                         } else {
                             const uint64_t bd =
-                                b_desc0 + (p.bres ? static_cast<uint32_t>(kb) : ring.stage) * b_blk_step;
+                                b_desc0 + (bres ? static_cast<uint32_t>(kb) : ring.stage) * b_blk_step;
                             // The last K block may hold fewer than 64 columns: skip the
                             // all-zero 16-column steps.
                             const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
@@ -1619,7 +1627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             Ring ring;
             // (the staged-window stem's weights are ready once packed: wpack)
-            bool ok = send(!p.bres || waited(STEMWIN ? wpack : bres_full, 0u, false));
+            bool ok = send(!bres || waited(STEMWIN ? wpack : bres_full, 0u, false));
             Ring ar;
             for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
                 const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
@@ -1629,7 +1637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
                     bool good = !GATHER || waited(&full_a[ring.stage], ring.phase, false);
                     if (FOLD) good = waited(&tempty[ar.stage], ar.phase ^ 1u, false);
-                    if (good && (!GATHER || !p.bres))
+                    if (good && (!GATHER || !bres))
                         good = waited(&full_b[ring.stage], ring.phase, false);
                     if (!send(good)) {
                         ok = false;
@@ -1654,7 +1662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kw = 0; kw < p.win_kw; ++kw)
                         ptx::tma_load_4d(sB + (kh * p.fold_n + kw * p.C_out) * 64, &tmap_b, bres_full,
                                          0, kw, kh, 0);
-            } else if (p.bres) {
+            } else if (bres) {
                 // Weights resident: every K block of the one column tile, once (in
                 // a pair each CTA holds half of the columns; CTA 0's barrier counts
                 // both halves).
@@ -1721,7 +1729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (PLANE) {
                 // Streamed weights: block (tap, cc) of the tile's column tile per
                 // B slot, in the order the MMA thread consumes them.
-                if (!p.bres) {
+                if (!bres) {
                     const int taps = p.x_KH * p.win_kw;
                     Ring rb;
                     uint32_t issued = 0;
@@ -1776,7 +1784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (rank == 0) {
                             const uint32_t tx =
                                 static_cast<uint32_t>(rows + rows_peer) * row_bytes +
-                                (p.bres ? 0u
+                                (bres ? 0u
                                         : static_cast<uint32_t>(p.win_kw) * BB * (PAIR ? 2u : 1u));
                             ptx::mbar_arrive_expect_tx(&full_b[ring.stage], tx);
                         }
@@ -1793,7 +1801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  &full_b[ring.stage], cc * BK, -p.win_pad, h,
                                                  static_cast<int>(n));
                         }
-                        if (!p.bres)
+                        if (!bres)
                             for (int kw = 0; kw < p.win_kw; ++kw) {
                                 uint8_t* dst = sB + (ring.stage * p.b_per_stage + kw) * BB;
                                 const int col = ((kh * p.win_kw + kw) * p.win_cc + cc) * BK;
@@ -1809,7 +1817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (rank == 0)
                     for (uint32_t i = first; i < issued; ++i)
                         drain_wait(&full_b[i % S], (i / S) & 1u, 1000000000ull);
-            } else if (!p.bres || !GATHER) {
+            } else if (!bres || !GATHER) {
                 // im2win, strided 1x1: a box of win_rows output rows x W_out pixels
                 // x 64 K
                 const uint32_t a_tx =
@@ -1817,7 +1825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     : (IM2WIN || STRIDED) ? static_cast<uint32_t>(p.win_rows * p.win_wout) * 128u
                     : FOLD                ? AST
                                           : static_cast<uint32_t>(kABytes);
-                const uint32_t kTx = (p.bres ? 0u : static_cast<uint32_t>(BB)) + a_tx;
+                const uint32_t kTx = (bres ? 0u : static_cast<uint32_t>(BB)) + a_tx;
                 Ring ring;
                 uint32_t issued = 0;
                 bool ok = true;
@@ -1860,7 +1868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else if (!GATHER)
                             ptx::tma_load_2d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
                                              kb * BK, u.m0);
-                        if (!p.bres) {
+                        if (!bres) {
                             if (PAIR)  // this CTA's half of the column tile
                                 ptx::tma_load_2d_pair(
                                     sB + ring.stage * BB, &tmap_b,
@@ -1883,7 +1891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // The resident weights must have landed before the CTA exits (a pair's
     // land on CTA 0's barrier, for both CTAs).
-    if (warp == kTmaWarp && lane == 0 && p.bres && rank == 0)
+    if (warp == kTmaWarp && lane == 0 && bres && rank == 0)
         drain_wait(bres_full, 0u, 1000000000ull);
     ptx::tc_fence_before();
     // a pair's CTA 0 reads the peer's shared memory and writes its TMEM: neither
@@ -1985,8 +1993,8 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
     if ((AMODE == kATmaGather || AMODE == kATmaGatherPair) && p.stages < kMinGatherTurnStages)
         return cudaErrorInvalidValue;
     // 32-column staging exists for the eight-warp epilogue only
-    constexpr bool kEpi8 = AMODE == kAWindow || AMODE == kAWindowPair || AMODE == kADense ||
-                           AMODE == kAIm2win || AMODE == kAStrided;
+    constexpr bool kEpi8 = is_window(AMODE) || AMODE == kADense || AMODE == kAIm2win ||
+                           AMODE == kAStrided;
     if (p.epi_c32 && !(kEpi8 && p.tma_store)) return cudaErrorInvalidValue;
     if ((AMODE == kANarrowWin || is_stemwin(AMODE)) && (p.nw_slots < 1 || p.nw_slots > kMaxSlots))
         return cudaErrorInvalidValue;
@@ -2005,6 +2013,10 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
             p.sw_steps != (p.sw_nkb - 1) * 4 + p.sw_last || p.sw_steps > kStemWinMaxSteps)
             return cudaErrorInvalidValue;
     }
+    if (AMODE == kAWindowT &&
+        (p.bres != 1 || p.tma_store != 1 || p.epi_c32 != 0 || p.splits != 1 || p.sk ||
+         p.win_kw != 3 || p.n_tiles != 1))
+        return cudaErrorInvalidValue;  // the plan the kernel is built for
     if (kFold) {
         // the folded window's shared-memory layout, its unrolled loops and its
         // epilogue's register arrays: 32 channels per 64-byte row, KW*C_out MMA
@@ -2164,6 +2176,7 @@ cudaError_t launch_igemm(int amode, int bn, const CUtensorMap& ta, const CUtenso
     case kATmaGather: return launch_mode<kATmaGather>(bn, ta, tb, ty, p, st);
     case kAWindow: return launch_mode<kAWindow>(bn, ta, tb, ty, p, st);
     case kAWindowPair: return launch_mode<kAWindowPair>(bn, ta, tb, ty, p, st);
+    case kAWindowT: return launch_mode<kAWindowT>(bn, ta, tb, ty, p, st);
     case kAIm2win: return launch_mode<kAIm2win>(bn, ta, tb, ty, p, st);
     case kAStrided: return launch_mode<kAStrided>(bn, ta, tb, ty, p, st);
     case kATmaGatherPair: return launch_mode<kATmaGatherPair>(bn, ta, tb, ty, p, st);

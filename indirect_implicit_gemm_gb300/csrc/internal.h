@@ -181,7 +181,15 @@ enum AMode : int {
     kAWinFold3 = 17,  // the folded window for kernels of at most 3 x 3: the same kernel with
                       // its tap loops unrolled to 3 (measured on the 32-channel 3x3 layer at
                       // 150x150: 111.7 us against 126.4 us with loops sized for 7 x 5)
+    kAWindowT = 18,   // the window mode's common plan fixed at compile time: KW = 3, resident
+                      // weights, TMA-store epilogue in 64-column chunks, no split, no stream-K
+                      // (the kernel is smaller: 64-channel 3x3 layer at 112x112 158.9 ->
+                      // 145.3 us, 64->128 at 56x56 17.4 -> 16.9 us, in a timing copy)
 };
+constexpr bool is_window(int amode)
+{
+    return amode == kAWindow || amode == kAWindowPair || amode == kAWindowT;
+}
 constexpr bool is_fold(int amode) { return amode == kAWinFold || amode == kAWinFold3; }
 // The folded window's limits: kernel width (registers of the epilogue's shuffle
 // sum), kernel height (the unrolled MMA sequence), for kAWinFold and for

@@ -296,7 +296,10 @@ MULTI_TILE = [
        stride=2, pad=1, seed=72), 0, 12),
     (S("multi_window_pair_1x3", N=456, C_in=64, H=14, W=14, C_out=256, KH=1, KW=3, seed=73),
      0, 9),
-    (S("multi_window_c64_1x3", N=456, C_in=64, H=14, W=14, C_out=64, KH=1, KW=3, seed=74), 0, 4),
+    # (the window kernel built for the common plan: KW = 3, resident weights, TMA store)
+    (S("multi_window_c64_1x3", N=456, C_in=64, H=14, W=14, C_out=64, KH=1, KW=3, seed=74), 0, 18),
+    (S("multi_window_c64_1x5", N=456, C_in=64, H=14, W=14, C_out=64, KH=1, KW=5, pad=2, seed=86),
+     0, 4),
     (S("multi_strided_1x1_s2", N=456, C_in=64, H=32, W=32, C_out=64, KH=1, KW=1, stride=2,
        pad=0, seed=75), 0, 11),
     (S("multi_dense_1x1", N=456, C_in=64, H=16, W=16, C_out=64, KH=1, KW=1, pad=0, seed=76),
