@@ -10,7 +10,7 @@ Functions and the passages they follow
 --------------------------------------
 ``output_size``
     Output extent along one axis, floor((L + 2p - d(K-1) - 1)/s) + 1.
-    "Unifying Convolutions and GEMM", section 5 prints (H + 2p - K)//s + 1;
+    "Unifying Convolutions and GEMM", section 5 gives the undilated extent;
     the dilated form reduces to it at d = 1.
 ``conv2d_direct`` / ``conv2d_points``
     The naive 7-loop convolution ("Unifying Convolutions and GEMM",

@@ -21,8 +21,8 @@
  * The loops run in the page's printed order (n, co, ho, wo, ci, kh, kw);
  * the section-1 listing omits padding, dilation, bias and the initialisation
  * of Y, and the readings used here are: Y starts at bias[co] (or 0 when no
- * bias is given, as section 5's "if bias is not None"), padding contributes
- * zeros (section 5 pads with F.unfold's zeros), and tap kh sits d*kh rows
+ * bias is given: section 5 makes the bias optional), padding contributes
+ * zeros (section 5 pads with zeros before unfolding), and tap kh sits d*kh rows
  * from the window origin (the usual meaning of dilation d; d = 1 gives the
  * listing's ho*stride+kh).
  *
@@ -56,7 +56,7 @@ static double bf16_to_double(uint16_t bits)
 }
 
 /* Output size along one spatial axis: floor((L + 2p - d(K-1) - 1)/s) + 1.
- * With d = 1 this is the tutorial's (L + 2p - K)//s + 1 (section 5). */
+ * With d = 1 this reduces to the undilated extent section 5 gives. */
 long oracle_output_size(long L, long K, long s, long p, long d)
 {
     long span = L + 2 * p - d * (K - 1) - 1;
