@@ -168,6 +168,26 @@ def set_tuning(bn: int = 0, max_stages: int = 0, stream_k: int = 0):
     """Force the tile width, cap the ring depth and/or allow stream-K in later plans
     (0 = the planner's own choice)."""
     load().convgb_set_tuning(int(bn), int(max_stages), int(stream_k))
+    _shape_cache.clear()  # workspace sizes follow the plan
+
+
+# (path, N, C_in, H, W, C_out, KH, KW, stride, pad, dilation) -> (H_out, W_out,
+# workspace bytes): the per-call queries of conv2d_fwd_path, made once per shape
+_shape_cache = {}
+
+
+def _shape_info(lib, key):
+    got = _shape_cache.get(key)
+    if got is None:
+        path, N, C_in, H, W, C_out, KH, KW, stride, pad, dilation = key
+        H_out, W_out = output_dims(H, W, KH, KW, stride, pad, dilation)
+        need = lib.convgb_conv2d_fwd_path_workspace_size(path, N, C_in, H, W, C_out, KH, KW,
+                                                         stride, pad, dilation)
+        got = (H_out, W_out, need)
+        if len(_shape_cache) > 4096:
+            _shape_cache.clear()
+        _shape_cache[key] = got
+    return got
 
 
 def output_dims(H, W, KH, KW, stride=1, pad=0, dilation=1):
@@ -213,7 +233,8 @@ def conv2d_fwd_path(path, x, w, bias=None, stride=1, pad=0, dilation=1,
         raise ValueError("x has %d channels, w expects %d" % (C_in, C_in2))
     if bias is not None and tuple(bias.shape) != (C_out,):
         raise ValueError("bias must have shape [C_out]")
-    H_out, W_out = output_dims(H, W, KH, KW, stride, pad, dilation)
+    H_out, W_out, need = _shape_info(lib, (path, N, C_in, H, W, C_out, KH, KW, stride, pad,
+                                           dilation))
     if out_dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("out_dtype must be bfloat16 or float32")
     if y is None:
@@ -223,8 +244,6 @@ def conv2d_fwd_path(path, x, w, bias=None, stride=1, pad=0, dilation=1,
         if tuple(y.shape) != (N, H_out, W_out, C_out):
             raise ValueError("y has shape %s, expected %s" % (tuple(y.shape),
                                                               (N, H_out, W_out, C_out)))
-    need = lib.convgb_conv2d_fwd_path_workspace_size(path, N, C_in, H, W, C_out, KH, KW,
-                                                     stride, pad, dilation)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
