@@ -281,6 +281,26 @@ def graph_time_ms(fn, steps, stream):
     return start.elapsed_time(end)
 
 
+def single_launch_us(layer, stream, reps=21):
+    """One conv2d_fwd on an idle GPU, issued eagerly through the binding (host
+    call included), bracketed by events: the latency a lone call sees, apart
+    from the graph-replayed throughput figure.  Median of `reps`."""
+    times = []
+    for i in range(reps):
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        layer.step(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+        times.append(start.elapsed_time(end) * 1e3)
+    times.sort()
+    return {"median_us": times[len(times) // 2], "min_us": times[0],
+            "note": "one eager conv2d_fwd through the Python binding on an idle GPU, "
+                    "events around it; the headline value is CUDA-graph replay"}
+
+
 def event_time_ms(fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -700,6 +720,7 @@ def main():
             roof["tensor_peak_at_clock_tflops"] = clk_peak
             roof["tensor_frac_at_clock"] = num["flops"] / (k_ms * 1e-3) / 1e12 / clk_peak
 
+    single = single_launch_us(layer, stream)
     e2e_ms, h2d, d2h = time_e2e(g, c, max(10, args.steps // 10), 3, dev, stream)
     link = time_link(h2d, d2h, max(10, args.steps // 10), dev)
     e2e = {"value": world * num["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -760,6 +781,7 @@ def main():
                    "frac_of_roofline": t_roof * 1e3 / ms_step},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": layer.launches_per_step() * args.steps,
+        "single_launch": single,
         "clocks": clocks, "sweep": sweep,
     }
     if rank == 0:
