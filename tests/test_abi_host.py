@@ -157,6 +157,48 @@ def test_winfold_selection_and_plan(lib):
         lib.plan_info(4, 32, 40, 40, 128, 3, 3, 1, 1, 1, path=lib.PATH_WINFOLD)
 
 
+FOLD_GEOMS = [  # (N, H, W, C_out, KH, KW, pad, dilation)
+    (1, 32, 32, 32, 3, 3, 1, 1), (3, 37, 45, 64, 3, 3, 1, 1), (2, 20, 70, 32, 5, 5, 2, 1),
+    (1, 16, 40, 32, 7, 5, 3, 1), (2, 12, 33, 32, 3, 3, 2, 2), (4, 9, 64, 96, 3, 1, 1, 1),
+    (2, 5, 64, 32, 1, 3, 1, 1), (1, 9, 40, 32, 3, 3, 5, 2), (8, 150, 150, 32, 3, 3, 1, 1),
+]
+
+
+@pytest.mark.parametrize("geom", FOLD_GEOMS, ids=str)
+def test_winfold_plan_geometry(lib, geom):
+    """The folded window's tiling, from the plan the library reports, against the
+    geometry stated in include/convgb.h: segments of G = 32 - (KW-1)d output
+    pixels, four output rows per tile, one tile per (image, row block,
+    segment); 128- or 256-column accumulators by the MMA width KW*C_out; no
+    workspace."""
+    N, H, W, C_out, KH, KW, p, d = geom
+    pl = lib.plan_info(N, 32, H, W, C_out, KH, KW, 1, p, d, path=lib.PATH_WINFOLD)
+    Ho = oracle.output_size(H, KH, 1, p, d)
+    Wo = oracle.output_size(W, KW, 1, p, d)
+    G = 32 - (KW - 1) * d
+    assert pl["segment_outputs"] == G and pl["tile_rows"] == 0
+    assert pl["m_tiles"] == N * -(-Ho // 4) * -(-Wo // G)
+    assert pl["n_tiles"] == 1 and pl["splits"] == 1 and pl["k_blocks"] == 1
+    assert pl["bn"] == (128 if KW * C_out <= 128 else 256)
+    assert pl["a_mode"] == (17 if KH <= 3 and KW <= 3 else 16)
+    # one stage per accumulator slot: four of 128 columns or two of 256
+    assert pl["stages"] == (4 if pl["bn"] == 128 else 2)
+    if lib.select_path(N, 32, H, W, C_out, KH, KW, 1, p, d) == lib.PATH_WINFOLD:
+        assert lib.workspace_size(N, 32, H, W, C_out, KH, KW, 1, p, d) == 0
+
+
+def test_winfold_rejects_shapes_outside_its_limits(lib):
+    for args in [(1, 32, 40, 40, 32, 3, 3, 2, 1, 1),    # stride 2
+                 (1, 16, 40, 40, 32, 3, 3, 1, 1, 1),    # 16 channels
+                 (1, 32, 31, 31, 32, 3, 3, 1, 1, 1),    # rows narrower than a segment
+                 (1, 32, 40, 40, 48, 3, 3, 1, 1, 1),    # C_out not a multiple of 32
+                 (1, 32, 40, 40, 64, 5, 5, 1, 2, 1),    # KW*C_out = 320 > 256
+                 (1, 32, 40, 40, 32, 3, 3, 1, 13, 13),  # G = 6 < 8
+                 (1, 32, 40, 40, 32, 9, 3, 1, 4, 1)]:   # KH = 9 > 7
+        with pytest.raises(lib.ConvgbError):
+            lib.plan_info(*args, path=lib.PATH_WINFOLD)
+
+
 def test_dense_path_needs_no_workspace(lib):
     assert lib.workspace_size(32, 256, 56, 56, 64, 1, 1, 1, 0, 1) == 0
     assert lib.workspace_size(32, 512, 7, 7, 2048, 1, 1, 1, 0, 1) == 0
