@@ -183,9 +183,13 @@ typedef struct convgb_plan {
     int segment_outputs;  /* CONVGB_PATH_WINFOLD: output pixels per segment, G (0 on other
                              paths).  Each output row is cut into spr = ceil(W_out / G)
                              segments of G pixels (the last one shorter) and the
-                             output rows of an image into HB = ceil(H_out / 4) blocks
-                             of four; tile t = (n*HB + hb)*spr + k holds segment k of
-                             rows 4*hb .. 4*hb + 3 of image n, so tile_rows is 0 */
+                             output rows of an image into HB = ceil(H_out / U) blocks
+                             of U = segment_rows; tile t = (n*HB + hb)*spr + k holds
+                             segment k of rows U*hb .. U*hb + U - 1 of image n, so
+                             tile_rows is 0 */
+    int segment_rows;     /* CONVGB_PATH_WINFOLD: output rows per tile, U (4, or 8 for
+                             kernels up to 3x3 whose MMA is at most 128 columns wide;
+                             0 on other paths) */
 } convgb_plan;
 
 /* Fills *plan with what conv2d_fwd_path(path, ...) would launch for this shape

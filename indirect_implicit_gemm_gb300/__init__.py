@@ -55,7 +55,7 @@ class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "path", "a_mode", "bn", "m_tiles", "tile_rows", "n_tiles", "splits", "k_blocks", "stages",
         "weights_resident", "cta_pair", "tma_store", "epilogue_tiles", "epilogue_c32",
-        "stream_k", "segment_outputs")]
+        "stream_k", "segment_outputs", "segment_rows")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -215,6 +215,8 @@ StemWinGeom stemwin_geom(const ConvShape& c)
 struct FoldGeom {
     bool ok = false;
     int G = 0, spr = 0, HB = 0, R = 0, n_mma = 0, b_bytes = 0;
+    int U = 0;  // output rows per work unit: 4, or 8 (two tiles) for 3x3-sized kernels
+                // whose MMA fits 128 columns
     long long tiles = 0;
 };
 FoldGeom fold_geom(const ConvShape& c)
@@ -224,14 +226,16 @@ FoldGeom fold_geom(const ConvShape& c)
     if (c.KW > kFoldMaxKW || c.KH > kFoldMaxKH) return f;
     // segments are 32 columns inside the row; a box spans R rows
     if (c.W < 32) return f;
-    f.R = kFoldRows + (c.KH - 1) * c.d;
+    const bool pair = c.KW <= kFold3MaxK && c.KH <= kFold3MaxK && c.KW * c.C_out <= 128;
+    f.U = pair ? 2 * kFoldRows : kFoldRows;
+    f.R = f.U + (c.KH - 1) * c.d;
     if (f.R > 256) return f;
     f.G = 32 - (c.KW - 1) * c.d;
     if (f.G < 8) return f;
     f.n_mma = c.KW * c.C_out;
     if (f.n_mma > 256 || f.n_mma % 16 != 0) return f;
     f.spr = (c.W_out + f.G - 1) / f.G;
-    f.HB = (c.H_out + kFoldRows - 1) / kFoldRows;
+    f.HB = (c.H_out + f.U - 1) / f.U;
     f.tiles = (long long)c.N * f.HB * f.spr;
     if (f.tiles >= (1LL << 31)) return f;
     f.b_bytes = (c.KH * f.n_mma * 64 + 1023) / 1024 * 1024;
@@ -784,9 +788,9 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         g.n_tiles = 1;
         g.bres = 1;
         g.a_stage_bytes = f.R * kFoldRowBytes;
-        // one stage per accumulator slot (four of 128 columns, two of 256): a
-        // tile's one commit frees both
-        const int st = g.bn == 128 ? 4 : 2;
+        // one stage per accumulator slot (four of 128 columns, two of 256; two
+        // pairs of 128 for units of two tiles): a unit's one commit frees both
+        const int st = f.U == 2 * kFoldRows ? 2 : g.bn == 128 ? 4 : 2;
         g.stages = fold_smem_bytes(f.b_bytes, st, g.a_stage_bytes) <= smem_limit() ? st : 0;
         g.min_stages = st;
         return g;
@@ -1607,6 +1611,7 @@ convgb_status convgb_plan_info(int path, int N, int C_in, int H, int W, int C_ou
     out->epilogue_c32 = g.epi_c32;
     out->stream_k = g.sk;
     out->segment_outputs = is_fold(g.amode) ? fold_geom(c).G : 0;
+    out->segment_rows = is_fold(g.amode) ? fold_geom(c).U : 0;
     return CONVGB_OK;
 }
 

@@ -433,6 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool IM2WIN = AMODE == kAIm2win;
     constexpr bool STRIDED = AMODE == kAStrided;
     constexpr bool FOLD = is_fold(AMODE);
+    // the 3x3-sized folded window with 128-column accumulators works in units of
+    // two tiles: eight output rows, one box, one hand-off and one commit, the two
+    // 4-row halves in a pair of accumulators (one per epilogue warp group)
+    constexpr bool FPAIR = AMODE == kAWinFold3 && BN == 128;
     // its tap loops' length (the kernel's code size matters: see kAWinFold3)
     constexpr int FKW = AMODE == kAWinFold3 ? kFold3MaxK : kFoldMaxKW;
     constexpr int FKH = AMODE == kAWinFold3 ? kFold3MaxK : kFoldMaxKH;
@@ -630,16 +634,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t echunk = 0;  // staged chunks so far (double-buffered staging alternates)
         int bias_n0 = -1;
         Ring ar;  // accumulator index and the parity of its current use
-        for (int tile = t_first; tile < total_tiles; tile += t_step, ++lt, ar.next(NACC)) {
+        for (int tile = t_first; tile < total_tiles;
+             tile += t_step, ++lt, ar.next(FPAIR ? NACC / 2 : NACC)) {
             // folded window: warps 0-3 take the even tiles, 4-7 the odd ones (measured
             // on the 32-channel 3x3 layer at 150x150: 144 -> 124 us against both
-            // groups converting half of every tile's channels)
-            if (FOLD && (lt & 1u) != static_cast<uint32_t>(half)) continue;
+            // groups converting half of every tile's channels); in units of two
+            // tiles, warp group h takes half h of every unit
+            if (FOLD && !FPAIR && (lt & 1u) != static_cast<uint32_t>(half)) continue;
             const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
-            const uint32_t acc = ar.stage;
+            const uint32_t acc = FPAIR ? 2u * ar.stage + static_cast<uint32_t>(half) : ar.stage;
             // tcgen05.ld below is warp-collective: the whole warp proceeds or unwinds,
             // and with the TMA store all four warps do (they share named barriers).
-            bool ready = __all_sync(0xffffffffu, wait_bar(&tfull[acc], ar.phase, wc, kRoleEpilogue));
+            bool ready = __all_sync(0xffffffffu, wait_bar(&tfull[FPAIR ? ar.stage : acc], ar.phase,
+                                                          wc, kRoleEpilogue));
             if (tma_store) {
                 if (lane == 0) sVote[warp] = ready ? 1u : 0u;
                 ptx::named_barrier_sync(1, kEpiN);
@@ -662,7 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t nhb, k, n, hb;
                 p.fold_spr_div.divmod(static_cast<uint32_t>(u.m0), nhb, k);
                 p.fold_hb_div.divmod(nhb, n, hb);
-                const int ho = static_cast<int>(hb) * kFoldRows + quad;
+                const int ho = (FPAIR ? static_cast<int>(hb) * 2 + half : static_cast<int>(hb)) *
+                                   kFoldRows + quad;
                 const int wo = static_cast<int>(k) * p.fold_g + lane;
                 const bool live = ho < p.fold_hout && lane < p.fold_g && wo < p.win_wout;
                 const int c0 = min(max(static_cast<int>(k) * p.fold_g - p.win_pad, 0), p.x_W - 32);
@@ -1486,14 +1494,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring ring;
             bool ok = receive();  // resident weights (or nothing to wait for)
             Ring ar;
-            for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
+            for (int tile = t_first; ok && tile < total_tiles;
+                 tile += t_step, ar.next(FPAIR ? C::kAcc / 2 : C::kAcc)) {
                 const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 const uint32_t acc = ar.stage;
                 // accumulator drained by the epilogue (the folded window: handed over
                 // together with its one stage below)
                 if (!FOLD && !receive()) break;
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                // (units of two tiles: accumulators 2*acc and 2*acc + 1)
+                const uint32_t d_tmem = tmem_base + (FPAIR ? 2u * acc : acc) * BN;
                 // window mode: (kh, cc) of the K block, walked instead of divided
                 int win_kh = 0, win_cc = 0;
                 if (WINDOW && u.kb0 != 0) {  // split K only
@@ -1566,15 +1576,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 static_cast<uint32_t>(p.win_d * kFoldRowBytes) >> 4;
                             const uint32_t b_kh_step = static_cast<uint32_t>(p.fold_n * 64) >> 4;
 #pragma unroll
-                            for (int kh = 0; kh < FKH; ++kh)
-                                if (kh < p.x_KH) {
+                            for (int h = 0; h < (FPAIR ? 2 : 1); ++h)
 #pragma unroll
-                                    for (int kk = 0; kk < 2; ++kk)
-                                        mma_issue<PAIR>(d_tmem,
-                                                        ad + static_cast<uint32_t>(kh) * a_kh_step + 2 * kk,
-                                                        b_desc0 + static_cast<uint32_t>(kh) * b_kh_step + 2 * kk,
-                                                        idesc, (kh != 0 || kk != 0) ? 1u : 0u);
-                                }
+                                for (int kh = 0; kh < FKH; ++kh)
+                                    if (kh < p.x_KH) {
+#pragma unroll
+                                        for (int kk = 0; kk < 2; ++kk)
+                                            mma_issue<PAIR>(
+                                                d_tmem + static_cast<uint32_t>(h * BN),
+                                                ad + static_cast<uint32_t>(h * kFoldRows * kFoldRowBytes >> 4) +
+                                                    static_cast<uint32_t>(kh) * a_kh_step + 2 * kk,
+                                                b_desc0 + static_cast<uint32_t>(kh) * b_kh_step + 2 * kk,
+                                                idesc, (kh != 0 || kk != 0) ? 1u : 0u);
+                                    }
                         } else {
                             const uint64_t bd =
                                 b_desc0 + (bres ? static_cast<uint32_t>(kb) : ring.stage) * b_blk_step;
@@ -1629,14 +1643,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (the staged-window stem's weights are ready once packed: wpack)
             bool ok = send(!bres || waited(STEMWIN ? wpack : bres_full, 0u, false));
             Ring ar;
-            for (int tile = t_first; ok && tile < total_tiles; tile += t_step, ar.next(C::kAcc)) {
+            for (int tile = t_first; ok && tile < total_tiles;
+                 tile += t_step, ar.next(FPAIR ? C::kAcc / 2 : C::kAcc)) {
                 const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 // (the folded window: one hand-off per tile, the accumulator and the
-                // stage together)
+                // stage together; in units of two tiles both accumulators)
                 if (!FOLD && !send(waited(&tempty[ar.stage], ar.phase ^ 1u, PAIR))) break;
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
                     bool good = !GATHER || waited(&full_a[ring.stage], ring.phase, false);
-                    if (FOLD) good = waited(&tempty[ar.stage], ar.phase ^ 1u, false);
+                    if (FOLD)
+                        good = FPAIR ? waited(&tempty[2 * ar.stage], ar.phase ^ 1u, false) &&
+                                           waited(&tempty[2 * ar.stage + 1], ar.phase ^ 1u, false)
+                                     : waited(&tempty[ar.stage], ar.phase ^ 1u, false);
                     if (good && (!GATHER || !bres))
                         good = waited(&full_b[ring.stage], ring.phase, false);
                     if (!send(good)) {
@@ -1853,7 +1871,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int c0 =
                                 min(max(static_cast<int>(k) * p.fold_g - p.win_pad, 0), p.x_W - 32);
                             ptx::tma_load_4d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage], 0,
-                                             c0, static_cast<int>(hb) * kFoldRows - p.win_pad,
+                                             c0, static_cast<int>(hb) * (FPAIR ? 2 * kFoldRows : kFoldRows) -
+                                                     p.win_pad,
                                              static_cast<int>(n));
                         } else if (IM2WIN) {
                             ptx::tma_load_3d(sA + ring.stage * AST, &tmap_a, &full_b[ring.stage],
@@ -1980,6 +1999,8 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
     constexpr bool kPairMode = AMODE == kAWindowPair || AMODE == kATmaGatherPair;
     constexpr bool kFold = is_fold(AMODE);
     constexpr int kFKW = AMODE == kAWinFold3 ? kFold3MaxK : kFoldMaxKW;
+    constexpr bool kFPair = AMODE == kAWinFold3 && BN == 128;  // units of two tiles
+    constexpr int kFU = kFPair ? 2 * kFoldRows : kFoldRows;     // output rows per unit
     constexpr int kFKH = AMODE == kAWinFold3 ? kFold3MaxK : kFoldMaxKH;
     const int smem =
         kPlane ? plane_smem_bytes(BN, p.stages, p.a_stage_bytes, p.bres ? p.kb_total : p.b_stages,
@@ -2028,11 +2049,11 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
                         p.fold_n <= BN && p.win_kw >= 1 && p.win_kw <= kFKW &&
                         p.x_KH >= 1 && p.x_KH <= kFKH && p.win_d >= 1 && p.x_W >= 32 &&
                         p.fold_g == 32 - (p.win_kw - 1) * p.win_d && p.fold_g >= 1 &&
-                        p.a_stage_bytes == (kFoldRows + (p.x_KH - 1) * p.win_d) * kFoldRowBytes &&
-                        kFoldRows + (p.x_KH - 1) * p.win_d <= 256 && p.num_kb == 1 &&
+                        p.a_stage_bytes == (kFU + (p.x_KH - 1) * p.win_d) * kFoldRowBytes &&
+                        kFU + (p.x_KH - 1) * p.win_d <= 256 && p.num_kb == 1 &&
                         p.fold_bbytes >= p.x_KH * p.fold_n * 64 && p.fold_bbytes % 1024 == 0 &&
                         p.bres == 1 && p.n_tiles == 1 && p.splits == 1 && !p.sk && !p.tma_store &&
-                        p.stages == Cfg<BN>::kAcc &&
+                        p.stages == (kFPair ? Cfg<BN>::kAcc / 2 : Cfg<BN>::kAcc) &&
                         p.fold_hout >= 1 && p.m_tiles >= 1 && p.m_step == 1;
         if (!ok) return cudaErrorInvalidValue;
     }

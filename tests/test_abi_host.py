@@ -142,7 +142,9 @@ def test_winfold_selection_and_plan(lib):
     assert (pl["path"], pl["a_mode"], pl["segment_outputs"], pl["tile_rows"]) == (8, 17, 30, 0)
     # 5x5: the instantiation with tap loops for up to 7 x 5
     assert lib.plan_info(128, 32, 150, 150, 32, 5, 5, 1, 2, 1)["a_mode"] == 16
-    assert pl["m_tiles"] == 128 * 38 * 5 and pl["k_blocks"] == 1  # 4-row blocks x segments
+    # 8-row units (3x3, 96-column MMA) x segments
+    assert pl["segment_rows"] == 8
+    assert pl["m_tiles"] == 128 * 19 * 5 and pl["k_blocks"] == 1
     assert pl["weights_resident"] == 1 and pl["splits"] == 1 and pl["tma_store"] == 0
     assert lib.workspace_size(128, 32, 150, 150, 32, 3, 3, 1, 1, 1) == 0
     # rows narrower than a 32-pixel segment stay on the gather path
@@ -176,13 +178,15 @@ def test_winfold_plan_geometry(lib, geom):
     Ho = oracle.output_size(H, KH, 1, p, d)
     Wo = oracle.output_size(W, KW, 1, p, d)
     G = 32 - (KW - 1) * d
-    assert pl["segment_outputs"] == G and pl["tile_rows"] == 0
-    assert pl["m_tiles"] == N * -(-Ho // 4) * -(-Wo // G)
+    U = 8 if KH <= 3 and KW <= 3 and KW * C_out <= 128 else 4
+    assert pl["segment_outputs"] == G and pl["tile_rows"] == 0 and pl["segment_rows"] == U
+    assert pl["m_tiles"] == N * -(-Ho // U) * -(-Wo // G)
     assert pl["n_tiles"] == 1 and pl["splits"] == 1 and pl["k_blocks"] == 1
     assert pl["bn"] == (128 if KW * C_out <= 128 else 256)
     assert pl["a_mode"] == (17 if KH <= 3 and KW <= 3 else 16)
-    # one stage per accumulator slot: four of 128 columns or two of 256
-    assert pl["stages"] == (4 if pl["bn"] == 128 else 2)
+    # one stage per accumulator slot: four of 128 columns or two of 256, or two
+    # pairs of 128 for 8-row units
+    assert pl["stages"] == (2 if U == 8 else 4 if pl["bn"] == 128 else 2)
     if lib.select_path(N, 32, H, W, C_out, KH, KW, 1, p, d) == lib.PATH_WINFOLD:
         assert lib.workspace_size(N, 32, H, W, C_out, KH, KW, 1, p, d) == 0
 

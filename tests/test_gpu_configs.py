@@ -42,18 +42,19 @@ def border_points(shape, Ho, Wo):
 def fold_tile_points(shape, plan, Ho, Wo, rng, per_tile=PER_TILE):
     """Folded-window plans: tile t = (n*HB + hb)*spr + k holds output pixels
     k*G .. k*G + G - 1 (G = segment_outputs, spr segments per row, the last one
-    shorter) of output rows 4*hb .. 4*hb + 3 (HB = ceil(H_out / 4) row blocks).
-    per_tile / 4 (at least one) random outputs in each of a tile's rows."""
-    G = plan["segment_outputs"]
+    shorter) of output rows U*hb .. U*hb + U - 1 (U = segment_rows, HB =
+    ceil(H_out / U) row blocks).  per_tile / 4 (at least one) random outputs in
+    each of a tile's rows."""
+    G, U = plan["segment_outputs"], plan["segment_rows"]
     spr = -(-Wo // G)
-    HB = -(-Ho // 4)
+    HB = -(-Ho // U)
     assert plan["m_tiles"] == shape.N * HB * spr, plan
     per_row = max(1, per_tile // 4)
-    t = np.repeat(np.arange(plan["m_tiles"], dtype=np.int64), 4 * per_row)
-    q = np.tile(np.repeat(np.arange(4, dtype=np.int64), per_row), plan["m_tiles"])
+    t = np.repeat(np.arange(plan["m_tiles"], dtype=np.int64), U * per_row)
+    q = np.tile(np.repeat(np.arange(U, dtype=np.int64), per_row), plan["m_tiles"])
     nhb, k = np.divmod(t, spr)
     n, hb = np.divmod(nhb, HB)
-    ho = hb * 4 + q
+    ho = hb * U + q
     keep = ho < Ho
     t, k, n, ho = t[keep], k[keep], n[keep], ho[keep]
     span = np.minimum(Wo, (k + 1) * G) - k * G
