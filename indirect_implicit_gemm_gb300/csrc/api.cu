@@ -711,7 +711,12 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         g.win_wv = c.W_out + (c.KW - 1) * c.d;
         g.win_rows = 128 / g.win_wv;
         g.m_step = g.win_rows;
-        g.a_stage_bytes = window_stage_rows(c.KW, c.d) * 128;
+        // A slot = the staged rows only; the MMAs' reads past them (for discarded
+        // outputs) land in the next slot or, after the last, in a pad of
+        // extra_smem bytes.  On the 64->128 3x3 layer at 56x56 this makes room
+        // for a fourth slot beside 144 KB of resident weights.
+        g.a_stage_bytes = (g.win_rows * g.win_wv * 128 + 1023) / 1024 * 1024;
+        g.extra_smem = std::max(0, window_stage_rows(c.KW, c.d) * 128 - g.a_stage_bytes);
         g.num_kb = c.KH * (c.C_in / 64);  // one K block per (kh, 64-channel block)
         g.m_tiles = (int)(((long long)c.N * c.H_out + g.win_rows - 1) / g.win_rows);
         g.bn = pick_bn(c.C_out);
@@ -724,25 +729,27 @@ GemmPlan plan_gemm_ring(int path, const ConvShape& c)
         // resident on one CTA, as on the 64->128 layer, the pair is slower).
         const int all_kb = c.KH * c.KW * (c.C_in / 64);
         const bool solo_bres =
-            g.n_tiles == 1 && igemm_pick_stages(g.bn, 1, all_kb, g.a_stage_bytes, 1) >= 3;
+            g.n_tiles == 1 &&
+            igemm_pick_stages(g.bn, 1, all_kb, g.a_stage_bytes, 1, g.extra_smem) >= 3;
         g.pair = (g.m_tiles >= 2 && (g.bn == 256 || (g.bn == 128 && !solo_bres))) ? 1 : 0;
         auto bnb = [&] { return g.pair ? g.bn / 2 : g.bn; };
-        if (g.n_tiles == 1 && igemm_pick_stages(bnb(), 1, all_kb, g.a_stage_bytes, 1) >= 3) {
+        if (g.n_tiles == 1 &&
+            igemm_pick_stages(bnb(), 1, all_kb, g.a_stage_bytes, 1, g.extra_smem) >= 3) {
             g.bres = 1;
             g.b_per_stage = 1;
-            g.stages = igemm_pick_stages(bnb(), 1, all_kb, g.a_stage_bytes, 1);
+            g.stages = igemm_pick_stages(bnb(), 1, all_kb, g.a_stage_bytes, 1, g.extra_smem);
         } else {
             // Streamed weights: a slot holds the KW blocks of one (kh, cc).  A
             // 256-wide column tile only on a pair with three slots beside the
             // epilogue's staging tile; otherwise 128 so that enough slots fit.
             if (g.bn > 128 && !(g.pair && igemm_pick_stages(g.bn / 2, 0, 0, g.a_stage_bytes, c.KW,
-                                                            kEpiStageBytes) >= 3)) {
+                                                            g.extra_smem + kEpiStageBytes) >= 3)) {
                 g.bn = 128;
                 g.n_tiles = (c.C_out + 127) / 128;
                 g.pair = 0;
             }
             g.b_per_stage = c.KW;
-            g.stages = igemm_pick_stages(bnb(), 0, 0, g.a_stage_bytes, c.KW);
+            g.stages = igemm_pick_stages(bnb(), 0, 0, g.a_stage_bytes, c.KW, g.extra_smem);
         }
         if (g.pair) g.amode = kAWindowPair;
         const long long im2col = c.M * c.K * 2;
@@ -1174,6 +1181,7 @@ convgb_status prepare_gemm(const GemmPlan& g, const IgemmArgs& a, PreparedGemm* 
         p.win_d = c.d;
         p.win_pad = c.p;
         p.win_cc = c.C_in / 64;
+        p.win_tail = g.extra_smem;
         p.ho_div = FastDiv((uint32_t)c.H_out);
         p.x_H = c.H;
         p.x_W = c.W;

@@ -478,7 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kTmemAlloc = PLANE ? 512u : static_cast<uint32_t>(C::kTmemCols);
     // (the folded window's resident weights: KH blocks of KW*C_out 64-byte rows)
     uint8_t* sA = data + (FOLD ? static_cast<uint32_t>(p.fold_bbytes) : b_blocks * BB);
-    uint8_t* sStg = sA + S * AST;  // narrow window: nw_slots slots of staged input rows
+    // narrow window: nw_slots slots of staged input rows; window: the pad that the
+    // last A slot's reads past its staged rows fall into
+    uint8_t* sStg = sA + S * AST + (WINDOW ? static_cast<uint32_t>(p.win_tail) : 0u);
     const uint32_t NS = STAGEDROWS ? static_cast<uint32_t>(p.nw_slots) : 1u;
     // TMA-store epilogue: a 128 x 64 bf16 staging tile (128-byte swizzle) and the
     // current column tile's bias in fp32.
@@ -1991,6 +1993,7 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         }
     }
     const int extra = ((AMODE == kANarrowWin || is_stemwin(AMODE)) ? p.nw_slots * p.nw_slot_bytes
+                       : is_window(AMODE)                           ? p.win_tail
                                                                     : 0) +
                       (p.tma_store ? (p.epi_c32 ? kEpiNarrowStageBytes + (p.epi_bufs - 1) * kEpiNarrowTileBytes
                                                 : kEpiStageBytes + (p.epi_bufs - 1) * kEpiTileBytes)
@@ -2032,6 +2035,15 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
             p.sw_wbytes > p.stages * p.a_stage_bytes || p.sw_wbytes % 16 != 0 ||
             p.kb_total != p.num_kb * p.sw_nkb || p.sw_last < 1 || p.sw_last > 4 ||
             p.sw_steps != (p.sw_nkb - 1) * 4 + p.sw_last || p.sw_steps > kStemWinMaxSteps)
+            return cudaErrorInvalidValue;
+    }
+    if (is_window(AMODE)) {
+        // every MMA read of an A slot (128 + (KW-1)*d rows of 128 bytes from the
+        // slot's start) stays inside the ring and its pad, and the staged rows fit
+        // a slot; slots and pad keep the staging tile 1024-byte aligned
+        if (p.win_tail < 0 || p.win_tail % 1024 != 0 || p.a_stage_bytes % 1024 != 0 ||
+            p.win_rows < 1 || p.win_rows * p.win_wv * 128 > p.a_stage_bytes ||
+            (BM + (p.win_kw - 1) * p.win_d) * 128 > p.a_stage_bytes + p.win_tail)
             return cudaErrorInvalidValue;
     }
     if (AMODE == kAWindowT &&

@@ -70,6 +70,10 @@ struct IgemmParams {
     // window mode (stride 1): tile = win_rows output rows of win_wv virtual
     // pixels (W_out real + (KW-1)*d spill); K block kb = (kh, cc)
     int win_wv, win_rows, win_groups, win_wout, win_kw, win_d, win_pad, win_cc;
+    // window mode: bytes after the last A slot that its MMAs may still read (an
+    // A slot holds the win_rows * win_wv staged rows; the MMAs read 128 + (KW-1)*d
+    // rows from it, the ones past the staged rows only for discarded outputs)
+    int win_tail;
     FastDiv ho_div;          // divides an output-row index (n*H_out + ho) by H_out
     int x_H, x_W, x_KH;      // window mode: input geometry (L2 prefetch of input rows)
     int st_s;                // strided 1x1 mode: the stride
@@ -217,7 +221,8 @@ int igemm_smem_bytes(int bn, int stages, int bres, int num_kb, int a_stage_bytes
                      int b_per_stage, int extra_bytes = 0);
 int igemm_pick_stages(int bn, int bres, int num_kb, int a_stage_bytes, int b_per_stage,
                       int extra_bytes = 0);
-// Rows of an A ring slot in window mode (128 plus the tap spill, rounded to 8).
+// Rows that window-mode MMAs read from an A ring slot (128 plus the tap spill,
+// rounded to 8).
 int window_stage_rows(int kw, int d);
 // Dynamic shared memory of a folded-window CTA: resident weights of b_bytes
 // (a multiple of 1024), `stages` A stages and the fp32 bias.
