@@ -854,17 +854,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
                 if (tma_store) {
-#pragma unroll 1
-                    for (int c64 = 0; c64 < BN / 64; ++c64) {
-                        uint32_t ra[32], rb[32];
-                        if (EPI8) {
-                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + half * 32, ra);
-                        } else {
-                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
-                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
-                        }
-                        ptx::tmem_ld_wait();
-                        if (last_sub && c64 + 1 == BN / 64) release_acc(acc);
+                    // One 64-column chunk from registers (ra, and rb for the second
+                    // 32 columns with four warps) through the staging tile to y.
+                    auto stage_store = [&](int c64, const uint32_t* ra, const uint32_t* rb) {
                         // The staging tile is free once the store that last used it
                         // has read it: the previous chunk's, or with two tiles the one
                         // before.
@@ -931,6 +923,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             ptx::bulk_commit_group();
                         }
+                    };
+                    if (EPI8 && BN == 128) {
+                        // Both chunks' TMEM loads at once: one load latency per tile,
+                        // and the accumulator goes back to the MMA thread before the
+                        // conversions start.
+                        uint32_t r0[32], r1[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + half * 32, r0);
+                        ptx::tmem_ld_32x32b_x32(taddr + 64 + half * 32, r1);
+                        ptx::tmem_ld_wait();
+                        if (last_sub) release_acc(acc);
+                        stage_store(0, r0, r0);
+                        stage_store(1, r1, r1);
+                        continue;
+                    }
+#pragma unroll 1
+                    for (int c64 = 0; c64 < BN / 64; ++c64) {
+                        uint32_t ra[32], rb[32];
+                        if (EPI8) {
+                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + half * 32, ra);
+                        } else {
+                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
+                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
+                        }
+                        ptx::tmem_ld_wait();
+                        if (last_sub && c64 + 1 == BN / 64) release_acc(acc);
+                        stage_store(c64, ra, rb);
                     }
                     continue;
                 }
