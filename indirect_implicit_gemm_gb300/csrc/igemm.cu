@@ -935,20 +935,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (last_sub) release_acc(acc);
                         stage_store(0, r0, r0);
                         stage_store(1, r1, r1);
-                        continue;
-                    }
+                    } else {
 #pragma unroll 1
-                    for (int c64 = 0; c64 < BN / 64; ++c64) {
-                        uint32_t ra[32], rb[32];
-                        if (EPI8) {
-                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + half * 32, ra);
-                        } else {
-                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
-                            ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
+                        for (int c64 = 0; c64 < BN / 64; ++c64) {
+                            uint32_t ra[32], rb[32];
+                            if (EPI8) {
+                                ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + half * 32, ra);
+                            } else {
+                                ptx::tmem_ld_32x32b_x32(taddr + c64 * 64, ra);
+                                ptx::tmem_ld_32x32b_x32(taddr + c64 * 64 + 32, rb);
+                            }
+                            ptx::tmem_ld_wait();
+                            if (last_sub && c64 + 1 == BN / 64) release_acc(acc);
+                            stage_store(c64, ra, rb);
                         }
-                        ptx::tmem_ld_wait();
-                        if (last_sub && c64 + 1 == BN / 64) release_acc(acc);
-                        stage_store(c64, ra, rb);
                     }
                     continue;
                 }
