@@ -1546,9 +1546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                  tile += t_step, ar.next(FPAIR ? C::kAcc / 2 : C::kAcc)) {
                 const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 const uint32_t acc = ar.stage;
-                // accumulator drained by the epilogue (the folded window: handed over
-                // together with its one stage below)
-                if (!FOLD && !receive()) break;
+                // accumulator drained by the epilogue (the folded window and the
+                // fixed-plan window kernel: handed over with the first stage below)
+                if (!FOLD && !WT && !receive()) break;
                 ptx::tc_fence_after();
                 // (units of two tiles: accumulators 2*acc and 2*acc + 1)
                 const uint32_t d_tmem = tmem_base + (FPAIR ? 2u * acc : acc) * BN;
@@ -1695,10 +1695,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                  tile += t_step, ar.next(FPAIR ? C::kAcc / 2 : C::kAcc)) {
                 const Unit u = unit_of<BN, PAIR, SKM>(p, tile, rank, skr);
                 // (the folded window: one hand-off per tile, the accumulator and the
-                // stage together; in units of two tiles both accumulators)
-                if (!FOLD && !send(waited(&tempty[ar.stage], ar.phase ^ 1u, PAIR))) break;
+                // stage together; in units of two tiles both accumulators.  The
+                // fixed-plan window kernel hands the accumulator over with the
+                // tile's first K block: each hand-off leaves the MMA thread idle
+                // for ~200 cycles, which the tensor core does not hide)
+                bool acc_ok = true;
+                if (WT)
+                    acc_ok = waited(&tempty[ar.stage], ar.phase ^ 1u, PAIR);
+                else if (!FOLD && !send(waited(&tempty[ar.stage], ar.phase ^ 1u, PAIR)))
+                    break;
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ring.next(S)) {
-                    bool good = !GATHER || waited(&full_a[ring.stage], ring.phase, false);
+                    bool good = (!WT || kb != u.kb0 || acc_ok) &&
+                                (!GATHER || waited(&full_a[ring.stage], ring.phase, false));
                     if (FOLD)
                         good = FPAIR ? waited(&tempty[2 * ar.stage], ar.phase ^ 1u, false) &&
                                            waited(&tempty[2 * ar.stage + 1], ar.phase ^ 1u, false)
