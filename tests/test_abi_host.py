@@ -159,6 +159,24 @@ def test_winfold_selection_and_plan(lib):
         lib.plan_info(4, 32, 40, 40, 128, 3, 3, 1, 1, 1, path=lib.PATH_WINFOLD)
 
 
+def test_window_plans_ring_depth(lib):
+    # A window A slot holds only the staged rows (two boxes of 58 pixels on the
+    # 64 -> 128 3x3 layer at 56x56) rather than every row the MMAs read, so a
+    # fourth slot fits beside the 144 KB of resident weights; the fixed-plan
+    # kernel (resident weights, TMA-store epilogue in 64-column chunks) runs it.
+    pl = lib.plan_info(32, 64, 56, 56, 128, 3, 3, 1, 1, 1)
+    assert (pl["path"], pl["a_mode"], pl["bn"], pl["cta_pair"]) == (lib.PATH_WINDOW, 18, 128, 0)
+    assert (pl["stages"], pl["weights_resident"], pl["tma_store"], pl["epilogue_c32"]) == (4, 1, 1, 0)
+    assert (pl["tile_rows"], pl["m_tiles"], pl["k_blocks"]) == (112, 32 * 56 // 2, 3)
+    # 128 channels at 56x56: a CTA pair with weight halves resident keeps four
+    # slots with the full 64-column staging tile
+    pl = lib.plan_info(128, 128, 56, 56, 128, 3, 3, 1, 1, 1)
+    assert (pl["a_mode"], pl["cta_pair"], pl["stages"], pl["epilogue_c32"]) == (9, 1, 4, 0)
+    # a one-row tile (W_out = 112) with 72 KB of weights: the ring's cap
+    pl = lib.plan_info(128, 64, 112, 112, 64, 3, 3, 1, 1, 1)
+    assert (pl["a_mode"], pl["bn"], pl["tile_rows"]) == (18, 64, 112) and pl["stages"] >= 7
+
+
 FOLD_GEOMS = [  # (N, H, W, C_out, KH, KW, pad, dilation)
     (1, 32, 32, 32, 3, 3, 1, 1), (3, 37, 45, 64, 3, 3, 1, 1), (2, 20, 70, 32, 5, 5, 2, 1),
     (1, 16, 40, 32, 7, 5, 3, 1), (2, 12, 33, 32, 3, 3, 2, 2), (4, 9, 64, 96, 3, 1, 1, 1),
