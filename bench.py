@@ -181,6 +181,23 @@ def profiled_traffic(workload):
     return None
 
 
+def sweep_summary(sweep):
+    """The per-configuration results as they ride on the headline line: one
+    short entry per workload (path, us, TFLOP/s, fraction of its roofline and
+    what bounds it, workspace bytes), so the line stays a few KB; each full
+    entry is printed on its own `sweep` line ahead of the headline line."""
+    out = {}
+    for ent in sweep:
+        if "error" in ent:
+            out[ent["workload"]] = {"error": ent["error"][:80]}
+            continue
+        out[ent["workload"]] = {"path": ent["path"], "us": round(ent["us"], 2),
+                                "tflops": round(ent["tflops"], 1),
+                                "frac": round(ent["frac_of_roofline"], 3), "bound": ent["bound"],
+                                "ws_B": ent["workspace_bytes"]}
+    return out
+
+
 def roofline_time_s(num, peaks):
     t_tc = num["flops"] / (peaks["bf16_tflops"] * 1e12)
     t_hbm = num["bytes"] / (peaks["hbm_gbs"] * 1e9)
@@ -782,7 +799,7 @@ def main():
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": layer.launches_per_step() * args.steps,
         "single_launch": single,
-        "clocks": clocks, "sweep": sweep,
+        "clocks": clocks, "sweep": sweep_summary(sweep),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

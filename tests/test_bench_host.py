@@ -87,3 +87,25 @@ def test_source_hash_ignores_comments_only():
     assert bench.strip_comments(src.replace("trailing", "other words")) == bench.strip_comments(src)
     assert bench.strip_comments(src.replace("int a = 1", "int a = 2")) != bench.strip_comments(src)
     assert len(bench.kernel_source_hash()) == 64
+
+
+def test_sweep_summary_keeps_every_workload_and_stays_short():
+    # the sweep entries of a recorded benchmark run, one per workload, as the
+    # headline line carries them: every workload present, a few KB in all
+    import json
+    import bench
+    import workloads
+    full = []
+    for i, c in enumerate(workloads.ALL):
+        full.append({"workload": c.name, "path": "window", "us": 10.0 + i / 3, "tflops": 900.123456,
+                     "gbs": 2000.5, "bound": "tensor", "roofline_us": 7.9, "frac_of_roofline": 0.5123456,
+                     "workspace_bytes": 0, "im2col_bytes": 115605504, "im2win_bytes": 1,
+                     "gemm_kernel_us": 9.9, "gemm_frac_of_roofline": 0.6, "im2win_us": 5.0,
+                     "im2win_gbs": 2528.8, "im2win_frac_hbm": 0.37})
+    full[3] = {"workload": workloads.ALL[3].name, "error": "x" * 300}
+    s = bench.sweep_summary(full)
+    assert list(s) == [c.name for c in workloads.ALL]
+    assert s[workloads.ALL[0].name] == {"path": "window", "us": 10.0, "tflops": 900.1, "frac": 0.512,
+                                        "bound": "tensor", "ws_B": 0}
+    assert len(s[workloads.ALL[3].name]["error"]) == 80
+    assert len(json.dumps(s)) < 3000 < len(json.dumps(full))
