@@ -177,6 +177,65 @@ def test_window_plans_ring_depth(lib):
     assert (pl["a_mode"], pl["bn"], pl["tile_rows"]) == (18, 64, 112) and pl["stages"] >= 7
 
 
+def _window_smem_bytes(pl, shape):
+    """Dynamic shared memory of a window-mode CTA, rebuilt from the plan's
+    visible fields: header and alignment, B blocks (all of them when resident,
+    KW per ring slot otherwise; half the columns on a CTA pair), the A slots of
+    the staged rows, the pad that the last slot's reads of 128 + (KW-1)*d rows
+    fall into, and the epilogue's staging tiles with the fp32 bias."""
+    N, C_in, H, W, C_out, KH, KW, s, p, d = shape
+    W_out = (W + 2 * p - (KW - 1) * d - 1) // s + 1
+    wv = W_out + (KW - 1) * d
+    rows = 128 // wv
+    slot = -(-rows * wv * 128 // 1024) * 1024
+    read = -(-(128 + (KW - 1) * d) // 8) * 8 * 128
+    pad = max(0, read - slot)
+    bnb = pl["bn"] // 2 if pl["cta_pair"] else pl["bn"]
+    b_blocks = KH * KW * C_in // 64 if pl["weights_resident"] else pl["stages"] * KW
+    if not pl["tma_store"]:
+        epi = 0
+    elif pl["epilogue_c32"]:
+        epi = 8192 + 1024 + (pl["epilogue_tiles"] - 1) * 8192
+    else:
+        epi = 16384 + 1024 + (pl["epilogue_tiles"] - 1) * 16384
+    return 512 + 1024 + b_blocks * bnb * 128 + pl["stages"] * slot + pad + epi, rows, W_out
+
+
+def test_window_plans_fit_shared_memory(lib):
+    # seeded random stride-1 shapes with C_in % 64 == 0: every plan the library
+    # makes on the window path fits the 227 KB a CTA may hold, with its ring of
+    # 2..8 slots and its tiles of whole output rows
+    import random
+    # the formula against a measured launch: ncu reports 229,888 bytes of dynamic
+    # shared memory for the 64 -> 128 3x3 layer at 56x56 (four slots of 15 KB,
+    # a 2 KB pad, 144 KB of weights, one staging tile)
+    head = (32, 64, 56, 56, 128, 3, 3, 1, 1, 1)
+    assert _window_smem_bytes(lib.plan_info(*head), head)[0] == 229888
+    rng = random.Random(2024)
+    seen, checked = set(), 0
+    for _ in range(400):
+        KH, KW = rng.choice([1, 2, 3, 5, 7]), rng.choice([2, 3, 5, 7])
+        d = rng.choice([1, 1, 2])
+        shape = (rng.choice([1, 2, 8, 32]), rng.choice([64, 128, 192, 256, 512]),
+                 rng.randint(KH * d, 60), rng.randint(KW * d, 120),
+                 rng.choice([32, 64, 96, 128, 192, 256, 384, 512]), KH, KW, 1,
+                 rng.randint(0, (KW - 1) * d // 2 + 1), d)
+        N, C_in, H, W, C_out = shape[:5]
+        if lib.select_path(N, C_in, H, W, C_out, KH, KW, 1, shape[8], d) != lib.PATH_WINDOW:
+            continue
+        pl = lib.plan_info(*shape)
+        if pl["a_mode"] not in (4, 9, 18):
+            continue
+        seen.add(pl["a_mode"])
+        checked += 1
+        smem, rows, W_out = _window_smem_bytes(pl, shape)
+        assert smem <= 232448, (shape, pl, smem)
+        assert 2 <= pl["stages"] <= 8, (shape, pl)
+        assert pl["tile_rows"] == rows * W_out, (shape, pl)
+        assert pl["k_blocks"] == KH * C_in // 64, (shape, pl)
+    assert seen == {4, 9, 18} and checked >= 60, (seen, checked)
+
+
 FOLD_GEOMS = [  # (N, H, W, C_out, KH, KW, pad, dilation)
     (1, 32, 32, 32, 3, 3, 1, 1), (3, 37, 45, 64, 3, 3, 1, 1), (2, 20, 70, 32, 5, 5, 2, 1),
     (1, 16, 40, 32, 7, 5, 3, 1), (2, 12, 33, 32, 3, 3, 2, 2), (4, 9, 64, 96, 3, 1, 1, 1),
